@@ -1,0 +1,442 @@
+#!/usr/bin/env python
+"""Benchmark of the L³ layer on B300: one JSON line on stdout (rank 0).
+
+Workload (default): the bf16 prefill batch — vocab 32768, v 262144 table rows, d 1024,
+d_v 256, T 8192 tokens (4 x 2048) with Zipf(1.1) ids, rows per id from the Zipf^0.7 rule
+capped at k = 512. A step is one l3_forward over the batch (route, gather-attend,
+GEMM-up + LayerNorm statistics, GEMM-mix); inputs are resident in HBM and L2 is flushed
+(a 256 MB write) before every timed step, outside its events. `e2e` times the same
+forward through l3_forward_host from pinned host buffers, copies included.
+
+Multi-GPU (torchrun): every rank runs an independent batch (its own token seed) on its
+own GPU with no collective on the data path; the timed region is bracketed by barriers,
+the time is the max over ranks, and value = all ranks' tokens / that time (weak scaling).
+
+`--impl reference` times the CPU fp64 oracle on bounded samples of the same workload
+(rank 0 only), the reference arm for this library.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import l3_workloads as W  # noqa: E402
+
+METRIC = "L^3 layer tokens/sec (fwd, fwd+bwd) on 1 B300; HBM GB/s vs ~8 TB/s roofline"
+FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0}
+
+
+# ---- host-side workload accounting ---------------------------------------------------------------
+
+def workload_bytes(p, ids: np.ndarray, offs: np.ndarray) -> dict:
+    """Algorithmic bytes and FLOPs of one forward over the batch (per kernel stage)."""
+    b = 2 if p.dtype == "bf16" else 4
+    uniq = np.unique(ids)
+    n = np.diff(offs.astype(np.int64))
+    uniq_rows = int(n[uniq].sum())
+    T = len(ids)
+    attend = uniq_rows * (p.d + p.d_v) * b + T * p.d * b + T * p.d_v * b
+    logical = int(n[ids].sum()) * (p.d + p.d_v) * b + 2 * T * p.d * b
+    return {
+        "unique_rows": uniq_rows,
+        "distinct_ids": int(len(uniq)),
+        "attend_bytes": attend,
+        "logical_bytes": logical,
+        "unique_bytes": uniq_rows * (p.d + p.d_v) * b + 2 * T * p.d * b + (p.d * p.d_v + 2 * p.d * p.d) * b,
+        "up_flops": 2 * T * p.d * p.d_v,
+        "mix_flops": 4 * T * p.d * p.d,
+    }
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return {"hbm_gbs": float(pk["hbm_gbs"]), "bf16_tflops": float(pk["bf16_tflops"]),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS, source="fallback")
+
+
+# ---- clocks --------------------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="l3clk", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        with open(self.path) as f:
+            for line in f:
+                parts = [s.strip() for s in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for nm, val in zip(names, parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(nm)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---- the CPU oracle as a baseline ------------------------------------------------------------------
+
+class _Rows:
+    """Host copy of the table rows of a set of ids, sliced like the full table."""
+
+    def __init__(self, table, offs, ids):
+        ranges = sorted({(int(offs[t]), int(offs[t + 1])) for t in set(int(i) for i in ids)})
+        rows = np.concatenate([np.arange(a, c) for a, c in ranges])
+        self.host = W.table_rows_to_numpy(table, rows)
+        self.pos, k = {}, 0
+        for a, c in ranges:
+            self.pos[(a, c)] = k
+            k += c - a
+
+    def __getitem__(self, sl):
+        k = self.pos[(sl.start, sl.stop)]
+        return self.host[k:k + sl.stop - sl.start]
+
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+
+        n = [i["num_threads"] for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return len(os.sched_getaffinity(0))
+
+
+def time_oracle(wl, offs_np, K, V, tokens) -> float:
+    """Seconds the oracle takes for the given tokens (tables rows copied to host first)."""
+    import oracle
+
+    Kh = _Rows(K, offs_np, wl.ids[tokens])
+    Vh = _Rows(V, offs_np, wl.ids[tokens])
+    t0 = time.perf_counter()
+    oracle.forward(offs_np, Kh, Vh, wl.W_up, wl.W_mix, wl.ids, wl.x, tokens=tokens)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(wl, offs_np, K, V, budget_s: float = 15.0) -> dict:
+    probe = list(range(min(16, wl.T)))
+    dt = time_oracle(wl, offs_np, K, V, probe)
+    S = int(min(wl.T, max(len(probe), budget_s * len(probe) / max(dt, 1e-6))))
+    toks = list(range(S))
+    sec = time_oracle(wl, offs_np, K, V, toks)
+    return {"value": S / sec, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"first {S} of {wl.T} tokens of the batch, fp64 numpy, one token at a time "
+                      f"({sec:.1f} s)"}
+
+
+# ---- runs -----------------------------------------------------------------------------------------
+
+def config_block(p, T, extra=None):
+    c = {"workload": f"{p.name}: vocab {p.vocab}, v {p.v}, d {p.d}, d_v {p.d_v}, T {T}, "
+                     f"k {p.k_max}, Zipf(1.1) ids, rows per id from freq^{p.power}",
+         "vocab": p.vocab, "v": p.v, "d": p.d, "d_v": p.d_v, "T": T, "k_max": p.k_max,
+         "l2": "flushed before every timed step (256 MB write outside the timed events)"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+def run_reference(args, rank):
+    if rank != 0:
+        return 0
+    import torch
+
+    p = W.PRESETS[args.config]
+    wl = W.make(args.config)
+    import oracle
+
+    offs_np = oracle.allocate(wl.freq, p.v, 1, p.k_max, p.power).offs
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    K, V = W.tables(wl, dev)
+    per_step = max(1, args.ref_tokens)
+    for w in range(args.warmup):
+        time_oracle(wl, offs_np, K, V, [w % wl.T])
+    total, toks = 0.0, 0
+    for k in range(args.steps):
+        sel = [(k * per_step + j) % wl.T for j in range(per_step)]
+        total += time_oracle(wl, offs_np, K, V, sel)
+        toks += per_step
+    value = toks / total
+    cores = blas_threads()
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_block(p, wl.T, {"sample_tokens_per_step": per_step}),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores,
+                             "kind": "oracle",
+                             "sample": f"{per_step} tokens per step of the {wl.T}-token batch"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import static_token_routed_csr_b300 as l3
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    p = W.PRESETS[args.config]
+    wl = W.make(args.config, shard=rank)
+    T = wl.T
+    offs_np = l3.l3_alloc_offsets(wl.freq, p.v, 1, p.k_max, p.power)
+    dt = W.torch_dtype(p)
+    K, V = W.tables(wl, dev)
+    offs = torch.as_tensor(offs_np, device=dev)
+    W_up = torch.as_tensor(wl.W_up, device=dev).to(dt)
+    W_mix = torch.as_tensor(wl.W_mix, device=dev).to(dt)
+    ids = torch.as_tensor(wl.ids, device=dev)
+    x = torch.as_tensor(wl.x, device=dev).to(dt)
+    y = torch.empty((T, p.d), dtype=dt, device=dev)
+    L = l3.make_layer(offs, K, V, W_up, W_mix, p.k_max)
+    ws = torch.empty(l3.l3_workspace_size(L, T, l3.L3_PASS_FORWARD), dtype=torch.uint8, device=dev)
+    l3.l3_check_layer(L, ws)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    nst = l3.L3_FWD_STAGES
+
+    def new_events():
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)]
+        for e in evs:
+            e.record()
+        return evs
+
+    evs = [new_events() for _ in range(args.steps)]
+    warm = new_events()
+    for _ in range(args.warmup):
+        flush.zero_()
+        l3.l3_forward_timed(L, ids, x, y, ws, warm)
+    torch.cuda.synchronize()
+    if l3.l3_get_error(ws) != 0:
+        raise RuntimeError("device-side error during warm-up")
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    clk = ClockSampler(local_rank)
+    barrier()
+    clk.start()
+    n0 = l3.l3_launch_count()
+    for k in range(args.steps):
+        flush.zero_()
+        l3.l3_forward_timed(L, ids, x, y, ws, evs[k])
+    barrier()
+    launches = l3.l3_launch_count() - n0
+    clocks = clk.stop()
+    step_ms = [evs[k][0].elapsed_time(evs[k][nst]) for k in range(args.steps)]
+    stage_ms = [statistics.mean(evs[k][s].elapsed_time(evs[k][s + 1]) for k in range(args.steps))
+                for s in range(nst)]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = world * T / (total_ms / 1e3)
+
+    # end to end through the host-buffer entry point
+    ws_h = torch.empty(l3.l3_workspace_size(L, T, l3.L3_PASS_FORWARD_HOST), dtype=torch.uint8,
+                       device=dev)
+    ids_h = ids.cpu().pin_memory()
+    x_h = x.cpu().pin_memory()
+    y_h = torch.empty((T, p.d), dtype=dt).pin_memory()
+    for _ in range(max(1, args.warmup)):
+        l3.l3_forward_host(L, ids_h, x_h, y_h, ws_h)
+    torch.cuda.synchronize()
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    barrier()
+    for k in range(args.steps):
+        flush.zero_()
+        e2e_ev[k][0].record()
+        l3.l3_forward_host(L, ids_h, x_h, y_h, ws_h)
+        e2e_ev[k][1].record()
+    barrier()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    if not torch.equal(y_h.to(dev), y):
+        raise RuntimeError("host-buffer forward disagrees with the device forward")
+    esz = 2 if p.dtype == "bf16" else 4
+
+    # fwd+bwd on the small fwd+bwd preset (reported beside the headline)
+    fb = fwd_bwd_rate(l3, dev, args)
+
+    if rank != 0:
+        return 0
+    acct = workload_bytes(p, wl.ids, offs_np)
+    peaks = load_peaks()
+    names = l3.STAGE_NAMES
+    dom = int(np.argmax(stage_ms))
+    dom_s = stage_ms[dom] / 1e3
+    if names[dom] in ("route", "attend"):
+        achieved = acct["attend_bytes"] / dom_s / 1e9
+        roof = {"kernel": "gather-attend", "bound": "hbm", "achieved": achieved,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                "traffic": None}
+    else:
+        flops = acct["up_flops"] if names[dom] == "up" else acct["mix_flops"]
+        achieved = flops / dom_s / 1e12
+        roof = {"kernel": "gemm-" + names[dom], "bound": "tensor", "achieved": achieved,
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"], "traffic": None}
+    roof["peak_source"] = peaks["source"]
+    attend_s = stage_ms[1] / 1e3
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": p.dtype,
+        "data": "synthetic (seeded Zipf ids, N(0,1) x, N(0,0.02^2) tables, N(0,1/fan_in) weights)",
+        "config": config_block(p, T),
+        "stage_ms": dict(zip(names, stage_ms)),
+        "attend_hbm": {"unique_gbs": acct["attend_bytes"] / attend_s / 1e9,
+                       "logical_gbs": acct["logical_bytes"] / attend_s / 1e9,
+                       "frac_of_8tbs": acct["attend_bytes"] / attend_s / 8e12,
+                       "frac_of_measured": acct["attend_bytes"] / attend_s / 1e9 / peaks["hbm_gbs"],
+                       "unique_rows": acct["unique_rows"], "distinct_ids": acct["distinct_ids"]},
+        "roofline": roof,
+        "e2e": {"value": world * T / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": T * 4 + T * p.d * esz, "d2h_bytes_per_step": T * p.d * esz},
+        "fwd_bwd": fb,
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, offs_np, K, V)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def fwd_bwd_rate(l3, dev, args) -> dict:
+    import torch
+
+    wl = W.make(5)
+    p = wl.p
+    offs_np = l3.l3_alloc_offsets(wl.freq, p.v, 1, p.k_max, p.power)
+    K, V = W.tables(wl, dev)
+    dt = torch.bfloat16
+    offs = torch.as_tensor(offs_np, device=dev)
+    Wu = torch.as_tensor(wl.W_up, device=dev).to(dt)
+    Wm = torch.as_tensor(wl.W_mix, device=dev).to(dt)
+    ids = torch.as_tensor(wl.ids, device=dev)
+    x = torch.as_tensor(wl.x, device=dev).to(dt)
+    dy = torch.as_tensor(wl.dy, device=dev).to(dt)
+    L = l3.make_layer(offs, K, V, Wu, Wm, p.k_max)
+    T = wl.T
+    ws = torch.empty(l3.l3_workspace_size(L, T, 0), dtype=torch.uint8, device=dev)
+    wsb = torch.empty(l3.l3_workspace_size(L, T, 1), dtype=torch.uint8, device=dev)
+    sv = torch.empty(l3.l3_saved_size(L, T), dtype=torch.uint8, device=dev)
+    y = torch.empty((T, p.d), dtype=dt, device=dev)
+    g = [torch.empty(s, device=dev) for s in ((T, p.d), (p.v, p.d), (p.v, p.d_v), (p.d, p.d_v), (p.d, 2 * p.d))]
+
+    def step():
+        l3.l3_forward(L, ids, x, y, ws, saved=sv)
+        l3.l3_backward(L, ids, x, dy, sv, *g, wsb)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        step()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    return {"workload": f"{p.name}: vocab {p.vocab}, v {p.v}, d {p.d}, d_v {p.d_v}, T {T}, k {p.k_max}",
+            "value": T / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
+            "l2": "not flushed (whole working set is under 2 MB)"}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--config", type=int, default=2, choices=sorted(W.PRESETS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-tokens", type=int, default=128,
+                    help="tokens per reference-arm step")
+    args = ap.parse_args(argv)
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        return run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

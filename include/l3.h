@@ -1,0 +1,228 @@
+/*
+ * l3.h — C ABI of a Large Lookup Layer (L³) library for NVIDIA B300 (sm_103a).
+ *
+ * The layer is the one described in "L³: Large Lookup Layers" (Tseng, De Sa;
+ * arXiv:2601.21461). Its gist.science explainer, Technical Summary:
+ *   - "Core Architecture": the layer takes a hidden state x and a token id t. Static
+ *     routing maps t to a fixed subset of a large embedding table (here: the contiguous
+ *     CSR row range offs[t] .. offs[t+1]-1 of a key table K and a value table V). The
+ *     output is  y = W_mix [ LayerNorm( W_up( V_tᵀ Softmax(K_t x) ) ) ; x ].
+ *   - "Information-Theoretic Embedding Allocation": a budget of v rows is spread over
+ *     the vocabulary; every token gets at least 1 and at most k rows.
+ *   - "Systems-Friendly Design", batch sorting: sorting a batch by token id makes the
+ *     layer's attention mask block-diagonal; the library sorts every batch and works
+ *     on the segments of equal ids.
+ *
+ * Conventions shared by every entry point:
+ *   - All pointers named *_host are host memory; every other pointer is device memory
+ *     on the current CUDA device. The caller owns all memory. The library never
+ *     allocates device memory: scratch comes from a caller-provided workspace sized by
+ *     l3_workspace_size.
+ *   - Device work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream). Argument errors are returned before anything is enqueued.
+ *   - Matrices are dense row-major. Element types: L3_F32 (float) or L3_BF16 (bfloat16,
+ *     accumulation in fp32).
+ *   - Errors found on the device (a token id outside [0, vocab), a bad offsets table, a
+ *     bounded wait that ran out) never trap: a kernel records them in the workspace's
+ *     status words, and l3_get_error reports them. The output rows concerned are then
+ *     unspecified.
+ *   - A workspace (and a saved-state buffer) must not be used by two calls that can run
+ *     at the same time. No C++ exception crosses this interface.
+ */
+#ifndef L3_H_
+#define L3_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define L3_ABI_VERSION 1
+
+typedef struct CUstream_st* l3_stream_t; /* = cudaStream_t */
+typedef struct CUevent_st* l3_event_t;   /* = cudaEvent_t  */
+
+typedef enum l3_status {
+  L3_OK = 0,
+  L3_ERR_INVALID_ARG = 1, /* null pointer, bad size or shape                          */
+  L3_ERR_INFEASIBLE = 2,  /* allocation: vocab*n_min <= v <= vocab*n_max does not hold */
+  L3_ERR_UNSUPPORTED = 3, /* shape outside what the kernels handle (see l3_layer)       */
+  L3_ERR_WORKSPACE = 4,   /* workspace smaller than l3_workspace_size                   */
+  L3_ERR_TOKEN_RANGE = 5, /* a token id was outside [0, vocab)          (device-found)  */
+  L3_ERR_CUDA = 6,        /* a CUDA runtime call failed                                 */
+  L3_ERR_LAYER = 7,       /* offsets not 0 = offs[0] < ... < offs[vocab] = v, or a range
+                             longer than k_max                           (device-found) */
+  L3_ERR_TIMEOUT = 8      /* a bounded device-side wait gave up          (device-found) */
+} l3_status;
+
+enum { L3_F32 = 0, L3_BF16 = 1 };
+
+/*
+ * A layer: its shapes and its parameters (device pointers, caller-owned).
+ *   offs   [vocab+1] int32   CSR offsets; token id t owns rows offs[t] .. offs[t+1]-1.
+ *                            Must hold 0 = offs[0] < offs[1] < ... < offs[vocab] = v and
+ *                            offs[t+1] - offs[t] <= k_max (l3_check_layer verifies).
+ *   K      [v, d]     dtype  key table
+ *   V      [v, d_v]   dtype  value table
+ *   W_up   [d, d_v]   dtype  (out x in): u = W_up a
+ *   W_mix  [d, 2d]    dtype  (out x in): y = W_mix [h; x]; columns 0..d-1 act on the
+ *                            LayerNorm output h, columns d..2d-1 on x.
+ * Supported: 1 <= k_max <= 512; d and d_v multiples of 64 with 64 <= d <= 4096 and
+ * 64 <= d_v <= 512; v < 2^31; vocab < 2^31. LayerNorm is over the d features, biased
+ * variance, no affine, epsilon ln_eps (> 0; 1e-5 is the usual value).
+ */
+typedef struct l3_layer {
+  int64_t vocab;
+  int64_t v;
+  int64_t d;
+  int64_t d_v;
+  int32_t k_max;
+  int32_t dtype; /* L3_F32 or L3_BF16 */
+  float ln_eps;
+  int32_t reserved; /* set to 0 */
+  const int32_t* offs;
+  const void* K;
+  const void* V;
+  const void* W_up;
+  const void* W_mix;
+} l3_layer;
+
+/* Passes for l3_workspace_size. */
+enum { L3_PASS_FORWARD = 0, L3_PASS_BACKWARD = 1, L3_PASS_FORWARD_HOST = 2 };
+
+/* Stages of l3_forward, for l3_forward_timed. */
+enum {
+  L3_STAGE_ROUTE = 0,  /* sort the batch by token id, build segments             */
+  L3_STAGE_ATTEND = 1, /* a = V_tᵀ softmax(K_t x) for every token                 */
+  L3_STAGE_UP = 2,     /* u = W_up a, LayerNorm statistics                         */
+  L3_STAGE_MIX = 3,    /* y = W_mix [LayerNorm(u); x]                              */
+  L3_FWD_STAGES = 4
+};
+
+/*
+ * Row allocation (host only, synchronous; touches no GPU). Explainer, Technical Summary,
+ * "Information-Theoretic Embedding Allocation": each of the vocab token ids gets n_t rows
+ * with n_min <= n_t <= n_max and sum n_t = v; frequent ids get more. The corpus-driven
+ * Algorithm 1 is not given on the pages; this is the frequency rule the library uses:
+ *   w_t = pow(freq[t], power); a water level c solves sum_t clamp(c w_t, n_min, n_max) = v
+ *   (200 bisection steps locate the clamped sets, then c is solved exactly for them, the
+ *   free weights summed in increasing id order); the real targets are rounded by largest
+ *   remainder (among ids below n_max; ties go to the lower id).
+ * Writes offs_out[0..vocab] (exclusive prefix sum of n_t: offs_out[0] = 0,
+ * offs_out[vocab] = v). freq: [vocab] positive finite values (any scale).
+ * Errors: L3_ERR_INVALID_ARG (null pointer, vocab < 1, n_min < 1, n_max < n_min,
+ * non-positive or non-finite freq, non-finite power, v >= 2^31), L3_ERR_INFEASIBLE.
+ */
+l3_status l3_alloc_offsets(const double* freq, int64_t vocab, int64_t v, int32_t n_min,
+                           int32_t n_max, double power, int32_t* offs_out);
+
+/* Bytes of workspace a call needs (pass: L3_PASS_*), 0 if the layer is invalid. */
+size_t l3_workspace_size(const l3_layer* layer, int64_t T, int32_t pass);
+
+/* Bytes of the saved-state buffer l3_forward fills for l3_backward. */
+size_t l3_saved_size(const l3_layer* layer, int64_t T);
+
+/*
+ * Check the offsets table on the device (static routing must map every id to a
+ * non-empty range of at most k_max rows inside [0, v)). Synchronises `stream`.
+ * Returns L3_OK, L3_ERR_LAYER, or an argument/CUDA error. ws: >= l3_workspace_size(
+ * layer, 0, L3_PASS_FORWARD) bytes.
+ */
+l3_status l3_check_layer(const l3_layer* layer, void* ws, size_t ws_bytes, l3_stream_t stream);
+
+/*
+ * Batch sorting (explainer, "Systems-Friendly Design"): stable sort of the T token ids
+ * and the segments of equal ids.
+ *   ids        [T]    int32 token ids (device)
+ *   perm       [T]    int32 out: perm[q] = original index of the q-th token in sorted order
+ *                     (equal ids keep their batch order)
+ *   seg_start  [T+1]  int32 out: segment s spans sorted positions seg_start[s] ..
+ *                     seg_start[s+1]-1; entries past n_seg are unspecified
+ *   seg_id     [T]    int32 out: token id of segment s (increasing in s)
+ *   n_seg      [1]    int32 out: number of segments (distinct ids)
+ * Any output pointer may be NULL to skip that copy. T may be 0.
+ */
+l3_status l3_route(const l3_layer* layer, const int32_t* ids, int64_t T, int32_t* perm,
+                   int32_t* seg_start, int32_t* seg_id, int32_t* n_seg, void* ws,
+                   size_t ws_bytes, l3_stream_t stream);
+
+/*
+ * Forward pass (explainer, "Core Architecture", the layer formula), for each token i:
+ *   s = K_t x_i (t = ids[i]); p = softmax(s) (no temperature); a_i = V_tᵀ p;
+ *   u_i = W_up a_i; h_i = LayerNorm(u_i); y_i = W_mix [h_i; x_i].
+ *   ids   [T]    int32 (device)
+ *   x     [T, d] layer dtype
+ *   y     [T, d] y_dtype (L3_F32, or the layer dtype)
+ *   saved nullable; if given, l3_saved_size(layer, T) bytes that l3_backward reads
+ *   ws    >= l3_workspace_size(layer, T, L3_PASS_FORWARD) bytes
+ * T may be 0 (nothing is enqueued). Errors: L3_ERR_INVALID_ARG, L3_ERR_UNSUPPORTED,
+ * L3_ERR_WORKSPACE, L3_ERR_CUDA; token ids out of range are reported by l3_get_error.
+ */
+l3_status l3_forward(const l3_layer* layer, const int32_t* ids, int64_t T, const void* x,
+                     void* y, int32_t y_dtype, void* saved, void* ws, size_t ws_bytes,
+                     l3_stream_t stream);
+
+/*
+ * l3_forward, recording events[k] on `stream` before stage k (k < L3_FWD_STAGES) and
+ * events[L3_FWD_STAGES] after the last stage: the elapsed time between events[k] and
+ * events[k+1] is stage k. events: L3_FWD_STAGES+1 created cudaEvent_t handles.
+ */
+l3_status l3_forward_timed(const l3_layer* layer, const int32_t* ids, int64_t T,
+                           const void* x, void* y, int32_t y_dtype, void* saved, void* ws,
+                           size_t ws_bytes, l3_stream_t stream, l3_event_t* events);
+
+/*
+ * l3_forward on HOST buffers: copies ids_host [T] int32 and x_host [T, d] (layer dtype)
+ * to the device, runs the forward and copies y back to y_host [T, d] (y_dtype), all
+ * enqueued on `stream` (one cudaMemcpyAsync per buffer). Host buffers should be pinned
+ * for asynchronous copies; the caller synchronises `stream` before reading y_host.
+ * ws: >= l3_workspace_size(layer, T, L3_PASS_FORWARD_HOST) bytes (holds the device
+ * copies as well as the forward's scratch).
+ */
+l3_status l3_forward_host(const l3_layer* layer, const int32_t* ids_host, int64_t T,
+                          const void* x_host, void* y_host, int32_t y_dtype, void* ws,
+                          size_t ws_bytes, l3_stream_t stream);
+
+/*
+ * Backward pass: gradients of sum(dy * y) for the layer formula, given the `saved` state
+ * of an l3_forward call on the same layer, ids and x.
+ *   dy       [T, d]      layer dtype
+ *   dx       [T, d]      fp32 out
+ *   dK       [v, d]      fp32 out; rows of ids absent from the batch are zero
+ *   dV       [v, d_v]    fp32 out; likewise
+ *   dW_up    [d, d_v]    fp32 out
+ *   dW_mix   [d, 2d]     fp32 out
+ * Every output is overwritten, not accumulated. dK and dV are deterministic segmented
+ * sums: for each id, its rows' gradients are summed over that id's tokens in batch order,
+ * with no floating-point atomics, so repeated calls give bitwise-identical results.
+ * ws: >= l3_workspace_size(layer, T, L3_PASS_BACKWARD) bytes.
+ */
+l3_status l3_backward(const l3_layer* layer, const int32_t* ids, int64_t T, const void* x,
+                      const void* dy, const void* saved, float* dx, float* dK, float* dV,
+                      float* dW_up, float* dW_mix, void* ws, size_t ws_bytes,
+                      l3_stream_t stream);
+
+/*
+ * Synchronise `stream`, then read and clear the status words that kernels of earlier
+ * calls wrote into `ws`. Returns L3_OK, L3_ERR_TOKEN_RANGE, L3_ERR_LAYER,
+ * L3_ERR_TIMEOUT or L3_ERR_CUDA (the first that applies, in that order of priority
+ * after L3_ERR_CUDA).
+ */
+l3_status l3_get_error(void* ws, l3_stream_t stream);
+
+/* Static string naming a status. */
+const char* l3_status_string(l3_status status);
+
+/* Kernels this library has launched in this process so far (host-side counter). */
+uint64_t l3_launch_count(void);
+
+/* L3_ABI_VERSION of the built library. */
+int32_t l3_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* L3_H_ */

@@ -1,0 +1,569 @@
+// C-ABI entry points of the L³ library: argument checks, workspace layout, and the order
+// of the kernels for the forward pass, the backward pass and batch routing.
+#include <atomic>
+#include <cmath>
+#include <cstring>
+
+#include "l3_internal.h"
+
+namespace l3 {
+
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+
+// Bump allocator over a caller-provided buffer (base == nullptr: measure only).
+struct Carve {
+  char* base;
+  size_t off = 0;
+  explicit Carve(void* b) : base(static_cast<char*>(b)) {}
+  template <typename T>
+  T* take(size_t n) {
+    off = align_up(off, kAlign);
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off += n * sizeof(T);
+    return p;
+  }
+  char* raw(size_t bytes) { return take<char>(bytes); }
+};
+
+bool valid_dtype(int dt) { return dt == L3_F32 || dt == L3_BF16; }
+size_t esize(int dt) { return dt == L3_BF16 ? 2 : 4; }
+
+l3_status check_layer_args(const l3_layer* L) {
+  if (!L) return L3_ERR_INVALID_ARG;
+  if (!L->offs || !L->K || !L->V || !L->W_up || !L->W_mix) return L3_ERR_INVALID_ARG;
+  if (!valid_dtype(L->dtype) || L->reserved != 0) return L3_ERR_INVALID_ARG;
+  if (L->vocab < 1 || L->v < L->vocab || L->v >= (int64_t(1) << 31) ||
+      L->vocab >= (int64_t(1) << 31))
+    return L3_ERR_INVALID_ARG;
+  if (!(L->ln_eps > 0.f) || !std::isfinite(L->ln_eps)) return L3_ERR_INVALID_ARG;
+  if (L->k_max < 1 || L->k_max > 512) return L3_ERR_UNSUPPORTED;
+  if (L->d < 64 || L->d > 2048 || L->d % 64 != 0) return L3_ERR_UNSUPPORTED;
+  if (L->d_v < 64 || L->d_v > 512 || L->d_v % 64 != 0) return L3_ERR_UNSUPPORTED;
+  if (L->v > L->vocab * int64_t(L->k_max)) return L3_ERR_INVALID_ARG;
+  return L3_OK;
+}
+
+// ---- workspace layouts ------------------------------------------------------------------------
+
+struct FwdWs {
+  DevStatus* st;
+  void* route_scratch;
+  int32_t *perm, *seg_start, *seg_id, *n_seg;
+  float* part;
+  float* a_f32;
+  __nv_bfloat16* a_bf16;
+  float* U;
+  float* mu;
+  float* rstd;
+  float* H;
+  float* Y;
+  int n_split;
+};
+
+FwdWs carve_fwd(Carve& c, const l3_layer* L, int64_t T) {
+  FwdWs w{};
+  const size_t t = size_t(T), d = size_t(L->d), dv = size_t(L->d_v);
+  w.st = c.take<DevStatus>(1);
+  w.route_scratch = c.raw(route_scratch_bytes(T));
+  w.perm = c.take<int32_t>(t);
+  w.seg_start = c.take<int32_t>(t + 1);
+  w.seg_id = c.take<int32_t>(t);
+  w.n_seg = c.take<int32_t>(1);
+  w.n_split = attend_choose_split(T, L->k_max);
+  w.part = c.take<float>(attend_part_floats(T, w.n_split, L->d_v));
+  w.a_f32 = c.take<float>(t * dv);
+  w.a_bf16 = L->dtype == L3_BF16 ? c.take<__nv_bfloat16>(t * dv) : nullptr;
+  w.U = c.take<float>(t * d);
+  w.mu = c.take<float>(t);
+  w.rstd = c.take<float>(t);
+  w.H = c.take<float>(t * d);
+  w.Y = c.take<float>(t * d);
+  return w;
+}
+
+struct Saved {
+  float* a;     // [T, d_v]
+  float* ml;    // [T, 2]
+  float* mu;    // [T]
+  float* rstd;  // [T]
+};
+
+Saved carve_saved(Carve& c, const l3_layer* L, int64_t T) {
+  Saved s{};
+  s.a = c.take<float>(size_t(T) * size_t(L->d_v));
+  s.ml = c.take<float>(size_t(T) * 2);
+  s.mu = c.take<float>(size_t(T));
+  s.rstd = c.take<float>(size_t(T));
+  return s;
+}
+
+struct BwdWs {
+  DevStatus* st;
+  void* route_scratch;
+  int32_t *seg_start, *n_seg;
+  float *U, *H, *mu, *rstd, *dC, *du, *dA, *p_buf, *ds_buf;
+};
+
+BwdWs carve_bwd(Carve& c, const l3_layer* L, int64_t T) {
+  BwdWs w{};
+  const size_t t = size_t(T), d = size_t(L->d), dv = size_t(L->d_v);
+  w.st = c.take<DevStatus>(1);
+  w.route_scratch = c.raw(route_scratch_bytes(T));
+  w.seg_start = c.take<int32_t>(t + 1);
+  w.n_seg = c.take<int32_t>(1);
+  w.U = c.take<float>(t * d);
+  w.H = c.take<float>(t * d);
+  w.mu = c.take<float>(t);
+  w.rstd = c.take<float>(t);
+  w.dC = c.take<float>(t * 2 * d);
+  w.du = c.take<float>(t * d);
+  w.dA = c.take<float>(t * dv);
+  w.p_buf = c.take<float>(t * size_t(L->k_max));
+  w.ds_buf = c.take<float>(t * size_t(L->k_max));
+  return w;
+}
+
+#define L3_CUDA(call)                      \
+  do {                                     \
+    if ((call) != cudaSuccess) {           \
+      (void)cudaGetLastError();            \
+      return L3_ERR_CUDA;                  \
+    }                                      \
+  } while (0)
+
+__global__ void check_offsets_kernel(const int32_t* __restrict__ offs, int64_t vocab, int64_t v,
+                                     int k_max, DevStatus* st) {
+  for (int64_t t = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; t < vocab;
+       t += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t a = offs[t], b = offs[t + 1];
+    bool bad = !(b > a) || (b - a) > k_max;
+    if (t == 0 && a != 0) bad = true;
+    if (t == vocab - 1 && b != v) bad = true;
+    if (bad) atomicOr(&st->layer_bad, 1);
+  }
+}
+
+l3_status forward_impl(const l3_layer* L, const int32_t* ids, int64_t T, const void* x, void* y,
+                       int32_t y_dtype, void* saved, void* ws, size_t ws_bytes,
+                       cudaStream_t s, cudaEvent_t* ev) {
+  l3_status e = check_layer_args(L);
+  if (e != L3_OK) return e;
+  if (T < 0 || T >= (int64_t(1) << 31)) return L3_ERR_INVALID_ARG;
+  if (!(y_dtype == L3_F32 || y_dtype == L->dtype)) return L3_ERR_INVALID_ARG;
+  if (T > 0 && (!ids || !x || !y || !ws)) return L3_ERR_INVALID_ARG;
+  if (ws_bytes < l3_workspace_size(L, T, L3_PASS_FORWARD)) return L3_ERR_WORKSPACE;
+  if (T == 0) return L3_OK;
+
+  Carve c(ws);
+  FwdWs w = carve_fwd(c, L, T);
+  Saved sv{};
+  if (saved) {
+    Carve cs(saved);
+    sv = carve_saved(cs, L, T);
+  }
+  float* a_f32 = saved ? sv.a : w.a_f32;
+  float* mu = saved ? sv.mu : w.mu;
+  float* rstd = saved ? sv.rstd : w.rstd;
+  const int d = int(L->d), dv = int(L->d_v);
+
+  L3_CUDA(cudaMemsetAsync(w.st, 0, sizeof(DevStatus), s));
+  if (ev) L3_CUDA(cudaEventRecord(ev[L3_STAGE_ROUTE], s));
+  const uint64_t* keys = nullptr;
+  L3_CUDA(launch_route(ids, T, L->vocab, w.route_scratch,
+                       RouteOut{w.perm, w.seg_start, w.seg_id, w.n_seg}, w.st, s, &keys));
+
+  if (ev) L3_CUDA(cudaEventRecord(ev[L3_STAGE_ATTEND], s));
+  AttendArgs aa{};
+  aa.sorted_keys = keys;
+  aa.T = T;
+  aa.offs = L->offs;
+  aa.K = L->K;
+  aa.V = L->V;
+  aa.x = x;
+  aa.d = d;
+  aa.d_v = dv;
+  aa.k_max = L->k_max;
+  aa.dtype = L->dtype;
+  aa.a_f32 = (L->dtype == L3_F32 || saved) ? a_f32 : nullptr;
+  aa.a_bf16 = w.a_bf16;
+  aa.ml = saved ? sv.ml : nullptr;
+  aa.part = w.part;
+  aa.n_split = w.n_split;
+  L3_CUDA(launch_attend_fwd(aa, s));
+
+  if (ev) L3_CUDA(cudaEventRecord(ev[L3_STAGE_UP], s));
+  // u = W_up a: U[i, n] = sum_k A[i, k] W_up[n, k]
+  SimtGemm up{};
+  up.M = T;
+  up.N = d;
+  up.K = dv;
+  if (L->dtype == L3_BF16) {
+    up.A = w.a_bf16;
+    up.a_dtype = L3_BF16;
+  } else {
+    up.A = a_f32;
+    up.a_dtype = L3_F32;
+  }
+  up.a_sm = dv;
+  up.a_sk = 1;
+  up.B = L->W_up;
+  up.b_dtype = L->dtype;
+  up.b_sk = 1;
+  up.b_sn = dv;
+  up.C = w.U;
+  up.ldc = d;
+  up.alpha = 1.f;
+  up.beta = 0.f;
+  L3_CUDA(launch_simt_gemm(up, s));
+  L3_CUDA(launch_ln_stats(w.U, T, d, L->ln_eps, mu, rstd, s));
+
+  if (ev) L3_CUDA(cudaEventRecord(ev[L3_STAGE_MIX], s));
+  L3_CUDA(launch_ln_apply(w.U, mu, rstd, T, d, w.H, s));
+  float* Y = y_dtype == L3_F32 ? static_cast<float*>(y) : w.Y;
+  // y = W_mix[:, :d] h + W_mix[:, d:] x
+  SimtGemm mix{};
+  mix.M = T;
+  mix.N = d;
+  mix.K = d;
+  mix.A = w.H;
+  mix.a_dtype = L3_F32;
+  mix.a_sm = d;
+  mix.a_sk = 1;
+  mix.B = L->W_mix;
+  mix.b_dtype = L->dtype;
+  mix.b_sk = 1;
+  mix.b_sn = 2 * d;
+  mix.C = Y;
+  mix.ldc = d;
+  mix.alpha = 1.f;
+  mix.beta = 0.f;
+  L3_CUDA(launch_simt_gemm(mix, s));
+  mix.A = x;
+  mix.a_dtype = L->dtype;
+  mix.B = static_cast<const char*>(L->W_mix) + size_t(d) * esize(L->dtype);
+  mix.beta = 1.f;
+  L3_CUDA(launch_simt_gemm(mix, s));
+  if (y_dtype != L3_F32) L3_CUDA(launch_cast(Y, y, y_dtype, T * d, s));
+  if (ev) L3_CUDA(cudaEventRecord(ev[L3_FWD_STAGES], s));
+  return L3_OK;
+}
+
+}  // namespace
+
+void count_launch(int n) { g_launches.fetch_add(uint64_t(n), std::memory_order_relaxed); }
+
+cudaError_t launch_check_offsets(const int32_t* offs, int64_t vocab, int64_t v, int k_max,
+                                 DevStatus* st, cudaStream_t stream) {
+  int64_t blocks = (vocab + 255) / 256;
+  if (blocks > 148 * 8) blocks = 148 * 8;
+  check_offsets_kernel<<<unsigned(blocks), 256, 0, stream>>>(offs, vocab, v, k_max, st);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace l3
+
+using namespace l3;
+
+extern "C" {
+
+size_t l3_workspace_size(const l3_layer* L, int64_t T, int32_t pass) {
+  if (check_layer_args(L) != L3_OK || T < 0) return 0;
+  Carve c(nullptr);
+  if (pass == L3_PASS_FORWARD || pass == L3_PASS_FORWARD_HOST) {
+    carve_fwd(c, L, T);
+    if (pass == L3_PASS_FORWARD_HOST) {
+      c.take<int32_t>(size_t(T));
+      c.raw(size_t(T) * size_t(L->d) * esize(L->dtype));
+      c.raw(size_t(T) * size_t(L->d) * 4);
+    }
+  } else if (pass == L3_PASS_BACKWARD) {
+    carve_bwd(c, L, T);
+  } else {
+    return 0;
+  }
+  return align_up(c.off, kAlign);
+}
+
+size_t l3_saved_size(const l3_layer* L, int64_t T) {
+  if (check_layer_args(L) != L3_OK || T < 0) return 0;
+  Carve c(nullptr);
+  carve_saved(c, L, T);
+  return align_up(c.off, kAlign);
+}
+
+l3_status l3_check_layer(const l3_layer* L, void* ws, size_t ws_bytes, l3_stream_t stream) {
+  l3_status e = check_layer_args(L);
+  if (e != L3_OK) return e;
+  if (!ws) return L3_ERR_INVALID_ARG;
+  if (ws_bytes < l3_workspace_size(L, 0, L3_PASS_FORWARD)) return L3_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  DevStatus* st = static_cast<DevStatus*>(ws);
+  L3_CUDA(cudaMemsetAsync(st, 0, sizeof(DevStatus), s));
+  L3_CUDA(launch_check_offsets(L->offs, L->vocab, L->v, L->k_max, st, s));
+  DevStatus h{};
+  L3_CUDA(cudaMemcpyAsync(&h, st, sizeof(h), cudaMemcpyDeviceToHost, s));
+  L3_CUDA(cudaStreamSynchronize(s));
+  return h.layer_bad ? L3_ERR_LAYER : L3_OK;
+}
+
+l3_status l3_route(const l3_layer* L, const int32_t* ids, int64_t T, int32_t* perm,
+                   int32_t* seg_start, int32_t* seg_id, int32_t* n_seg, void* ws,
+                   size_t ws_bytes, l3_stream_t stream) {
+  l3_status e = check_layer_args(L);
+  if (e != L3_OK) return e;
+  if (T < 0 || T >= (int64_t(1) << 31) || !ws || (T > 0 && !ids)) return L3_ERR_INVALID_ARG;
+  if (ws_bytes < l3_workspace_size(L, T, L3_PASS_FORWARD)) return L3_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  Carve c(ws);
+  FwdWs w = carve_fwd(c, L, T);
+  L3_CUDA(cudaMemsetAsync(w.st, 0, sizeof(DevStatus), s));
+  const uint64_t* keys = nullptr;
+  L3_CUDA(launch_route(ids, T, L->vocab, w.route_scratch, RouteOut{perm, seg_start, seg_id, n_seg},
+                       w.st, s, &keys));
+  return L3_OK;
+}
+
+l3_status l3_forward(const l3_layer* L, const int32_t* ids, int64_t T, const void* x, void* y,
+                     int32_t y_dtype, void* saved, void* ws, size_t ws_bytes,
+                     l3_stream_t stream) {
+  return forward_impl(L, ids, T, x, y, y_dtype, saved, ws, ws_bytes,
+                      reinterpret_cast<cudaStream_t>(stream), nullptr);
+}
+
+l3_status l3_forward_timed(const l3_layer* L, const int32_t* ids, int64_t T, const void* x,
+                           void* y, int32_t y_dtype, void* saved, void* ws, size_t ws_bytes,
+                           l3_stream_t stream, l3_event_t* events) {
+  if (!events) return L3_ERR_INVALID_ARG;
+  return forward_impl(L, ids, T, x, y, y_dtype, saved, ws, ws_bytes,
+                      reinterpret_cast<cudaStream_t>(stream),
+                      reinterpret_cast<cudaEvent_t*>(events));
+}
+
+l3_status l3_forward_host(const l3_layer* L, const int32_t* ids_host, int64_t T,
+                          const void* x_host, void* y_host, int32_t y_dtype, void* ws,
+                          size_t ws_bytes, l3_stream_t stream) {
+  l3_status e = check_layer_args(L);
+  if (e != L3_OK) return e;
+  if (T < 0 || T >= (int64_t(1) << 31)) return L3_ERR_INVALID_ARG;
+  if (T == 0) return L3_OK;
+  if (!ids_host || !x_host || !y_host || !ws) return L3_ERR_INVALID_ARG;
+  if (!(y_dtype == L3_F32 || y_dtype == L->dtype)) return L3_ERR_INVALID_ARG;
+  if (ws_bytes < l3_workspace_size(L, T, L3_PASS_FORWARD_HOST)) return L3_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  Carve c(ws);
+  carve_fwd(c, L, T);
+  const size_t fwd_bytes = align_up(c.off, kAlign);
+  const size_t xb = size_t(T) * size_t(L->d) * esize(L->dtype);
+  const size_t yb = size_t(T) * size_t(L->d) * esize(y_dtype);
+  int32_t* ids_d = c.take<int32_t>(size_t(T));
+  void* x_d = c.raw(xb);
+  void* y_d = c.raw(size_t(T) * size_t(L->d) * 4);
+  L3_CUDA(cudaMemcpyAsync(ids_d, ids_host, size_t(T) * 4, cudaMemcpyHostToDevice, s));
+  L3_CUDA(cudaMemcpyAsync(x_d, x_host, xb, cudaMemcpyHostToDevice, s));
+  e = forward_impl(L, ids_d, T, x_d, y_d, y_dtype, nullptr, ws, fwd_bytes, s, nullptr);
+  if (e != L3_OK) return e;
+  L3_CUDA(cudaMemcpyAsync(y_host, y_d, yb, cudaMemcpyDeviceToHost, s));
+  return L3_OK;
+}
+
+l3_status l3_backward(const l3_layer* L, const int32_t* ids, int64_t T, const void* x,
+                      const void* dy, const void* saved, float* dx, float* dK, float* dV,
+                      float* dW_up, float* dW_mix, void* ws, size_t ws_bytes,
+                      l3_stream_t stream) {
+  l3_status e = check_layer_args(L);
+  if (e != L3_OK) return e;
+  if (T < 0 || T >= (int64_t(1) << 31)) return L3_ERR_INVALID_ARG;
+  if (!dK || !dV || !dW_up || !dW_mix || !ws) return L3_ERR_INVALID_ARG;
+  if (T > 0 && (!ids || !x || !dy || !saved || !dx)) return L3_ERR_INVALID_ARG;
+  if (ws_bytes < l3_workspace_size(L, T, L3_PASS_BACKWARD)) return L3_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int d = int(L->d), dv = int(L->d_v);
+  Carve c(ws);
+  BwdWs w = carve_bwd(c, L, T);
+  L3_CUDA(cudaMemsetAsync(w.st, 0, sizeof(DevStatus), s));
+  L3_CUDA(cudaMemsetAsync(dK, 0, size_t(L->v) * size_t(d) * 4, s));
+  L3_CUDA(cudaMemsetAsync(dV, 0, size_t(L->v) * size_t(dv) * 4, s));
+  if (T == 0) {
+    L3_CUDA(cudaMemsetAsync(dW_up, 0, size_t(d) * size_t(dv) * 4, s));
+    L3_CUDA(cudaMemsetAsync(dW_mix, 0, size_t(d) * size_t(2 * d) * 4, s));
+    return L3_OK;
+  }
+  Carve cs(const_cast<void*>(saved));
+  Saved sv = carve_saved(cs, L, T);
+
+  const uint64_t* keys = nullptr;
+  L3_CUDA(launch_route(ids, T, L->vocab, w.route_scratch,
+                       RouteOut{nullptr, w.seg_start, nullptr, w.n_seg}, w.st, s, &keys));
+  // Recompute u = W_up a (fp32 a from the forward) and h = LayerNorm(u).
+  SimtGemm g{};
+  g.M = T;
+  g.N = d;
+  g.K = dv;
+  g.A = sv.a;
+  g.a_dtype = L3_F32;
+  g.a_sm = dv;
+  g.a_sk = 1;
+  g.B = L->W_up;
+  g.b_dtype = L->dtype;
+  g.b_sk = 1;
+  g.b_sn = dv;
+  g.C = w.U;
+  g.ldc = d;
+  g.alpha = 1.f;
+  g.beta = 0.f;
+  L3_CUDA(launch_simt_gemm(g, s));
+  L3_CUDA(launch_ln_stats(w.U, T, d, L->ln_eps, w.mu, w.rstd, s));
+  L3_CUDA(launch_ln_apply(w.U, w.mu, w.rstd, T, d, w.H, s));
+  // dW_mix[:, :d] = dyᵀ h, dW_mix[:, d:] = dyᵀ x
+  g = SimtGemm{};
+  g.M = d;
+  g.N = d;
+  g.K = T;
+  g.A = dy;
+  g.a_dtype = L->dtype;
+  g.a_sm = 1;
+  g.a_sk = d;
+  g.B = w.H;
+  g.b_dtype = L3_F32;
+  g.b_sk = d;
+  g.b_sn = 1;
+  g.C = dW_mix;
+  g.ldc = 2 * d;
+  g.alpha = 1.f;
+  g.beta = 0.f;
+  L3_CUDA(launch_simt_gemm(g, s));
+  g.B = x;
+  g.b_dtype = L->dtype;
+  g.C = dW_mix + d;
+  L3_CUDA(launch_simt_gemm(g, s));
+  // dC = dy W_mix  [T, 2d]
+  g = SimtGemm{};
+  g.M = T;
+  g.N = 2 * d;
+  g.K = d;
+  g.A = dy;
+  g.a_dtype = L->dtype;
+  g.a_sm = d;
+  g.a_sk = 1;
+  g.B = L->W_mix;
+  g.b_dtype = L->dtype;
+  g.b_sk = 2 * d;
+  g.b_sn = 1;
+  g.C = w.dC;
+  g.ldc = 2 * d;
+  g.alpha = 1.f;
+  g.beta = 0.f;
+  L3_CUDA(launch_simt_gemm(g, s));
+  L3_CUDA(launch_ln_backward(w.dC, 2 * d, w.H, w.rstd, T, d, w.du, s));
+  // dW_up = duᵀ a  [d, d_v]
+  g = SimtGemm{};
+  g.M = d;
+  g.N = dv;
+  g.K = T;
+  g.A = w.du;
+  g.a_dtype = L3_F32;
+  g.a_sm = 1;
+  g.a_sk = d;
+  g.B = sv.a;
+  g.b_dtype = L3_F32;
+  g.b_sk = dv;
+  g.b_sn = 1;
+  g.C = dW_up;
+  g.ldc = dv;
+  g.alpha = 1.f;
+  g.beta = 0.f;
+  L3_CUDA(launch_simt_gemm(g, s));
+  // da = du W_up  [T, d_v]
+  g = SimtGemm{};
+  g.M = T;
+  g.N = dv;
+  g.K = d;
+  g.A = w.du;
+  g.a_dtype = L3_F32;
+  g.a_sm = d;
+  g.a_sk = 1;
+  g.B = L->W_up;
+  g.b_dtype = L->dtype;
+  g.b_sk = dv;
+  g.b_sn = 1;
+  g.C = w.dA;
+  g.ldc = dv;
+  g.alpha = 1.f;
+  g.beta = 0.f;
+  L3_CUDA(launch_simt_gemm(g, s));
+
+  AttendBwdArgs ab{};
+  ab.sorted_keys = keys;
+  ab.T = T;
+  ab.offs = L->offs;
+  ab.K = L->K;
+  ab.V = L->V;
+  ab.x = x;
+  ab.d = d;
+  ab.d_v = dv;
+  ab.k_max = L->k_max;
+  ab.dtype = L->dtype;
+  ab.da = w.dA;
+  ab.dx_in = w.dC + d;
+  ab.ldx_in = 2 * d;
+  ab.dx = dx;
+  ab.p_buf = w.p_buf;
+  ab.ds_buf = w.ds_buf;
+  L3_CUDA(launch_attend_bwd(ab, s));
+
+  SegReduceArgs sr{};
+  sr.sorted_keys = keys;
+  sr.T = T;
+  sr.seg_start = w.seg_start;
+  sr.n_seg = w.n_seg;
+  sr.offs = L->offs;
+  sr.x = x;
+  sr.dtype = L->dtype;
+  sr.da = w.dA;
+  sr.d = d;
+  sr.d_v = dv;
+  sr.k_max = L->k_max;
+  sr.p_buf = w.p_buf;
+  sr.ds_buf = w.ds_buf;
+  sr.dK = dK;
+  sr.dV = dV;
+  L3_CUDA(launch_seg_reduce(sr, s));
+  return L3_OK;
+}
+
+l3_status l3_get_error(void* ws, l3_stream_t stream) {
+  if (!ws) return L3_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  DevStatus h{};
+  L3_CUDA(cudaStreamSynchronize(s));
+  L3_CUDA(cudaMemcpy(&h, ws, sizeof(h), cudaMemcpyDeviceToHost));
+  L3_CUDA(cudaMemset(ws, 0, sizeof(h)));
+  if (h.token_range) return L3_ERR_TOKEN_RANGE;
+  if (h.layer_bad) return L3_ERR_LAYER;
+  if (h.timeout) return L3_ERR_TIMEOUT;
+  return L3_OK;
+}
+
+const char* l3_status_string(l3_status st) {
+  switch (st) {
+    case L3_OK: return "L3_OK";
+    case L3_ERR_INVALID_ARG: return "L3_ERR_INVALID_ARG";
+    case L3_ERR_INFEASIBLE: return "L3_ERR_INFEASIBLE";
+    case L3_ERR_UNSUPPORTED: return "L3_ERR_UNSUPPORTED";
+    case L3_ERR_WORKSPACE: return "L3_ERR_WORKSPACE";
+    case L3_ERR_TOKEN_RANGE: return "L3_ERR_TOKEN_RANGE";
+    case L3_ERR_CUDA: return "L3_ERR_CUDA";
+    case L3_ERR_LAYER: return "L3_ERR_LAYER";
+    case L3_ERR_TIMEOUT: return "L3_ERR_TIMEOUT";
+  }
+  return "L3_ERR_UNKNOWN";
+}
+
+uint64_t l3_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int32_t l3_abi_version(void) { return L3_ABI_VERSION; }
+
+}  // extern "C"

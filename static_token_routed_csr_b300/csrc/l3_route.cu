@@ -1,0 +1,227 @@
+// Batch sorting by token id ("L³: Large Lookup Layers", gist.science explainer,
+// Technical Summary, "Systems-Friendly Design": sorting a batch by token id turns the
+// layer's attention mask block-diagonal).
+//
+// Keys are (id << 32) | batch position. They are unique, so any correct sort of the keys
+// is the stable sort of the ids. Batches up to kSmallT tokens are sorted by one CTA in
+// shared memory (bitonic); larger ones are cut into kChunk-key runs sorted the same way,
+// then merged pairwise (each key finds its rank in the other run by binary search).
+// A last pass marks segment starts and numbers the segments.
+#include "l3_internal.h"
+
+namespace l3 {
+
+namespace {
+
+constexpr int kChunk = 4096;  // keys per CTA sort (32 KB of shared memory)
+
+__device__ inline uint64_t make_key(const int32_t* ids, int64_t T, int64_t vocab, int64_t i,
+                                    DevStatus* st) {
+  if (i >= T) return ~0ull;
+  int32_t id = ids[i];
+  if (id < 0 || int64_t(id) >= vocab) {
+    atomicOr(&st->token_range, 1);
+    id = 0;  // keep every later access in bounds; the row's output is unspecified
+  }
+  return (uint64_t(uint32_t(id)) << 32) | uint64_t(i);
+}
+
+// Bitonic sort of n (power of two, <= kChunk) keys in shared memory by the whole CTA.
+__device__ void block_bitonic(uint64_t* s, int n) {
+  for (int k = 2; k <= n; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        int p = i ^ j;
+        if (p > i) {
+          uint64_t a = s[i], b = s[p];
+          bool up = (i & k) == 0;
+          if ((a > b) == up) {
+            s[i] = b;
+            s[p] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// Exclusive scan of one int per thread across the CTA (blockDim.x == 1024).
+__device__ int block_exclusive_scan(int v, int* warp_tot, int* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  if (lane == 31) warp_tot[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    int w = lane < (int)(blockDim.x >> 5) ? warp_tot[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int u = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += u;
+    }
+    warp_tot[lane] = wi - w;
+    if (lane == 31) *total = wi;
+  }
+  __syncthreads();
+  int r = warp_tot[wid] + incl - v;
+  __syncthreads();
+  return r;
+}
+
+// Segment pass over sorted keys: perm, seg_start, seg_id, n_seg. One CTA of 1024 threads
+// walks the batch in tiles of 1024*kItems keys, carrying the segment count across tiles.
+constexpr int kItems = 4;
+
+__device__ void segment_pass(const uint64_t* keys, int64_t T, int32_t* perm,
+                             int32_t* seg_start, int32_t* seg_id, int32_t* n_seg,
+                             int* warp_tot, int* total) {
+  int carry = 0;
+  const int64_t tile = int64_t(blockDim.x) * kItems;
+  for (int64_t base = 0; base < T; base += tile) {
+    int flags[kItems];
+    int cnt = 0;
+#pragma unroll
+    for (int u = 0; u < kItems; ++u) {
+      int64_t q = base + int64_t(threadIdx.x) * kItems + u;
+      flags[u] = 0;
+      if (q < T) {
+        uint64_t k = keys[q];
+        flags[u] = (q == 0 || (keys[q - 1] >> 32) != (k >> 32)) ? 1 : 0;
+        if (perm) perm[q] = int32_t(uint32_t(k));
+      }
+      cnt += flags[u];
+    }
+    int ex = block_exclusive_scan(cnt, warp_tot, total);
+    int s = carry + ex;
+#pragma unroll
+    for (int u = 0; u < kItems; ++u) {
+      int64_t q = base + int64_t(threadIdx.x) * kItems + u;
+      if (flags[u]) {
+        if (seg_start) seg_start[s] = int32_t(q);
+        if (seg_id) seg_id[s] = int32_t(keys[q] >> 32);
+        ++s;
+      }
+    }
+    carry += *total;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    if (seg_start) seg_start[carry] = int32_t(T);
+    if (n_seg) *n_seg = carry;
+  }
+}
+
+__global__ void __launch_bounds__(1024) route_small_kernel(const int32_t* __restrict__ ids,
+                                                           int64_t T, int64_t vocab,
+                                                           uint64_t* keys_out, int32_t* perm,
+                                                           int32_t* seg_start, int32_t* seg_id,
+                                                           int32_t* n_seg, DevStatus* st) {
+  __shared__ uint64_t s[kChunk];
+  __shared__ int warp_tot[32];
+  __shared__ int total;
+  int n = 1;
+  while (n < T) n <<= 1;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) s[i] = make_key(ids, T, vocab, i, st);
+  __syncthreads();
+  block_bitonic(s, n);
+  for (int i = threadIdx.x; i < T; i += blockDim.x) keys_out[i] = s[i];
+  __syncthreads();
+  segment_pass(s, T, perm, seg_start, seg_id, n_seg, warp_tot, &total);
+}
+
+__global__ void __launch_bounds__(1024) route_chunk_kernel(const int32_t* __restrict__ ids,
+                                                           int64_t T, int64_t vocab,
+                                                           uint64_t* keys_out, DevStatus* st) {
+  __shared__ uint64_t s[kChunk];
+  const int64_t base = int64_t(blockIdx.x) * kChunk;
+  for (int i = threadIdx.x; i < kChunk; i += blockDim.x) s[i] = make_key(ids, T, vocab, base + i, st);
+  __syncthreads();
+  block_bitonic(s, kChunk);
+  for (int i = threadIdx.x; i < kChunk; i += blockDim.x)
+    if (base + i < T) keys_out[base + i] = s[i];
+}
+
+// Number of keys in a[0..n) smaller than key (a sorted ascending).
+__device__ inline int64_t lower_bound(const uint64_t* a, int64_t n, uint64_t key) {
+  int64_t lo = 0, hi = n;
+  while (lo < hi) {
+    int64_t mid = (lo + hi) >> 1;
+    if (a[mid] < key)
+      lo = mid + 1;
+    else
+      hi = mid;
+  }
+  return lo;
+}
+
+// Merge sorted runs of width w pairwise: in -> out.
+__global__ void route_merge_kernel(const uint64_t* __restrict__ in, uint64_t* __restrict__ out,
+                                   int64_t T, int64_t w) {
+  const int64_t p = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (p >= T) return;
+  const int64_t L = p / (2 * w) * (2 * w);
+  const int64_t mid = L + w < T ? L + w : T;
+  const int64_t R = L + 2 * w < T ? L + 2 * w : T;
+  const uint64_t key = in[p];
+  int64_t rank;
+  if (p < mid)
+    rank = (p - L) + lower_bound(in + mid, R - mid, key);
+  else
+    rank = (p - mid) + lower_bound(in + L, mid - L, key);
+  out[L + rank] = key;
+}
+
+__global__ void __launch_bounds__(1024) route_segment_kernel(const uint64_t* __restrict__ keys,
+                                                             int64_t T, int32_t* perm,
+                                                             int32_t* seg_start, int32_t* seg_id,
+                                                             int32_t* n_seg) {
+  __shared__ int warp_tot[32];
+  __shared__ int total;
+  segment_pass(keys, T, perm, seg_start, seg_id, n_seg, warp_tot, &total);
+}
+
+}  // namespace
+
+size_t route_scratch_bytes(int64_t T) {
+  return 2 * align_up(size_t(T) * sizeof(uint64_t), kAlign);
+}
+
+// Sorted keys end up in the returned buffer (one of the two scratch halves).
+cudaError_t launch_route(const int32_t* ids, int64_t T, int64_t vocab, void* scratch,
+                         RouteOut out, DevStatus* st, cudaStream_t stream,
+                         const uint64_t** sorted_keys) {
+  uint64_t* k0 = static_cast<uint64_t*>(scratch);
+  uint64_t* k1 = reinterpret_cast<uint64_t*>(static_cast<char*>(scratch) +
+                                             align_up(size_t(T) * sizeof(uint64_t), kAlign));
+  if (T <= kChunk) {
+    route_small_kernel<<<1, 1024, 0, stream>>>(ids, T, vocab, k0, out.perm, out.seg_start,
+                                               out.seg_id, out.n_seg, st);
+    count_launch();
+    *sorted_keys = k0;
+    return cudaGetLastError();
+  }
+  const int64_t nchunks = (T + kChunk - 1) / kChunk;
+  route_chunk_kernel<<<unsigned(nchunks), 1024, 0, stream>>>(ids, T, vocab, k0, st);
+  count_launch();
+  uint64_t *src = k0, *dst = k1;
+  for (int64_t w = kChunk; w < T; w *= 2) {
+    route_merge_kernel<<<unsigned((T + 255) / 256), 256, 0, stream>>>(src, dst, T, w);
+    count_launch();
+    uint64_t* t = src;
+    src = dst;
+    dst = t;
+  }
+  route_segment_kernel<<<1, 1024, 0, stream>>>(src, T, out.perm, out.seg_start, out.seg_id,
+                                               out.n_seg);
+  count_launch();
+  *sorted_keys = src;
+  return cudaGetLastError();
+}
+
+}  // namespace l3
