@@ -75,7 +75,9 @@ def load_peaks():
 # ---- clocks --------------------------------------------------------------------------------------
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples (every 50 ms) kept for the window around the timed region."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -83,6 +85,7 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.path = None
+        self.t0 = self.t1 = None
 
     def start(self):
         fd, self.path = tempfile.mkstemp(prefix="l3clk", suffix=".csv")
@@ -90,12 +93,25 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
+            return
+        deadline = time.time() + 5.0
+        while time.time() < deadline and os.path.getsize(self.path) == 0:
+            time.sleep(0.02)
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+        time.sleep(0.15)
 
     def stop(self) -> dict:
+        import datetime
+
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -103,25 +119,29 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        sm, mx, reasons = [], [], set()
+        rows = []
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
         with open(self.path) as f:
             for line in f:
                 parts = [s.strip() for s in line.split(",")]
-                if len(parts) < 9:
+                if len(parts) < 10:
                     continue
                 try:
-                    sm.append(float(parts[1]))
-                    mx.append(float(parts[2]))
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
                 except ValueError:
                     continue
-                for nm, val in zip(names, parts[5:9]):
-                    if val.lower().startswith("active"):
-                        reasons.add(nm)
         os.unlink(self.path)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        lo, hi = (self.t0 or 0) - 0.1, (self.t1 or 1e30) + 0.1
+        win = [r for r in rows if lo <= r[0] <= hi]
+        if not win and rows:  # timed region shorter than the sampling interval: nearest sample
+            mid = 0.5 * ((self.t0 or 0) + (self.t1 or 0))
+            win = [min(rows, key=lambda r: abs(r[0] - mid))]
+        reasons = sorted({nm for r in win for nm, val in zip(names, r[3])
+                          if val.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[1] for r in win) if win else None,
+                "sm_max_mhz": max(r[2] for r in win) if win else None, "reasons": reasons,
+                "samples": len(win)}
 
 
 # ---- the CPU oracle as a baseline ------------------------------------------------------------------
@@ -272,13 +292,15 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize()
 
     clk = ClockSampler(local_rank)
-    barrier()
     clk.start()
+    barrier()
+    clk.mark_start()
     n0 = l3.l3_launch_count()
     for k in range(args.steps):
         flush.zero_()
         l3.l3_forward_timed(L, ids, x, y, ws, evs[k])
     barrier()
+    clk.mark_end()
     launches = l3.l3_launch_count() - n0
     clocks = clk.stop()
     step_ms = [evs[k][0].elapsed_time(evs[k][nst]) for k in range(args.steps)]
@@ -289,7 +311,7 @@ def run_ours(args, rank, world, local_rank):
         t = torch.tensor([total_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms = float(t.item())
-    value = world * T / (total_ms / 1e3)
+    value = world * T * args.steps / (total_ms / 1e3)
 
     # end to end through the host-buffer entry point
     ws_h = torch.empty(l3.l3_workspace_size(L, T, l3.L3_PASS_FORWARD_HOST), dtype=torch.uint8,
@@ -354,7 +376,7 @@ def run_ours(args, rank, world, local_rank):
                        "frac_of_measured": acct["attend_bytes"] / attend_s / 1e9 / peaks["hbm_gbs"],
                        "unique_rows": acct["unique_rows"], "distinct_ids": acct["distinct_ids"]},
         "roofline": roof,
-        "e2e": {"value": world * T / (e2e_ms / 1e3), "unit": "tokens/s",
+        "e2e": {"value": world * T * args.steps / (e2e_ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": T * 4 + T * p.d * esz, "d2h_bytes_per_step": T * p.d * esz},
         "fwd_bwd": fb,
         "gpu_launches": launches,
