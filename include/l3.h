@@ -17,15 +17,16 @@
  *   - All pointers named *_host are host memory; every other pointer is device memory
  *     on the current CUDA device. The caller owns all memory. The library never
  *     allocates device memory: scratch comes from a caller-provided workspace sized by
- *     l3_workspace_size.
+ *     l3_workspace_size (l3_route_noalloc alone uses a fixed array the library declares).
  *   - Device work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
  *     legacy default stream). Argument errors are returned before anything is enqueued.
  *   - Matrices are dense row-major. Element types: L3_F32 (float) or L3_BF16 (bfloat16,
  *     accumulation in fp32).
  *   - Errors found on the device (a token id outside [0, vocab), a bad offsets table, a
  *     bounded wait that ran out) never trap: a kernel records them in the workspace's
- *     status words, and l3_get_error reports them. The output rows concerned are then
- *     unspecified.
+ *     status words, and l3_get_error reports them. Every call clears the status words of
+ *     its workspace when it starts, so l3_get_error reports the most recent call. The
+ *     output rows concerned are then unspecified.
  *   - A workspace (and a saved-state buffer) must not be used by two calls that can run
  *     at the same time. No C++ exception crosses this interface.
  */
@@ -69,7 +70,7 @@ enum { L3_F32 = 0, L3_BF16 = 1 };
  *   W_up   [d, d_v]   dtype  (out x in): u = W_up a
  *   W_mix  [d, 2d]    dtype  (out x in): y = W_mix [h; x]; columns 0..d-1 act on the
  *                            LayerNorm output h, columns d..2d-1 on x.
- * Supported: 1 <= k_max <= 512; d and d_v multiples of 64 with 64 <= d <= 4096 and
+ * Supported: 1 <= k_max <= 512; d and d_v multiples of 64 with 64 <= d <= 2048 and
  * 64 <= d_v <= 512; v < 2^31; vocab < 2^31. LayerNorm is over the d features, biased
  * variance, no affine, epsilon ln_eps (> 0; 1e-5 is the usual value).
  */
@@ -149,6 +150,27 @@ l3_status l3_route(const l3_layer* layer, const int32_t* ids, int64_t T, int32_t
                    size_t ws_bytes, l3_stream_t stream);
 
 /*
+ * l3_route_noalloc: l3_route without a workspace. The paper has no counterpart to this
+ * entry point; it exists for callers that cannot allocate device memory when they need
+ * the sort — for example a plugin inside a host program that owns every device
+ * allocation and offers no hook for more, or a latency-critical loop that must not enter
+ * an allocator. Its scratch is a fixed array of about 1 MiB declared by the library in
+ * device memory (each GPU that loads the library holds it until the process exits);
+ * nothing is allocated or freed by this call.
+ *   ids, perm, seg_start, seg_id: as for l3_route (perm, seg_start, seg_id may be NULL)
+ *   n_seg  [1] int32 out, required: the number of segments, or -1 if some token id was
+ *          outside [0, vocab) (the other outputs are then unspecified)
+ * Only layer->vocab is read. T may be 0; T > 65536 returns L3_ERR_WORKSPACE. The first
+ * call on a device looks up the array's device address with that device current, so
+ * make that first call before any stream capture. Every call shares the one array and
+ * clears its status words on entry; calls whose GPU work overlaps (on streams with no
+ * ordering between them) race on it.
+ */
+l3_status l3_route_noalloc(const l3_layer* layer, const int32_t* ids, int64_t T,
+                           int32_t* perm, int32_t* seg_start, int32_t* seg_id,
+                           int32_t* n_seg, l3_stream_t stream);
+
+/*
  * Forward pass (explainer, "Core Architecture", the layer formula), for each token i:
  *   s = K_t x_i (t = ids[i]); p = softmax(s) (no temperature); a_i = V_tᵀ p;
  *   u_i = W_up a_i; h_i = LayerNorm(u_i); y_i = W_mix [h_i; x_i].
@@ -205,8 +227,8 @@ l3_status l3_backward(const l3_layer* layer, const int32_t* ids, int64_t T, cons
                       l3_stream_t stream);
 
 /*
- * Synchronise `stream`, then read and clear the status words that kernels of earlier
- * calls wrote into `ws`. Returns L3_OK, L3_ERR_TOKEN_RANGE, L3_ERR_LAYER,
+ * Synchronise `stream`, then read and clear the status words that the kernels of the
+ * most recent call on `ws` wrote there. Returns L3_OK, L3_ERR_TOKEN_RANGE, L3_ERR_LAYER,
  * L3_ERR_TIMEOUT or L3_ERR_CUDA (the first that applies, in that order of priority
  * after L3_ERR_CUDA).
  */

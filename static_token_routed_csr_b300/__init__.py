@@ -18,7 +18,7 @@ __all__ = [
     "L3Error", "L3Layer", "lib", "make_layer", "L3_F32", "L3_BF16",
     "L3_PASS_FORWARD", "L3_PASS_BACKWARD", "L3_PASS_FORWARD_HOST", "L3_FWD_STAGES",
     "STAGE_NAMES", "l3_alloc_offsets", "l3_workspace_size", "l3_saved_size",
-    "l3_check_layer", "l3_route", "l3_forward", "l3_forward_timed", "l3_forward_host",
+    "l3_check_layer", "l3_route", "l3_route_noalloc", "l3_forward", "l3_forward_timed", "l3_forward_host",
     "l3_backward", "l3_get_error", "l3_status_string", "l3_launch_count", "l3_abi_version",
 ]
 
@@ -59,6 +59,7 @@ _SIGNATURES = {
     "l3_saved_size": (_SZ, [_LP, _I64]),
     "l3_check_layer": (_I32, [_LP, _P, _SZ, _P]),
     "l3_route": (_I32, [_LP, _P, _I64, _P, _P, _P, _P, _P, _SZ, _P]),
+    "l3_route_noalloc": (_I32, [_LP, _P, _I64, _P, _P, _P, _P, _P]),
     "l3_forward": (_I32, [_LP, _P, _I64, _P, _P, _I32, _P, _P, _SZ, _P]),
     "l3_forward_timed": (_I32, [_LP, _P, _I64, _P, _P, _I32, _P, _P, _SZ, _P, _P]),
     "l3_forward_host": (_I32, [_LP, _P, _I64, _P, _P, _I32, _P, _SZ, _P]),
@@ -166,6 +167,14 @@ def l3_route(layer: L3Layer, ids, ws, perm=None, seg_start=None, seg_id=None, n_
     _check(lib().l3_route(ctypes.byref(layer), _ptr(ids), T, _ptr(perm), _ptr(seg_start),
                           _ptr(seg_id), _ptr(n_seg), _ptr(ws), ws.numel() * ws.element_size(),
                           _stream(stream)), "l3_route")
+
+
+def l3_route_noalloc(layer: L3Layer, ids, n_seg, perm=None, seg_start=None, seg_id=None,
+                     stream=None) -> None:
+    """l3_route without a workspace (the library's own fixed scratch; see include/l3.h)."""
+    _check(lib().l3_route_noalloc(ctypes.byref(layer), _ptr(ids), ids.numel(), _ptr(perm),
+                                  _ptr(seg_start), _ptr(seg_id), _ptr(n_seg), _stream(stream)),
+           "l3_route_noalloc")
 
 
 def l3_forward(layer: L3Layer, ids, x, y, ws, saved=None, stream=None) -> None:
