@@ -313,6 +313,12 @@ def run_ours(args, rank, world, local_rank):
         total_ms = float(t.item())
     value = world * T * args.steps / (total_ms / 1e3)
 
+    if args.fwd_only:
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": world * T * args.steps / (total_ms / 1e3),
+                              "unit": "tokens/s", "stage_ms": dict(zip(l3.STAGE_NAMES, stage_ms)),
+                              "note": "forward only (profiling run)"}), flush=True)
+        return 0
     # end to end through the host-buffer entry point
     ws_h = torch.empty(l3.l3_workspace_size(L, T, l3.L3_PASS_FORWARD_HOST), dtype=torch.uint8,
                        device=dev)
@@ -437,6 +443,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--config", type=int, default=2, choices=sorted(W.PRESETS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fwd-only", action="store_true",
+                    help="skip the e2e and fwd+bwd legs (for profiler captures)")
     ap.add_argument("--ref-tokens", type=int, default=128,
                     help="tokens per reference-arm step")
     args = ap.parse_args(argv)

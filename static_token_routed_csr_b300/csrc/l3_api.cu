@@ -54,11 +54,15 @@ struct FwdWs {
   float* part;
   float* a_f32;
   __nv_bfloat16* a_bf16;
+  // fp32 layers (CUDA-core GEMMs)
   float* U;
   float* mu;
   float* rstd;
   float* H;
-  float* Y;
+  // bf16 layers (tensor-core GEMMs)
+  __nv_bfloat16* U16;
+  float* stats;
+  float* colsum;
   int n_split;
 };
 
@@ -73,13 +77,18 @@ FwdWs carve_fwd(Carve& c, const l3_layer* L, int64_t T) {
   w.n_seg = c.take<int32_t>(1);
   w.n_split = attend_choose_split(T, L->k_max);
   w.part = c.take<float>(attend_part_floats(T, w.n_split, L->d_v));
-  w.a_f32 = c.take<float>(t * dv);
-  w.a_bf16 = L->dtype == L3_BF16 ? c.take<__nv_bfloat16>(t * dv) : nullptr;
-  w.U = c.take<float>(t * d);
   w.mu = c.take<float>(t);
   w.rstd = c.take<float>(t);
-  w.H = c.take<float>(t * d);
-  w.Y = c.take<float>(t * d);
+  if (L->dtype == L3_BF16) {
+    w.a_bf16 = c.take<__nv_bfloat16>(t * dv);
+    w.U16 = c.take<__nv_bfloat16>(t * d);
+    w.stats = c.take<float>(size_t(tc_up_stat_tiles(int(d))) * t * 2);
+    w.colsum = c.take<float>(d);
+  } else {
+    w.a_f32 = c.take<float>(t * dv);
+    w.U = c.take<float>(t * d);
+    w.H = c.take<float>(t * d);
+  }
   return w;
 }
 
@@ -186,7 +195,7 @@ l3_status forward_impl(const l3_layer* L, const int32_t* ids, int64_t T, const v
   aa.d_v = dv;
   aa.k_max = L->k_max;
   aa.dtype = L->dtype;
-  aa.a_f32 = (L->dtype == L3_F32 || saved) ? a_f32 : nullptr;
+  aa.a_f32 = (L->dtype == L3_F32 || saved) ? a_f32 : nullptr;  // fp32 copy for backward
   aa.a_bf16 = w.a_bf16;
   aa.ml = saved ? sv.ml : nullptr;
   aa.part = w.part;
@@ -194,22 +203,32 @@ l3_status forward_impl(const l3_layer* L, const int32_t* ids, int64_t T, const v
   L3_CUDA(launch_attend_fwd(aa, s));
 
   if (ev) L3_CUDA(cudaEventRecord(ev[L3_STAGE_UP], s));
+  if (L->dtype == L3_BF16) {
+    // Tensor cores: U = bf16(A W_upᵀ) with partial LayerNorm statistics, then
+    // y = rstd (U W1ᵀ - mu c) + x W2ᵀ with the statistics merged in the epilogue.
+    const auto* Wmix = static_cast<const __nv_bfloat16*>(L->W_mix);
+    L3_CUDA(launch_rowsum(Wmix, d, 2 * d, d, w.colsum, s));
+    L3_CUDA(launch_tc_up(w.a_bf16, static_cast<const __nv_bfloat16*>(L->W_up), T, d, dv, w.U16,
+                         w.stats, w.st, s));
+    if (ev) L3_CUDA(cudaEventRecord(ev[L3_STAGE_MIX], s));
+    L3_CUDA(launch_tc_mix(w.U16, static_cast<const __nv_bfloat16*>(x), Wmix, T, d, w.stats,
+                          w.colsum, L->ln_eps, y, y_dtype, saved ? sv.mu : nullptr,
+                          saved ? sv.rstd : nullptr, w.st, s));
+    if (ev) L3_CUDA(cudaEventRecord(ev[L3_FWD_STAGES], s));
+    return L3_OK;
+  }
+  // fp32 layers: CUDA-core GEMMs (fp32 parity rules out tf32 tensor cores).
   // u = W_up a: U[i, n] = sum_k A[i, k] W_up[n, k]
   SimtGemm up{};
   up.M = T;
   up.N = d;
   up.K = dv;
-  if (L->dtype == L3_BF16) {
-    up.A = w.a_bf16;
-    up.a_dtype = L3_BF16;
-  } else {
-    up.A = a_f32;
-    up.a_dtype = L3_F32;
-  }
+  up.A = a_f32;
+  up.a_dtype = L3_F32;
   up.a_sm = dv;
   up.a_sk = 1;
   up.B = L->W_up;
-  up.b_dtype = L->dtype;
+  up.b_dtype = L3_F32;
   up.b_sk = 1;
   up.b_sn = dv;
   up.C = w.U;
@@ -221,8 +240,8 @@ l3_status forward_impl(const l3_layer* L, const int32_t* ids, int64_t T, const v
 
   if (ev) L3_CUDA(cudaEventRecord(ev[L3_STAGE_MIX], s));
   L3_CUDA(launch_ln_apply(w.U, mu, rstd, T, d, w.H, s));
-  float* Y = y_dtype == L3_F32 ? static_cast<float*>(y) : w.Y;
-  // y = W_mix[:, :d] h + W_mix[:, d:] x
+  // y = W_mix[:, :d] h + W_mix[:, d:] x (fp32 y: y_dtype must be L3_F32 here)
+  float* Y = static_cast<float*>(y);
   SimtGemm mix{};
   mix.M = T;
   mix.N = d;
@@ -232,7 +251,7 @@ l3_status forward_impl(const l3_layer* L, const int32_t* ids, int64_t T, const v
   mix.a_sm = d;
   mix.a_sk = 1;
   mix.B = L->W_mix;
-  mix.b_dtype = L->dtype;
+  mix.b_dtype = L3_F32;
   mix.b_sk = 1;
   mix.b_sn = 2 * d;
   mix.C = Y;
@@ -241,11 +260,9 @@ l3_status forward_impl(const l3_layer* L, const int32_t* ids, int64_t T, const v
   mix.beta = 0.f;
   L3_CUDA(launch_simt_gemm(mix, s));
   mix.A = x;
-  mix.a_dtype = L->dtype;
-  mix.B = static_cast<const char*>(L->W_mix) + size_t(d) * esize(L->dtype);
+  mix.B = static_cast<const float*>(L->W_mix) + d;
   mix.beta = 1.f;
   L3_CUDA(launch_simt_gemm(mix, s));
-  if (y_dtype != L3_F32) L3_CUDA(launch_cast(Y, y, y_dtype, T * d, s));
   if (ev) L3_CUDA(cudaEventRecord(ev[L3_FWD_STAGES], s));
   return L3_OK;
 }

@@ -235,3 +235,17 @@ def test_backward_deterministic_and_untouched_rows_zero():
         present[c.offs_np[t]:c.offs_np[t + 1]] = True
     dK = g1["dK"].cpu().numpy()
     assert not dK[~present].any()
+
+
+def test_forward_bf16_saved_state_and_layernorm_statistics():
+    c = Case(2, T=1000)
+    y, sv = c.forward(saved=True)
+    torch.cuda.synchronize()
+    fw = c.oracle_forward()
+    a, ml, mu, rstd = c.saved_views(sv)
+    # a is the fp32 attend output (before any bf16 rounding); mu/rstd come from the
+    # tensor-core epilogue, computed on bf16-rounded u
+    assert_fp32_close(to_np(a), fw.a, "a (fp32 copy)")
+    np.testing.assert_allclose(to_np(rstd), fw.rstd, rtol=1e-2)
+    np.testing.assert_allclose(to_np(mu), fw.mu, rtol=0, atol=2e-2 * np.abs(fw.u).max())
+    assert_close(c.p, to_np(y), fw.y, "y")
