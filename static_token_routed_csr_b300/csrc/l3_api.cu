@@ -63,6 +63,11 @@ struct FwdWs {
   __nv_bfloat16* U16;
   float* stats;
   float* colsum;
+  // tensor-core gather-attend
+  __nv_bfloat16* x_sorted;
+  void* items;
+  int32_t* n_items;
+  bool attend_tc;
   int n_split;
 };
 
@@ -79,6 +84,12 @@ FwdWs carve_fwd(Carve& c, const l3_layer* L, int64_t T) {
   w.part = c.take<float>(attend_part_floats(T, w.n_split, L->d_v));
   w.mu = c.take<float>(t);
   w.rstd = c.take<float>(t);
+  w.attend_tc = attend_tc_supported(T, int(d), int(dv), L->dtype);
+  if (w.attend_tc) {
+    w.x_sorted = c.take<__nv_bfloat16>(t * d);
+    w.items = c.raw(attend_tc_items_bytes(T));
+    w.n_items = c.take<int32_t>(1);
+  }
   if (L->dtype == L3_BF16) {
     w.a_bf16 = c.take<__nv_bfloat16>(t * dv);
     w.U16 = c.take<__nv_bfloat16>(t * d);
@@ -200,7 +211,30 @@ l3_status forward_impl(const l3_layer* L, const int32_t* ids, int64_t T, const v
   aa.ml = saved ? sv.ml : nullptr;
   aa.part = w.part;
   aa.n_split = w.n_split;
-  L3_CUDA(launch_attend_fwd(aa, s));
+  if (w.attend_tc) {
+    AttendTcArgs at{};
+    at.sorted_keys = keys;
+    at.seg_start = w.seg_start;
+    at.n_seg = w.n_seg;
+    at.T = T;
+    at.offs = L->offs;
+    at.K = L->K;
+    at.V = L->V;
+    at.x = x;
+    at.v = L->v;
+    at.d = d;
+    at.d_v = dv;
+    at.x_sorted = w.x_sorted;
+    at.items = w.items;
+    at.n_items = w.n_items;
+    at.a_bf16 = w.a_bf16;
+    at.a_f32 = aa.a_f32;
+    at.ml = aa.ml;
+    at.st = w.st;
+    L3_CUDA(launch_attend_tc(at, s));
+  } else {
+    L3_CUDA(launch_attend_fwd(aa, s));
+  }
 
   if (ev) L3_CUDA(cudaEventRecord(ev[L3_STAGE_UP], s));
   if (L->dtype == L3_BF16) {

@@ -1,0 +1,591 @@
+// Gather-attend forward on tcgen05 tensor cores, one segment of equal token ids at a time
+// ("L³: Large Lookup Layers", gist.science explainer, Technical Summary: "Core
+// Architecture" for the aggregation a = V_tᵀ softmax(K_t x); "Systems-Friendly Design",
+// batch sorting, for grouping the tokens of one id so that its rows are read once).
+//
+// A work item is one id t with up to 64 of its tokens (longer segments are cut into
+// 64-token chunks). With n = n_t rows and the item's tokens X (sorted order, N = 16..64
+// columns):
+//   phase 1   Sᵀ = K_t Xᵀ           M = 128 table rows per chunk (TMEM lanes), N tokens,
+//                                    K = d in 64-wide blocks; up to 4 row chunks.
+//   softmax   per token: m = max_rows s, e = exp(s - m) (rows >= n give 0), l = sum e;
+//             Pᵀ = bf16(e) is written to shared memory as the phase-2 B operand.
+//   phase 2   Aᵀ = V_tᵀ Pᵀ           M = 128 value columns per chunk, N tokens, K = rows
+//                                    in 16-row steps (both operands MN-major).
+//   epilogue  a = Aᵀ / l, scattered to batch order (bf16 for the GEMM, fp32 if asked).
+// K_t, V_t rows arrive by TMA in 16-row boxes, so an id with few rows moves few bytes.
+// One persistent CTA per SM, 6 warps: TMA producer, MMA issuer, 4 softmax/epilogue
+// warps (one TMEM lane each). All waits are bounded; the softmax warps synchronise on an
+// mbarrier (bounded) rather than a named barrier, so no thread can be left waiting.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "l3_internal.h"
+#include "l3_tc.cuh"
+
+namespace l3 {
+
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kNT = 64;            // tokens per item
+constexpr int kStages = 6;
+constexpr int kKTile = 128 * 128;  // 128 rows x 64 bf16
+constexpr int kXTile = kNT * 128;  // 64 tokens x 64 bf16
+constexpr int kStageBytes = kKTile + kXTile;
+constexpr int kPBytes = 512 * 128;  // Pᵀ: up to 512 rows x 64 tokens bf16
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSCol = 0;    // Sᵀ chunk rc at columns 64 rc
+constexpr uint32_t kACol = 256;  // Aᵀ chunk dc at columns 256 + 64 dc
+constexpr int kSmemBytes = kStages * kStageBytes + kPBytes + 7 * kNT * 4 + 256 + 1024;
+
+struct Item {
+  int32_t q0;  // first sorted position
+  int32_t nt;  // tokens (1..64)
+  int32_t t;   // token id
+  int32_t pad;
+};
+
+struct TcAttendParams {
+  const Item* items;
+  const int32_t* n_items;
+  const uint64_t* sorted_keys;
+  const int32_t* offs;
+  int d, d_v;
+  __nv_bfloat16* a_bf16;  // [T, d_v] batch order
+  float* a_f32;           // nullable
+  float* ml;              // nullable [T, 2]
+  DevStatus* st;
+};
+
+// MN-major operand in the 128-byte swizzle: 64 elements (128 B) contiguous along M/N, K
+// rows 128 B apart in 8-row groups of 1024 B; further 64-element M/N blocks lbo bytes on.
+__device__ __forceinline__ uint64_t desc_mnmajor_sw128(uint32_t addr, uint32_t lbo_bytes) {
+  uint64_t d = 0;
+  d |= uint64_t((addr >> 4) & 0x3FFFu);
+  d |= uint64_t((lbo_bytes >> 4) & 0x3FFFu) << 16;  // stride between 64-element MN blocks
+  d |= uint64_t(1024 >> 4) << 32;                   // stride between 8-row K groups
+  d |= uint64_t(1) << 46;
+  d |= uint64_t(2) << 61;
+  return d;
+}
+
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
+  return tc::idesc_bf16_f32(M, N) | (uint32_t(a_mn) << 15) | (uint32_t(b_mn) << 16);
+}
+
+// Wait that ends only when the phase completes or this thread's own time limit runs out
+// (then it raises the CTA's abort flag): used where all 128 softmax threads must take
+// the same path, so no thread leaves a phase the others complete.
+__device__ __forceinline__ bool wait_own(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                         DevStatus* st, int code) {
+  volatile int never = 0;
+  if (tc::mbar_wait(bar, parity, &never, st, code)) return true;
+  *abort = 1;
+  return false;
+}
+
+// Barrier of the 128 softmax threads on an mbarrier (count 128), bounded.
+__device__ __forceinline__ bool group_sync(uint64_t* bar, uint32_t& phase, volatile int* abort,
+                                           DevStatus* st) {
+  tc::mbar_arrive(bar);
+  const bool ok = wait_own(bar, phase, abort, st, 0x4000);
+  phase ^= 1;
+  return ok;
+}
+
+// Butterfly reduce-scatter over 32 lanes of a 64-vector: afterwards v[0], v[1] hold the
+// reduction for entries 2*lane and 2*lane + 1.
+template <bool kMax>
+__device__ __forceinline__ void reduce_scatter64(float (&v)[64], int lane) {
+#pragma unroll
+  for (int step = 0; step < 5; ++step) {
+    const int o = 16 >> step;
+    const int half = 32 >> step;
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float lo = v[i], hi = v[i + half];
+      const float send = up ? lo : hi;
+      const float keep = up ? hi : lo;
+      const float got = __shfl_xor_sync(0xffffffffu, send, o);
+      v[i] = kMax ? fmaxf(keep, got) : keep + got;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    attend_tc_kernel(const __grid_constant__ CUtensorMap mapK,
+                     const __grid_constant__ CUtensorMap mapX,
+                     const __grid_constant__ CUtensorMap mapV, const TcAttendParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* stages = smem;
+  unsigned char* pbuf = smem + kStages * kStageBytes;
+  float* red = reinterpret_cast<float*>(pbuf + kPBytes);    // [4][64]
+  float* fin_m = red + 4 * kNT;                              // [64]
+  float* fin_l = fin_m + kNT;                                // [64]
+  int32_t* orig = reinterpret_cast<int32_t*>(fin_l + kNT);  // [64]
+  uint64_t* full = reinterpret_cast<uint64_t*>(orig + kNT);
+  uint64_t* empty = full + kStages;
+  uint64_t* s_full = empty + kStages;
+  uint64_t* s_free = s_full + 1;
+  uint64_t* a_full = s_free + 1;
+  uint64_t* a_free = a_full + 1;
+  uint64_t* drain = a_free + 1;
+  uint64_t* grp = drain + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(grp + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // Stage buffers start zeroed so that rows a partial TMA box leaves untouched are finite.
+  for (int i = threadIdx.x; i < kStages * kStageBytes / 16; i += kThreads)
+    reinterpret_cast<uint4*>(stages)[i] = make_uint4(0, 0, 0, 0);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 1);
+    }
+    tc::mbar_init(s_full, 1);
+    tc::mbar_init(s_free, 4);
+    tc::mbar_init(a_full, 1);
+    tc::mbar_init(a_free, 4);
+    tc::mbar_init(drain, 1);
+    tc::mbar_init(grp, 128);
+    *abort_flag = 0;
+    tc::fence_barrier_init();
+  }
+  tc::fence_proxy_async();
+  if (warp == 1) tc::tmem_alloc(tmem_slot, kTmemCols);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int n_items = *p.n_items;
+  const int KB = p.d / 64;
+  const int DC = p.d_v / 128;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tc::tma_prefetch_desc(&mapK);
+      tc::tma_prefetch_desc(&mapX);
+      tc::tma_prefetch_desc(&mapV);
+      uint32_t it = 0;
+      bool ok = true;
+      for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
+        const Item item = p.items[i];
+        const int r0 = p.offs[item.t];
+        const int n = p.offs[item.t + 1] - r0;
+        const int Nt = (item.nt + 15) & ~15;
+        const int RC = (n + 127) / 128;
+        for (int rc = 0; ok && rc < RC; ++rc) {
+          const int nvalid = n - 128 * rc < 128 ? n - 128 * rc : 128;
+          const int nbox = (nvalid + 15) / 16;
+          for (int kb = 0; kb < KB; ++kb) {
+            const uint32_t s = it % kStages, ph = (it / kStages) & 1;
+            if (!tc::mbar_wait(&empty[s], ph ^ 1, abort_flag, p.st, 0x100)) {
+              ok = false;
+              break;
+            }
+            unsigned char* st = stages + s * kStageBytes;
+            tc::mbar_arrive_expect_tx(&full[s], uint32_t(nbox + Nt / 16) * 2048u);
+            for (int bx = 0; bx < nbox; ++bx)
+              tc::tma_load_2d(&mapK, &full[s], st + bx * 2048, kb * 64, r0 + 128 * rc + 16 * bx);
+            for (int bx = 0; bx < Nt / 16; ++bx)
+              tc::tma_load_2d(&mapX, &full[s], st + kKTile + bx * 2048, kb * 64,
+                              item.q0 + 16 * bx);
+            ++it;
+          }
+        }
+        const int NB = (n + 63) / 64;
+        for (int b = 0; ok && b < NB; ++b) {
+          const int vrows = n - 64 * b < 64 ? n - 64 * b : 64;
+          const int nbox = (vrows + 15) / 16;
+          for (int dc = 0; dc < DC; ++dc) {
+            const uint32_t s = it % kStages, ph = (it / kStages) & 1;
+            if (!tc::mbar_wait(&empty[s], ph ^ 1, abort_flag, p.st, 0x100)) {
+              ok = false;
+              break;
+            }
+            unsigned char* st = stages + s * kStageBytes;
+            tc::mbar_arrive_expect_tx(&full[s], uint32_t(2 * nbox) * 2048u);
+            for (int h = 0; h < 2; ++h)
+              for (int bx = 0; bx < nbox; ++bx)
+                tc::tma_load_2d(&mapV, &full[s], st + h * 8192 + bx * 2048, dc * 128 + h * 64,
+                                r0 + 64 * b + 16 * bx);
+            ++it;
+          }
+        }
+      }
+      if (!ok) {
+        // Let the copies already issued land before the CTA's shared memory goes away.
+        const uint32_t first = it > uint32_t(kStages) ? it - kStages : 0;
+        volatile int no_abort = 0;
+        for (uint32_t j = first; j < it; ++j)
+          tc::mbar_wait(&full[j % kStages], (j / kStages) & 1, &no_abort, p.st, 0x1000,
+                        100000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      uint32_t it = 0, item_no = 0;
+      bool ok = true;
+      for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x, ++item_no) {
+        const Item item = p.items[i];
+        const int r0 = p.offs[item.t];
+        const int n = p.offs[item.t + 1] - r0;
+        const int Nt = (item.nt + 15) & ~15;
+        const int RC = (n + 127) / 128;
+        const uint32_t id1 = idesc_bf16(128, Nt, 0, 0);
+        const uint32_t id2 = idesc_bf16(128, Nt, 1, 1);
+        // phase 1: Sᵀ = K_t Xᵀ
+        for (int rc = 0; ok && rc < RC; ++rc) {
+          for (int kb = 0; kb < KB; ++kb) {
+            const uint32_t s = it % kStages, ph = (it / kStages) & 1;
+            if (!tc::mbar_wait(&full[s], ph, abort_flag, p.st, 0x200)) {
+              ok = false;
+              break;
+            }
+            tc::tc_fence_after();
+            const uint32_t a_addr = tc::smem_u32(stages + s * kStageBytes);
+            const uint32_t b_addr = a_addr + kKTile;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              tc::mma_bf16(tmem + kSCol + 64 * rc, tc::desc_kmajor_sw128(a_addr + 32 * k),
+                           tc::desc_kmajor_sw128(b_addr + 32 * k), id1,
+                           (kb > 0 || k > 0) ? 1u : 0u);
+            tc::mma_commit(&empty[s]);
+            ++it;
+          }
+        }
+        if (!ok) break;
+        tc::mma_commit(s_full);
+        // phase 2 needs Pᵀ (softmax done) and a free Aᵀ (previous epilogue done)
+        if (!tc::mbar_wait(s_free, item_no & 1, abort_flag, p.st, 0x400)) break;
+        if (!tc::mbar_wait(a_free, (item_no & 1) ^ 1, abort_flag, p.st, 0x400)) break;
+        tc::tc_fence_after();
+        const int NB = (n + 63) / 64;
+        const uint32_t p_addr = tc::smem_u32(pbuf);
+        for (int b = 0; ok && b < NB; ++b) {
+          for (int dc = 0; dc < DC; ++dc) {
+            const uint32_t s = it % kStages, ph = (it / kStages) & 1;
+            if (!tc::mbar_wait(&full[s], ph, abort_flag, p.st, 0x200)) {
+              ok = false;
+              break;
+            }
+            tc::tc_fence_after();
+            const uint32_t v_addr = tc::smem_u32(stages + s * kStageBytes);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              tc::mma_bf16(tmem + kACol + 64 * dc, desc_mnmajor_sw128(v_addr + 2048 * k, 8192),
+                           desc_mnmajor_sw128(p_addr + 8192 * b + 2048 * k, 8192), id2,
+                           (b > 0 || k > 0) ? 1u : 0u);
+            tc::mma_commit(&empty[s]);
+            ++it;
+          }
+        }
+        if (!ok) break;
+        tc::mma_commit(a_full);
+      }
+      // All MMAs issued by this thread must finish before TMEM is released.
+      tc::mma_commit(drain);
+      volatile int no_abort = 0;
+      tc::mbar_wait(drain, 0, &no_abort, p.st, 0x2000, 100000000ull);
+    }
+  } else {
+    const int q = warp & 3;
+    const int L = q * 32 + lane;  // TMEM lane: table row in a chunk / value column in a chunk
+    const uint32_t lane_base = tmem + (uint32_t(q * 32) << 16);
+    uint32_t item_no = 0, gph = 0;
+    for (int i = blockIdx.x; i < n_items; i += gridDim.x, ++item_no) {
+      const Item item = p.items[i];
+      const int r0 = p.offs[item.t];
+      const int n = p.offs[item.t + 1] - r0;
+      const int nt = item.nt;
+      const int RC = (n + 127) / 128;
+      const int NC = (nt + 31) / 32;  // 32-column TMEM loads per chunk
+      if (!wait_own(s_full, item_no & 1, abort_flag, p.st, 0x800)) break;
+      tc::tc_fence_after();
+      if (L < nt) orig[L] = int32_t(uint32_t(p.sorted_keys[item.q0 + L]));
+      // pass 1: per-token max over the rows
+      float v[64];
+#pragma unroll
+      for (int j = 0; j < 64; ++j) v[j] = -INFINITY;
+      for (int rc = 0; rc < RC; ++rc) {
+        const bool valid = 128 * rc + L < n;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          if (c < NC) {
+            float s[32];
+            tc::tmem_ld32(lane_base + kSCol + 64 * rc + 32 * c, s);
+            if (valid)
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[32 * c + j] = fmaxf(v[32 * c + j], s[j]);
+          }
+        }
+      }
+      reduce_scatter64<true>(v, lane);
+      red[q * kNT + 2 * lane] = v[0];
+      red[q * kNT + 2 * lane + 1] = v[1];
+      if (!group_sync(grp, gph, abort_flag, p.st)) break;
+      if (q == 0) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int j = 2 * lane + u;
+          fin_m[j] = fmaxf(fmaxf(red[j], red[kNT + j]), fmaxf(red[2 * kNT + j], red[3 * kNT + j]));
+        }
+      }
+      if (!group_sync(grp, gph, abort_flag, p.st)) break;
+      // pass 2: e = exp(s - m) as bf16 into Pᵀ, and its sum
+#pragma unroll
+      for (int j = 0; j < 64; ++j) v[j] = 0.f;
+      const int rows_written = ((n + 63) / 64) * 64;
+      for (int rc = 0; rc < RC; ++rc) {
+        const int row = 128 * rc + L;
+        const bool valid = row < n;
+        uint32_t packed[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) packed[j] = 0;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          if (c < NC) {
+            float s[32];
+            tc::tmem_ld32(lane_base + kSCol + 64 * rc + 32 * c, s);
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+              const int t0 = 32 * c + j, t1 = t0 + 1;
+              const float e0 = (valid && t0 < nt) ? expf(s[j] - fin_m[t0]) : 0.f;
+              const float e1 = (valid && t1 < nt) ? expf(s[j + 1] - fin_m[t1]) : 0.f;
+              const __nv_bfloat16 b0 = __float2bfloat16_rn(e0), b1 = __float2bfloat16_rn(e1);
+              v[t0] += __bfloat162float(b0);
+              v[t1] += __bfloat162float(b1);
+              packed[16 * c + j / 2] =
+                  uint32_t(__bfloat16_as_ushort(b0)) | (uint32_t(__bfloat16_as_ushort(b1)) << 16);
+            }
+          }
+        }
+        if (row < rows_written) {
+          // row of Pᵀ: 64 tokens = 8 chunks of 16 B, 128-byte swizzle within 8-row groups
+          unsigned char* prow = pbuf + row * 128;
+#pragma unroll
+          for (int c16 = 0; c16 < 8; ++c16)
+            *reinterpret_cast<uint4*>(prow + ((c16 ^ (row & 7)) << 4)) =
+                make_uint4(packed[4 * c16], packed[4 * c16 + 1], packed[4 * c16 + 2],
+                           packed[4 * c16 + 3]);
+        }
+      }
+      tc::fence_proxy_async();
+      reduce_scatter64<false>(v, lane);
+      red[q * kNT + 2 * lane] = v[0];
+      red[q * kNT + 2 * lane + 1] = v[1];
+      if (!group_sync(grp, gph, abort_flag, p.st)) break;
+      if (q == 0) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int j = 2 * lane + u;
+          fin_l[j] = (red[j] + red[kNT + j]) + (red[2 * kNT + j] + red[3 * kNT + j]);
+        }
+      }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(s_free);
+      if (!group_sync(grp, gph, abort_flag, p.st)) break;  // fin_l visible to all four warps
+      // epilogue: a = Aᵀ / l, batch order
+      if (!wait_own(a_full, item_no & 1, abort_flag, p.st, 0x800)) break;
+      tc::tc_fence_after();
+      for (int dc = 0; dc < DC; ++dc) {
+        const int col = 128 * dc + L;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          if (c < NC) {
+            float acc[32];
+            tc::tmem_ld32(lane_base + kACol + 64 * dc + 32 * c, acc);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int tok = 32 * c + j;
+              if (tok < nt) {
+                const float a = acc[j] / fin_l[tok];
+                const int64_t o = int64_t(orig[tok]) * p.d_v + col;
+                p.a_bf16[o] = __float2bfloat16_rn(a);
+                if (p.a_f32) p.a_f32[o] = a;
+              }
+            }
+          }
+        }
+      }
+      if (p.ml && L < nt) {
+        p.ml[2 * int64_t(orig[L])] = fin_m[L];
+        p.ml[2 * int64_t(orig[L]) + 1] = fin_l[L];
+      }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(a_free);
+      if (!group_sync(grp, gph, abort_flag, p.st)) break;  // orig/fin_* are rewritten next
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Items: for each segment, ceil(m / 64) chunks of its tokens, in segment order.
+__global__ void __launch_bounds__(1024) attend_items_kernel(const int32_t* __restrict__ seg_start,
+                                                           const int32_t* __restrict__ n_seg,
+                                                           const uint64_t* __restrict__ keys,
+                                                           Item* items, int32_t* n_items) {
+  __shared__ int warp_tot[32];
+  __shared__ int total;
+  const int S = *n_seg;
+  int carry = 0;
+  for (int base = 0; base < S; base += blockDim.x) {
+    const int s = base + threadIdx.x;
+    int cnt = 0, q0 = 0, m = 0;
+    if (s < S) {
+      q0 = seg_start[s];
+      m = seg_start[s + 1] - q0;
+      cnt = (m + kNT - 1) / kNT;
+    }
+    // exclusive scan of cnt over the CTA
+    const int wl = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, incl, o);
+      if (wl >= o) incl += u;
+    }
+    if (wl == 31) warp_tot[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+      const int w = wl < int(blockDim.x >> 5) ? warp_tot[wl] : 0;
+      int wi = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, wi, o);
+        if (wl >= o) wi += u;
+      }
+      warp_tot[wl] = wi - w;
+      if (wl == 31) total = wi;
+    }
+    __syncthreads();
+    const int ex = carry + warp_tot[wid] + incl - cnt;
+    if (s < S) {
+      const int t = int(keys[q0] >> 32);
+      for (int c = 0; c < cnt; ++c) {
+        Item it;
+        it.q0 = q0 + c * kNT;
+        it.nt = m - c * kNT < kNT ? m - c * kNT : kNT;
+        it.t = t;
+        it.pad = 0;
+        items[ex + c] = it;
+      }
+    }
+    carry += total;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *n_items = carry;
+}
+
+// x_sorted[q] = x[perm(q)] (bf16 rows of d elements), one warp per row.
+__global__ void gather_rows_kernel(const uint64_t* __restrict__ keys, int64_t T,
+                                   const __nv_bfloat16* __restrict__ x, int d,
+                                   __nv_bfloat16* __restrict__ xs) {
+  const int lane = threadIdx.x & 31;
+  const int64_t q = int64_t(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
+  if (q >= T) return;
+  const int64_t i = int64_t(uint32_t(keys[q]));
+  const uint4* src = reinterpret_cast<const uint4*>(x + i * d);
+  uint4* dst = reinterpret_cast<uint4*>(xs + q * d);
+  for (int c = lane; c < d / 8; c += 32) dst[c] = __ldg(src + c);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// bf16 [rows, cols] row-major; box 16 rows x 64 columns, 128-byte swizzle.
+bool make_map16(CUtensorMap* map, const void* base, int64_t rows, int64_t cols) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
+  cuuint64_t strides[1] = {cuuint64_t(cols) * 2};
+  cuuint32_t box[2] = {64, 16};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+}  // namespace
+
+bool attend_tc_supported(int64_t T, int d, int d_v, int dtype) {
+  return dtype == L3_BF16 && T >= 1024 && d % 64 == 0 && d_v % 128 == 0 && d_v <= 512;
+}
+
+size_t attend_tc_items_bytes(int64_t T) { return size_t(2 * T + 1) * sizeof(Item); }
+
+cudaError_t launch_attend_tc(const AttendTcArgs& a, cudaStream_t stream) {
+  if (a.T <= 0) return cudaSuccess;
+  gather_rows_kernel<<<unsigned((a.T + 7) / 8), 256, 0, stream>>>(
+      a.sorted_keys, a.T, static_cast<const __nv_bfloat16*>(a.x), a.d, a.x_sorted);
+  count_launch();
+  Item* items = static_cast<Item*>(a.items);
+  attend_items_kernel<<<1, 1024, 0, stream>>>(a.seg_start, a.n_seg, a.sorted_keys, items,
+                                               a.n_items);
+  count_launch();
+  CUtensorMap mk, mx, mv;
+  if (!make_map16(&mk, a.K, a.v, a.d) || !make_map16(&mx, a.x_sorted, a.T, a.d) ||
+      !make_map16(&mv, a.V, a.v, a.d_v))
+    return cudaErrorInvalidValue;
+  TcAttendParams p{};
+  p.items = items;
+  p.n_items = a.n_items;
+  p.sorted_keys = a.sorted_keys;
+  p.offs = a.offs;
+  p.d = a.d;
+  p.d_v = a.d_v;
+  p.a_bf16 = a.a_bf16;
+  p.a_f32 = a.a_f32;
+  p.ml = a.ml;
+  p.st = a.st;
+  static std::once_flag once;
+  static cudaError_t attr = cudaSuccess;
+  std::call_once(once, [] {
+    attr = cudaFuncSetAttribute(attend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kSmemBytes);
+  });
+  if (attr != cudaSuccess) return attr;
+  attend_tc_kernel<<<sm_count(), kThreads, kSmemBytes, stream>>>(mk, mx, mv, p);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace l3

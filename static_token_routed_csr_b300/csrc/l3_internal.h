@@ -42,6 +42,30 @@ int attend_choose_split(int64_t T, int k_max);
 size_t attend_part_floats(int64_t T, int n_split, int d_v);
 cudaError_t launch_attend_fwd(const AttendArgs& a, cudaStream_t stream);
 
+// ---- gather-attend on tensor cores (l3_attend_tc.cu), bf16 prefill batches -----------------
+struct AttendTcArgs {
+  const uint64_t* sorted_keys;
+  const int32_t* seg_start;
+  const int32_t* n_seg;
+  int64_t T;
+  const int32_t* offs;
+  const void* K;
+  const void* V;
+  const void* x;
+  int64_t v;
+  int d, d_v;
+  __nv_bfloat16* x_sorted;  // [T, d] scratch
+  void* items;              // attend_tc_items_bytes(T) scratch
+  int32_t* n_items;         // [1] scratch
+  __nv_bfloat16* a_bf16;    // [T, d_v]
+  float* a_f32;             // nullable
+  float* ml;                // nullable
+  DevStatus* st;
+};
+bool attend_tc_supported(int64_t T, int d, int d_v, int dtype);
+size_t attend_tc_items_bytes(int64_t T);
+cudaError_t launch_attend_tc(const AttendTcArgs& a, cudaStream_t stream);
+
 // ---- SIMT GEMM and row kernels (l3_gemm_simt.cu) -------------------------------------------
 // C[m, n] (fp32, row stride ldc) = alpha * sum_k A(m, k) B(k, n) + beta * C[m, n]
 // with A(m, k) = A[m*a_sm + k*a_sk], B(k, n) = B[k*b_sk + n*b_sn].

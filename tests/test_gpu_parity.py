@@ -237,15 +237,40 @@ def test_backward_deterministic_and_untouched_rows_zero():
     assert not dK[~present].any()
 
 
-def test_forward_bf16_saved_state_and_layernorm_statistics():
-    c = Case(2, T=1000)
+@pytest.mark.parametrize("T", [1000, 1500])  # CUDA-core attend below 1024 tokens, tensor cores above
+def test_forward_bf16_saved_state_and_layernorm_statistics(T):
+    c = Case(2, T=T)
     y, sv = c.forward(saved=True)
     torch.cuda.synchronize()
     fw = c.oracle_forward()
     a, ml, mu, rstd = c.saved_views(sv)
-    # a is the fp32 attend output (before any bf16 rounding); mu/rstd come from the
-    # tensor-core epilogue, computed on bf16-rounded u
-    assert_fp32_close(to_np(a), fw.a, "a (fp32 copy)")
+    if T < 1024:
+        # fp32 arithmetic on the bf16 inputs
+        assert_fp32_close(to_np(a), fw.a, "a (fp32 copy)")
+        np.testing.assert_allclose(to_np(ml[:, 1]), fw.l, rtol=1e-5)
+    else:
+        # tensor cores take the softmax weights as bf16: relative error ~2^-9
+        err = np.abs(to_np(a) - fw.a).max() / np.abs(fw.a).max()
+        assert err < 1e-2, err
+        np.testing.assert_allclose(to_np(ml[:, 1]), fw.l, rtol=1e-2)
+    np.testing.assert_allclose(to_np(ml[:, 0]), fw.m, rtol=0, atol=1e-3 * np.abs(fw.m).max() + 1e-4)
     np.testing.assert_allclose(to_np(rstd), fw.rstd, rtol=1e-2)
     np.testing.assert_allclose(to_np(mu), fw.mu, rtol=0, atol=2e-2 * np.abs(fw.u).max())
     assert_close(c.p, to_np(y), fw.y, "y")
+    assert l3.l3_get_error(c.ws) == 0
+
+
+def test_tensor_core_attend_one_long_segment_and_mixed_ranges():
+    # 1400 tokens: 1100 of id 0 (512 rows: 4 row chunks, 18 token chunks) and ids with
+    # few rows (partial 16-row boxes, single-token items)
+    rng = np.random.default_rng(7)
+    ids = np.concatenate([np.zeros(1100, np.int32), rng.integers(20000, 32768, 300).astype(np.int32)])
+    rng.shuffle(ids)
+    c = Case(2, ids=ids)
+    y, sv = c.forward(saved=True)
+    toks = np.unique(np.concatenate([np.nonzero(ids == 0)[0][::37], np.nonzero(ids != 0)[0][::5]]))
+    fw = c.oracle_forward(tokens=toks)
+    assert_close(c.p, to_np(y)[toks], fw.y, "y")
+    a = to_np(c.saved_views(sv)[0])[toks]
+    assert np.abs(a - fw.a).max() / np.abs(fw.a).max() < 1e-2
+    assert l3.l3_get_error(c.ws) == 0
