@@ -1,6 +1,7 @@
 // C-ABI entry points of the L³ library: argument checks, workspace layout, and the order
 // of the kernels for the forward pass, the backward pass and batch routing.
 #include <atomic>
+#include <climits>
 #include <cmath>
 #include <cstring>
 
@@ -52,6 +53,10 @@ struct FwdWs {
   void* route_scratch;
   int32_t *perm, *seg_start, *seg_id, *n_seg;
   float* part;
+  AttendGroup* groups;
+  int32_t* plan_hdr;
+  int32_t* counters;
+  AttendItem* items;
   float* a_f32;
   __nv_bfloat16* a_bf16;
   // fp32 layers (CUDA-core GEMMs)
@@ -63,12 +68,10 @@ struct FwdWs {
   __nv_bfloat16* U16;
   float* stats;
   float* colsum;
-  // tensor-core gather-attend
+  // tensor-core gather-attend of the long segments
   __nv_bfloat16* x_sorted;
-  void* items;
-  int32_t* n_items;
-  bool attend_tc;
-  int n_split;
+  int tc_th;      // segments with at least this many tokens go to tensor cores (0: none)
+  int max_items;  // bound on their item count
 };
 
 FwdWs carve_fwd(Carve& c, const l3_layer* L, int64_t T) {
@@ -80,15 +83,17 @@ FwdWs carve_fwd(Carve& c, const l3_layer* L, int64_t T) {
   w.seg_start = c.take<int32_t>(t + 1);
   w.seg_id = c.take<int32_t>(t);
   w.n_seg = c.take<int32_t>(1);
-  w.n_split = attend_choose_split(T, L->k_max);
-  w.part = c.take<float>(attend_part_floats(T, w.n_split, L->d_v));
   w.mu = c.take<float>(t);
   w.rstd = c.take<float>(t);
-  w.attend_tc = attend_tc_supported(T, int(d), int(dv), L->dtype);
-  if (w.attend_tc) {
+  w.part = c.take<float>(attend_part_floats(int(dv)));
+  w.groups = c.take<AttendGroup>(t + 1);
+  w.plan_hdr = c.take<int32_t>(kPlanHdrWords);
+  w.counters = c.take<int32_t>(t);
+  w.tc_th = attend_tc_threshold(T, int(d), int(dv), L->dtype);
+  if (w.tc_th > 0) {
+    w.max_items = int(T / w.tc_th + 1);
+    w.items = c.take<AttendItem>(size_t(w.max_items));
     w.x_sorted = c.take<__nv_bfloat16>(t * d);
-    w.items = c.raw(attend_tc_items_bytes(T));
-    w.n_items = c.take<int32_t>(1);
   }
   if (L->dtype == L3_BF16) {
     w.a_bf16 = c.take<__nv_bfloat16>(t * dv);
@@ -153,6 +158,17 @@ BwdWs carve_bwd(Carve& c, const l3_layer* L, int64_t T) {
     }                                      \
   } while (0)
 
+// Stage boundary event. Under stream capture the event becomes an event-record node of
+// the graph (cudaEventRecordExternal), so graph replays time their stages too.
+cudaError_t record_stage(cudaEvent_t ev, cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(s, &cs);
+  if (e != cudaSuccess) return e;
+  return cs == cudaStreamCaptureStatusActive
+             ? cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal)
+             : cudaEventRecord(ev, s);
+}
+
 __global__ void check_offsets_kernel(const int32_t* __restrict__ offs, int64_t vocab, int64_t v,
                                      int k_max, DevStatus* st) {
   for (int64_t t = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; t < vocab;
@@ -189,33 +205,45 @@ l3_status forward_impl(const l3_layer* L, const int32_t* ids, int64_t T, const v
   const int d = int(L->d), dv = int(L->d_v);
 
   L3_CUDA(cudaMemsetAsync(w.st, 0, sizeof(DevStatus), s));
-  if (ev) L3_CUDA(cudaEventRecord(ev[L3_STAGE_ROUTE], s));
+  if (ev) L3_CUDA(record_stage(ev[L3_STAGE_ROUTE], s));
   const uint64_t* keys = nullptr;
+  const int ch = attend_rows_per_chunk(d, dv, L->dtype);
+  PlanOut plan{w.groups, w.plan_hdr, w.counters, w.items, L->offs, L->v, L->k_max, ch,
+               attend_group_tokens(L->dtype), w.tc_th > 0 ? w.tc_th : INT32_MAX};
   L3_CUDA(launch_route(ids, T, L->vocab, w.route_scratch,
-                       RouteOut{w.perm, w.seg_start, w.seg_id, w.n_seg}, w.st, s, &keys));
+                       RouteOut{w.perm, w.seg_start, w.seg_id, w.n_seg}, w.st, s, &keys, &plan));
 
-  if (ev) L3_CUDA(cudaEventRecord(ev[L3_STAGE_ATTEND], s));
-  AttendArgs aa{};
-  aa.sorted_keys = keys;
-  aa.T = T;
-  aa.offs = L->offs;
-  aa.K = L->K;
-  aa.V = L->V;
-  aa.x = x;
-  aa.d = d;
-  aa.d_v = dv;
-  aa.k_max = L->k_max;
-  aa.dtype = L->dtype;
-  aa.a_f32 = (L->dtype == L3_F32 || saved) ? a_f32 : nullptr;  // fp32 copy for backward
-  aa.a_bf16 = w.a_bf16;
-  aa.ml = saved ? sv.ml : nullptr;
-  aa.part = w.part;
-  aa.n_split = w.n_split;
-  if (w.attend_tc) {
+  if (ev) L3_CUDA(record_stage(ev[L3_STAGE_ATTEND], s));
+  float* a_copy = (L->dtype == L3_F32 || saved) ? a_f32 : nullptr;  // fp32 copy for backward
+  float* ml = saved ? sv.ml : nullptr;
+  {
+    AttendArgs aa{};
+    aa.sorted_keys = keys;
+    aa.T = T;
+    aa.groups = w.groups;
+    aa.hdr = w.plan_hdr;
+    aa.counters = w.counters;
+    aa.K = L->K;
+    aa.V = L->V;
+    aa.x = x;
+    aa.v = L->v;
+    aa.d = d;
+    aa.d_v = dv;
+    aa.ch = ch;
+    aa.dtype = L->dtype;
+    aa.a_f32 = a_copy;
+    aa.a_bf16 = w.a_bf16;
+    aa.ml = ml;
+    aa.part = w.part;
+    aa.st = w.st;
+    L3_CUDA(launch_attend_fwd(aa, s));
+  }
+  if (w.tc_th > 0) {
     AttendTcArgs at{};
     at.sorted_keys = keys;
-    at.seg_start = w.seg_start;
-    at.n_seg = w.n_seg;
+    at.items = w.items;
+    at.hdr = w.plan_hdr;
+    at.max_items = w.max_items;
     at.T = T;
     at.offs = L->offs;
     at.K = L->K;
@@ -225,18 +253,14 @@ l3_status forward_impl(const l3_layer* L, const int32_t* ids, int64_t T, const v
     at.d = d;
     at.d_v = dv;
     at.x_sorted = w.x_sorted;
-    at.items = w.items;
-    at.n_items = w.n_items;
     at.a_bf16 = w.a_bf16;
-    at.a_f32 = aa.a_f32;
-    at.ml = aa.ml;
+    at.a_f32 = a_copy;
+    at.ml = ml;
     at.st = w.st;
     L3_CUDA(launch_attend_tc(at, s));
-  } else {
-    L3_CUDA(launch_attend_fwd(aa, s));
   }
 
-  if (ev) L3_CUDA(cudaEventRecord(ev[L3_STAGE_UP], s));
+  if (ev) L3_CUDA(record_stage(ev[L3_STAGE_UP], s));
   if (L->dtype == L3_BF16) {
     // Tensor cores: U = bf16(A W_upᵀ) with partial LayerNorm statistics, then
     // y = rstd (U W1ᵀ - mu c) + x W2ᵀ with the statistics merged in the epilogue.
@@ -244,11 +268,11 @@ l3_status forward_impl(const l3_layer* L, const int32_t* ids, int64_t T, const v
     L3_CUDA(launch_rowsum(Wmix, d, 2 * d, d, w.colsum, s));
     L3_CUDA(launch_tc_up(w.a_bf16, static_cast<const __nv_bfloat16*>(L->W_up), T, d, dv, w.U16,
                          w.stats, w.st, s));
-    if (ev) L3_CUDA(cudaEventRecord(ev[L3_STAGE_MIX], s));
+    if (ev) L3_CUDA(record_stage(ev[L3_STAGE_MIX], s));
     L3_CUDA(launch_tc_mix(w.U16, static_cast<const __nv_bfloat16*>(x), Wmix, T, d, w.stats,
                           w.colsum, L->ln_eps, y, y_dtype, saved ? sv.mu : nullptr,
                           saved ? sv.rstd : nullptr, w.st, s));
-    if (ev) L3_CUDA(cudaEventRecord(ev[L3_FWD_STAGES], s));
+    if (ev) L3_CUDA(record_stage(ev[L3_FWD_STAGES], s));
     return L3_OK;
   }
   // fp32 layers: CUDA-core GEMMs (fp32 parity rules out tf32 tensor cores).
@@ -272,7 +296,7 @@ l3_status forward_impl(const l3_layer* L, const int32_t* ids, int64_t T, const v
   L3_CUDA(launch_simt_gemm(up, s));
   L3_CUDA(launch_ln_stats(w.U, T, d, L->ln_eps, mu, rstd, s));
 
-  if (ev) L3_CUDA(cudaEventRecord(ev[L3_STAGE_MIX], s));
+  if (ev) L3_CUDA(record_stage(ev[L3_STAGE_MIX], s));
   L3_CUDA(launch_ln_apply(w.U, mu, rstd, T, d, w.H, s));
   // y = W_mix[:, :d] h + W_mix[:, d:] x (fp32 y: y_dtype must be L3_F32 here)
   float* Y = static_cast<float*>(y);
@@ -297,7 +321,7 @@ l3_status forward_impl(const l3_layer* L, const int32_t* ids, int64_t T, const v
   mix.B = static_cast<const float*>(L->W_mix) + d;
   mix.beta = 1.f;
   L3_CUDA(launch_simt_gemm(mix, s));
-  if (ev) L3_CUDA(cudaEventRecord(ev[L3_FWD_STAGES], s));
+  if (ev) L3_CUDA(record_stage(ev[L3_FWD_STAGES], s));
   return L3_OK;
 }
 

@@ -1,0 +1,519 @@
+// Gather-attend forward of bf16 layers for the short segments of equal ids (all segments of
+// a small batch), rows split across the GPU, products on warp-level tensor cores:
+//   for each token i with id t (rows R = offs[t] .. offs[t+1]-1):
+//   s = K_R x_i,  p = softmax(s),  a_i = V_Rᵀ p
+// ("L³: Large Lookup Layers", gist.science explainer, Technical Summary, "Core
+// Architecture"; "Systems-Friendly Design": the batch sorted by id, so a group of up to 8
+// tokens of one id shares every row it reads).
+//
+// Work list: the routing pass's plan (groups of <= 8 tokens, each group's rows in chunks of
+// `ch` = 8 or 16 rows), split evenly over one persistent CTA per SM.
+//
+// Data movement: a chunk's K rows and V rows are each one TMA copy. The tables are viewed
+// as 3-D tensors [column block of 64][row][64 columns] with the 128-byte swizzle, so a copy
+// lands the chunk as ch-row by 128-byte atoms whose 16-byte pieces are XOR-permuted by row:
+// the matrix loads below read them without shared-memory bank conflicts. A producer warp
+// keeps a ring of up to 4 stages in flight: it waits for a stage to be free, then issues
+// its two copies; full/empty mbarriers per stage, all waits bounded.
+//
+// Per chunk (8 consumer warps, synchronised by a named barrier the producer is not in):
+//   scores  Sᵀ[rows][tokens] = K_chunk Xᵀ with mma.sync m16n8k16 (bf16 in, fp32 out): the
+//           chunk's rows are M, the group's 8 token slots are N, and d is dealt to the
+//           warps in 16-wide steps. Each warp holds its steps' Xᵀ fragments in registers
+//           for the whole group, so per chunk only K is read from shared memory. bf16
+//           products are exact in fp32: this is fp32 accumulation of the bf16 inputs.
+//   softmax online update of the running max m and denominator l per token, and the
+//           chunk's weights e = exp(s - m) (fp32).
+//   values  accᵀ[d_v][tokens] = accᵀ * e^(m_old - m) + V_chunkᵀ Pᵀ, mma.sync with the
+//           value columns as M and the weights as N. The weights enter as two bf16 terms
+//           (hi = bf16(e), lo = bf16(e - hi)), which keeps them to about 2^-17 relative
+//           error; the accumulator stays in registers for the whole group.
+// A group that ends inside the CTA's range is finished there; otherwise its partial
+// (m, l, acc) is merged by the CTA that completes the group (see l3_attend_split.cuh).
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "l3_attend_split.cuh"
+
+namespace l3 {
+
+namespace {
+
+using namespace split;
+
+constexpr int kWarps = kThreads / 32;       // consumer warps (scores, softmax, values)
+constexpr int kCtaThreads = kThreads + 32;  // + one producer warp (TMA copies)
+constexpr int kMaxStages = 4;
+constexpr int kMaxMTiles = 4;   // 16-column value tiles per warp (d_v <= 512)
+constexpr int kMaxKSteps = 16;  // 16-wide k-steps per warp (d <= 2048)
+
+struct Misc {
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  float red[kWarps][16][kMT];  // per-warp score partials
+  float e_buf[16][kMT];
+  float m_run[2][kMT];
+  float l_run[2][kMT];
+  float scale[kMT];
+  int first_group;
+  int last;
+  int abort;
+};
+
+struct MmaShape {
+  int ch;           // rows per chunk: 8 or 16
+  int ks;           // padded row stride of the x tile (bytes)
+  int stages;
+  int k_bytes;      // K block of a stage: ch rows x d
+  int stage_bytes;  // K block, then the V block (ch rows x d_v)
+  int x_bytes;      // kMT token rows of x at stride ks
+  int smem;
+};
+
+MmaShape mma_shape(int d, int d_v) {
+  MmaShape s{};
+  s.ch = 16 * 2 * (d + d_v) <= 49152 ? 16 : 8;
+  s.ks = 2 * d + 16;
+  s.k_bytes = s.ch * 2 * d;
+  s.stage_bytes = int(align_up(size_t(s.ch) * 2 * (d + d_v), 1024));
+  s.x_bytes = int(align_up(size_t(kMT) * s.ks, 128));
+  const int fixed = 1024 + s.x_bytes + int(align_up(sizeof(Misc), 128));
+  s.stages = (kSmemLimit - fixed) / s.stage_bytes;
+  if (s.stages > kMaxStages) s.stages = kMaxStages;
+  s.smem = fixed + s.stages * s.stage_bytes;
+  return s;
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];"
+               : "=r"(r0), "=r"(r1)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2_t(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];"
+               : "=r"(r0), "=r"(r1)
+               : "r"(addr));
+}
+
+// D (16x8 fp32) += A (16x16 bf16, row) B (16x8 bf16, col)
+__device__ __forceinline__ void mma16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                      uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// D (16x8 fp32) += A (16x8 bf16, row) B (8x8 bf16, col)
+__device__ __forceinline__ void mma8(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5}, {%6}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(b0));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  return uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
+         (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+}
+// hi = bf16(v), lo = bf16(v - hi), packed in pairs (lower k in the low half).
+__device__ __forceinline__ void split_pair(float v0, float v1, uint32_t& hi, uint32_t& lo) {
+  const float h0 = __bfloat162float(__float2bfloat16_rn(v0));
+  const float h1 = __bfloat162float(__float2bfloat16_rn(v1));
+  hi = pack_bf16(h0, h1);
+  lo = pack_bf16(v0 - h0, v1 - h1);
+}
+
+// Byte offset of (row, column) in a block of `rows` rows laid out as [col / 64][row][64]
+// with the 128-byte swizzle (16-byte piece index XOR row % 8); the block is 1024-aligned.
+__device__ __forceinline__ uint32_t sw128(int rows, int row, int col) {
+  return uint32_t((col >> 6) * rows * 128 + row * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4));
+}
+
+__device__ __forceinline__ void tma_load_3d(const CUtensorMap* map, uint64_t* bar, uint32_t dst,
+                                            int32_t x, int32_t y, int32_t z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(tc::smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+// Barrier of the kThreads consumer threads (named barrier 1; the producer warp is not in it).
+__device__ __forceinline__ void cbar() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
+
+template <int CH>
+__global__ void __launch_bounds__(kCtaThreads, 1)
+    attend_mma_kernel(const __grid_constant__ CUtensorMap mapK,
+                      const __grid_constant__ CUtensorMap mapV, const AttendArgs a,
+                      const MmaShape sh) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* base = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* ring = base;
+  unsigned char* xt = base + sh.stages * sh.stage_bytes;
+  Misc* ms = reinterpret_cast<Misc*>(xt + sh.x_bytes);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g8 = lane >> 2, t4 = lane & 3;  // mma fragment coordinates
+  const int n_groups = a.hdr[kPlanGroups];
+  const int64_t C = a.hdr[kPlanChunks];
+  const int64_t G = int64_t(gridDim.x) < C ? int64_t(gridDim.x) : C;
+  const int b = blockIdx.x;
+  if (b >= G) return;
+  const int64_t cb = int64_t(b) * C / G, ce = int64_t(b + 1) * C / G;
+  const int nk = int(ce - cb);
+  const int d = a.d, dv = a.d_v, S = sh.stages, ks = sh.ks;
+  const __nv_bfloat16* __restrict__ Xg = static_cast<const __nv_bfloat16*>(a.x);
+  const AttendGroup* __restrict__ groups = a.groups;
+  const uint32_t ring_s = tc::smem_u32(ring), xt_s = tc::smem_u32(xt);
+
+  if (tid == 0) {
+    tc::tma_prefetch_desc(&mapK);
+    tc::tma_prefetch_desc(&mapV);
+    for (int s = 0; s < S; ++s) {
+      tc::mbar_init(&ms->full[s], 1);
+      tc::mbar_init(&ms->empty[s], 1);
+    }
+    ms->abort = 0;
+    ms->first_group = find_group(groups, n_groups, cb);
+    tc::fence_barrier_init();
+  }
+  __syncthreads();
+
+  volatile int* abort_flag = &ms->abort;
+
+  // Producer (warp kWarps, one lane): two TMA copies per chunk, once the consumers have
+  // released the stage. The group being fetched is kept in registers.
+  if (warp == kWarps) {
+    if (lane == 0) {
+      int pg = ms->first_group;
+      AttendGroup pgr = groups[pg];
+      int64_t p_next = groups[pg + 1].c0;
+      const uint32_t tx = uint32_t(CH) * 2u * uint32_t(d + dv);
+      int issued = 0;
+      for (; issued < nk; ++issued) {
+        const int s = issued % S;
+        if (!tc::mbar_wait_watch(&ms->empty[s], ((issued / S) & 1) ^ 1, abort_flag, a.st, 0x40000))
+          break;
+        const int64_t c = cb + issued;
+        while (p_next <= c) {
+          ++pg;
+          pgr = groups[pg];
+          p_next = groups[pg + 1].c0;
+        }
+        const int r0 = pgr.row0 + int(c - pgr.c0) * CH;
+        const uint32_t st = ring_s + uint32_t(s * sh.stage_bytes);
+        tc::mbar_arrive_expect_tx(&ms->full[s], tx);
+        tma_load_3d(&mapK, &ms->full[s], st, 0, r0, 0);
+        tma_load_3d(&mapV, &ms->full[s], st + uint32_t(sh.k_bytes), 0, r0, 0);
+      }
+      if (issued < nk) {
+        // Stopped early: let the copies in flight land before the CTA's memory goes away.
+        volatile int no_abort = 0;
+        for (int j = issued - S > 0 ? issued - S : 0; j < issued; ++j)
+          tc::mbar_wait(&ms->full[j % S], (j / S) & 1, &no_abort, a.st, 0x20000, 100000000ull);
+      }
+    }
+    return;
+  }
+
+  const int n_mt = dv / 16;   // value tiles
+  const int nks = d / 16;     // k-steps; warp w takes w, w + 8, ...
+  float acc[kMaxMTiles][4];
+  uint32_t bx[kMaxKSteps][2];  // Xᵀ fragments of this warp's k-steps
+  int cg = -1, q0 = 0, mt = 0;
+  bool ok = true;
+
+  auto finish = [&](int par) {
+    const int64_t c0 = groups[cg].c0, c1 = groups[cg + 1].c0;
+    const bool whole = c0 >= cb && c1 <= ce;
+    const bool second = c0 > cb;
+    const int n0 = 2 * t4, n1 = 2 * t4 + 1;  // this lane's token slots
+    const int64_t i0 = n0 < mt ? int64_t(uint32_t(a.sorted_keys[q0 + n0])) : 0;
+    const int64_t i1 = n1 < mt ? int64_t(uint32_t(a.sorted_keys[q0 + n1])) : 0;
+    const float inv0 = n0 < mt ? 1.f / ms->l_run[par][n0] : 0.f;
+    const float inv1 = n1 < mt ? 1.f / ms->l_run[par][n1] : 0.f;
+#pragma unroll
+    for (int mi = 0; mi < kMaxMTiles; ++mi) {
+      const int mtile = warp + kWarps * mi;
+      if (mtile >= n_mt) break;
+      const int col0 = 16 * mtile + g8, col1 = col0 + 8;
+      if (whole) {
+        if (n0 < mt) {
+          write_a(a, i0, col0, acc[mi][0] * inv0);
+          write_a(a, i0, col1, acc[mi][2] * inv0);
+        }
+        if (n1 < mt) {
+          write_a(a, i1, col0, acc[mi][1] * inv1);
+          write_a(a, i1, col1, acc[mi][3] * inv1);
+        }
+      } else {
+        if (n0 < mt) {
+          float* pe = part_entry(a, b, second, n0);
+          pe[2 + col0] = acc[mi][0];
+          pe[2 + col1] = acc[mi][2];
+        }
+        if (n1 < mt) {
+          float* pe = part_entry(a, b, second, n1);
+          pe[2 + col0] = acc[mi][1];
+          pe[2 + col1] = acc[mi][3];
+        }
+      }
+    }
+    if (whole) {
+      if (a.ml && tid < mt) {
+        const int64_t i = int64_t(uint32_t(a.sorted_keys[q0 + tid]));
+        a.ml[2 * i] = ms->m_run[par][tid];
+        a.ml[2 * i + 1] = ms->l_run[par][tid];
+      }
+      return;
+    }
+    if (tid < mt) {
+      float* pe = part_entry(a, b, second, tid);
+      pe[0] = ms->m_run[par][tid];
+      pe[1] = ms->l_run[par][tid];
+    }
+    arrive_and_merge(a, cg, c0, c1, C, G, q0, mt, &ms->last, kThreads, [] { cbar(); });
+  };
+
+  int64_t c_next = -1;  // first chunk of the group after the current one
+  AttendGroup gr{};
+  for (int k = 0; k < nk; ++k) {
+    const int64_t c = cb + k;
+    int g = cg;
+    if (cg < 0 || c >= c_next) {
+      g = cg < 0 ? ms->first_group : cg;
+      while (groups[g + 1].c0 <= c) ++g;
+    }
+    if (g != cg) {
+      if (cg >= 0) {
+        finish(k & 1);
+        cbar();
+      }
+      cg = g;
+      gr = groups[g];
+      c_next = groups[g + 1].c0;
+      q0 = gr.q0;
+      mt = gr.mt;
+      // x rows of the group's tokens (rows past mt zero), then each warp's Xᵀ fragments
+      const int npc = d / 8;
+      for (int idx = tid; idx < kMT * npc; idx += kThreads) {
+        const int j = idx / npc, pc = idx - j * npc;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (j < mt) {
+          const int64_t i = int64_t(uint32_t(a.sorted_keys[q0 + j]));
+          v = __ldg(reinterpret_cast<const uint4*>(Xg + i * d) + pc);
+        }
+        *reinterpret_cast<uint4*>(xt + j * ks + pc * 16) = v;
+      }
+#pragma unroll
+      for (int mi = 0; mi < kMaxMTiles; ++mi) acc[mi][0] = acc[mi][1] = acc[mi][2] = acc[mi][3] = 0.f;
+      if (tid < kMT) {
+        ms->m_run[k & 1][tid] = -INFINITY;
+        ms->l_run[k & 1][tid] = 0.f;
+      }
+      cbar();
+      // B fragment of step s16: tokens (lanes 0-7) at k 0-7, (lanes 8-15) at k 8-15
+      const uint32_t b_addr = xt_s + uint32_t((lane & 7) * ks + ((lane >> 3) & 1) * 16);
+#pragma unroll
+      for (int i = 0; i < kMaxKSteps; ++i) {
+        const int s16 = warp + kWarps * i;
+        if (s16 < nks) ldsm_x2(b_addr + s16 * 32, bx[i][0], bx[i][1]);
+      }
+    }
+    const int j0 = int(c - gr.c0);
+    const int nr = gr.n - j0 * CH < CH ? gr.n - j0 * CH : CH;
+
+    tc::mbar_wait(&ms->full[k % S], (k / S) & 1, abort_flag, a.st, 0x10000);
+    cbar();
+    if (*abort_flag) {  // some consumer's wait ran out (it set the flag before the barrier)
+      ok = false;
+      break;
+    }
+    const uint32_t st_s = ring_s + uint32_t((k % S) * sh.stage_bytes);
+    const uint32_t v_s = st_s + uint32_t(sh.k_bytes);
+
+    // scores: Sᵀ = K_chunk Xᵀ
+    {
+      float sc[8][4];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) sc[u][0] = sc[u][1] = sc[u][2] = sc[u][3] = 0.f;
+      // A: matrix q from lanes 8q..8q+7; rows (lane & 7) (+8 for q odd when CH == 16),
+      // k offset 8 for q >= 2 (CH == 16) or q == 1 (CH == 8, two matrices).
+      const int arow = (lane & 7) + (CH == 16 ? ((lane >> 3) & 1) * 8 : 0);
+      const int akof = CH == 16 ? (lane >> 4) * 8 : ((lane >> 3) & 1) * 8;
+#pragma unroll
+      for (int i = 0; i < kMaxKSteps; ++i) {
+        const int s16 = warp + kWarps * i;
+        if (s16 < nks) {
+          const uint32_t addr = st_s + sw128(CH, arow, s16 * 16 + akof);
+          if (CH == 16) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(addr, a0, a1, a2, a3);
+            mma16(sc[i & 7], a0, a1, a2, a3, bx[i][0], bx[i][1]);
+          } else {
+            uint32_t a0, a2;
+            ldsm_x2(addr, a0, a2);
+            mma16(sc[i & 7], a0, a0, a2, a2, bx[i][0], bx[i][1]);  // rows 8-15 repeat 0-7
+          }
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        sc[0][i] = ((sc[0][i] + sc[1][i]) + (sc[2][i] + sc[3][i])) +
+                   ((sc[4][i] + sc[5][i]) + (sc[6][i] + sc[7][i]));
+      *reinterpret_cast<float2*>(&ms->red[warp][g8][2 * t4]) = make_float2(sc[0][0], sc[0][1]);
+      *reinterpret_cast<float2*>(&ms->red[warp][g8 + 8][2 * t4]) = make_float2(sc[0][2], sc[0][3]);
+    }
+    cbar();
+    // softmax update: thread (token j = tid / 16, row r = tid % 16) sums the warps' partial
+    // score, and the 16 lanes of a token reduce max and sum by shuffles.
+    const int par = k & 1;
+    if (tid < 16 * kMT) {
+      const int j = tid >> 4, r = tid & 15;
+      float s = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) s += ms->red[w][r][j];
+      const float mo = ms->m_run[par][j];
+      float mx = r < nr ? s : -INFINITY;
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      const float mn = fmaxf(mo, mx);
+      const float e = (r < nr && j < mt) ? expf(s - mn) : 0.f;
+      float sum = e;
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      ms->e_buf[r][j] = e;
+      if (r == 0) {
+        if (j < mt) {
+          const float scl = expf(mo - mn);
+          ms->scale[j] = scl;
+          ms->m_run[par ^ 1][j] = mn;
+          ms->l_run[par ^ 1][j] = fmaf(ms->l_run[par][j], scl, sum);
+        } else {
+          ms->scale[j] = 0.f;
+        }
+      }
+    }
+    cbar();
+    // values: accᵀ = accᵀ * scale + V_chunkᵀ Pᵀ (P as bf16 hi + lo)
+    {
+      const float sc0 = ms->scale[2 * t4], sc1 = ms->scale[2 * t4 + 1];
+      uint32_t bh0, bl0, bh1 = 0, bl1 = 0;
+      split_pair(ms->e_buf[2 * t4][g8], ms->e_buf[2 * t4 + 1][g8], bh0, bl0);
+      if (CH == 16) split_pair(ms->e_buf[2 * t4 + 8][g8], ms->e_buf[2 * t4 + 9][g8], bh1, bl1);
+      // Vᵀ tile (16 value columns x CH rows) by transposing loads: lanes 0-7 rows 0-7 at
+      // column 0, lanes 8-15 rows 0-7 at column 8, lanes 16-31 rows 8-15.
+      const int vrow = (lane & 7) + (CH == 16 ? (lane >> 4) * 8 : 0);
+      const int vcol = ((lane >> 3) & 1) * 8;
+      uint32_t va[kMaxMTiles][4];
+#pragma unroll
+      for (int mi = 0; mi < kMaxMTiles; ++mi) {
+        const int mtile = warp + kWarps * mi;
+        if (mtile < n_mt) {
+          acc[mi][0] *= sc0;
+          acc[mi][1] *= sc1;
+          acc[mi][2] *= sc0;
+          acc[mi][3] *= sc1;
+          const uint32_t addr = v_s + sw128(CH, vrow, 16 * mtile + vcol);
+          if (CH == 16)
+            ldsm_x4_t(addr, va[mi][0], va[mi][1], va[mi][2], va[mi][3]);
+          else
+            ldsm_x2_t(addr, va[mi][0], va[mi][1]);
+        }
+      }
+      // all hi products, then all lo products: dependent pairs are kMaxMTiles mmas apart
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t b0 = h ? bl0 : bh0, b1 = h ? bl1 : bh1;
+#pragma unroll
+        for (int mi = 0; mi < kMaxMTiles; ++mi) {
+          if (warp + kWarps * mi < n_mt) {
+            if (CH == 16)
+              mma16(acc[mi], va[mi][0], va[mi][1], va[mi][2], va[mi][3], b0, b1);
+            else
+              mma8(acc[mi], va[mi][0], va[mi][1], b0);
+          }
+        }
+      }
+    }
+    cbar();  // the stage and the score buffers are free again
+    if (tid == 0) tc::mbar_arrive(&ms->empty[k % S]);
+  }
+
+  if (ok && cg >= 0) finish(nk & 1);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// bf16 table [rows, cols] viewed as [cols / 64][rows][64]; box: all column blocks of
+// `box_rows` rows, 128-byte swizzle.
+bool make_row_block_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols,
+                        int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {64, cuuint64_t(rows), cuuint64_t(cols / 64)};
+  cuuint64_t strides[2] = {cuuint64_t(cols) * 2, 128};
+  cuuint32_t box[3] = {64, cuuint32_t(box_rows), cuuint32_t(cols / 64)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int CH>
+cudaError_t launch_ch(const AttendArgs& a, const MmaShape& sh, cudaStream_t stream) {
+  CUtensorMap mk, mv;
+  if (!make_row_block_map(&mk, a.K, a.v, a.d, CH) || !make_row_block_map(&mv, a.V, a.v, a.d_v, CH))
+    return cudaErrorInvalidValue;
+  static cudaError_t attr = cudaFuncSetAttribute(
+      attend_mma_kernel<CH>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+  if (attr != cudaSuccess) return attr;
+  int grid = sm_count();
+  if (grid > kMaxCtas) grid = kMaxCtas;
+  attend_mma_kernel<CH><<<grid, kCtaThreads, sh.smem, stream>>>(mk, mv, a, sh);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int attend_mma_rows_per_chunk(int d, int d_v) { return mma_shape(d, d_v).ch; }
+
+cudaError_t launch_attend_mma(const AttendArgs& a, cudaStream_t stream) {
+  const MmaShape sh = mma_shape(a.d, a.d_v);
+  if (sh.stages < 2 || sh.smem > kSmemLimit || sh.ch != a.ch ||
+      a.d_v > 16 * kWarps * kMaxMTiles || a.d > 16 * kWarps * kMaxKSteps || a.d % 64 != 0 ||
+      a.d_v % 64 != 0)
+    return cudaErrorInvalidValue;
+  return sh.ch == 16 ? launch_ch<16>(a, sh, stream) : launch_ch<8>(a, sh, stream);
+}
+
+}  // namespace l3

@@ -1,4 +1,4 @@
-// Gather-attend forward on tcgen05 tensor cores, one segment of equal token ids at a time
+// Gather-attend forward on tcgen05 tensor cores for the long segments of equal token ids
 // ("L³: Large Lookup Layers", gist.science explainer, Technical Summary: "Core
 // Architecture" for the aggregation a = V_tᵀ softmax(K_t x); "Systems-Friendly Design",
 // batch sorting, for grouping the tokens of one id so that its rows are read once).
@@ -40,12 +40,8 @@ constexpr uint32_t kSCol = 0;    // Sᵀ chunk rc at columns 64 rc
 constexpr uint32_t kACol = 256;  // Aᵀ chunk dc at columns 256 + 64 dc
 constexpr int kSmemBytes = kStages * kStageBytes + kPBytes + 7 * kNT * 4 + 256 + 1024;
 
-struct Item {
-  int32_t q0;  // first sorted position
-  int32_t nt;  // tokens (1..64)
-  int32_t t;   // token id
-  int32_t pad;
-};
+static_assert(kNT == kTcNT, "item size of the plan");
+using Item = AttendItem;
 
 struct TcAttendParams {
   const Item* items;
@@ -436,74 +432,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Items: for each segment, ceil(m / 64) chunks of its tokens, in segment order.
-__global__ void __launch_bounds__(1024) attend_items_kernel(const int32_t* __restrict__ seg_start,
-                                                           const int32_t* __restrict__ n_seg,
-                                                           const uint64_t* __restrict__ keys,
-                                                           Item* items, int32_t* n_items) {
-  __shared__ int warp_tot[32];
-  __shared__ int total;
-  const int S = *n_seg;
-  int carry = 0;
-  for (int base = 0; base < S; base += blockDim.x) {
-    const int s = base + threadIdx.x;
-    int cnt = 0, q0 = 0, m = 0;
-    if (s < S) {
-      q0 = seg_start[s];
-      m = seg_start[s + 1] - q0;
-      cnt = (m + kNT - 1) / kNT;
-    }
-    // exclusive scan of cnt over the CTA
-    const int wl = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    int incl = cnt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int u = __shfl_up_sync(0xffffffffu, incl, o);
-      if (wl >= o) incl += u;
-    }
-    if (wl == 31) warp_tot[wid] = incl;
-    __syncthreads();
-    if (wid == 0) {
-      const int w = wl < int(blockDim.x >> 5) ? warp_tot[wl] : 0;
-      int wi = w;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int u = __shfl_up_sync(0xffffffffu, wi, o);
-        if (wl >= o) wi += u;
-      }
-      warp_tot[wl] = wi - w;
-      if (wl == 31) total = wi;
-    }
-    __syncthreads();
-    const int ex = carry + warp_tot[wid] + incl - cnt;
-    if (s < S) {
-      const int t = int(keys[q0] >> 32);
-      for (int c = 0; c < cnt; ++c) {
-        Item it;
-        it.q0 = q0 + c * kNT;
-        it.nt = m - c * kNT < kNT ? m - c * kNT : kNT;
-        it.t = t;
-        it.pad = 0;
-        items[ex + c] = it;
-      }
-    }
-    carry += total;
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) *n_items = carry;
-}
-
-// x_sorted[q] = x[perm(q)] (bf16 rows of d elements), one warp per row.
-__global__ void gather_rows_kernel(const uint64_t* __restrict__ keys, int64_t T,
+// x_sorted[q] = x[perm(q)] (bf16 rows of d elements) for the tokens of the items, one CTA
+// per item, one warp per row.
+__global__ void gather_rows_kernel(const Item* __restrict__ items, const int32_t* __restrict__ hdr,
+                                   const uint64_t* __restrict__ keys,
                                    const __nv_bfloat16* __restrict__ x, int d,
                                    __nv_bfloat16* __restrict__ xs) {
+  if (int(blockIdx.x) >= hdr[kPlanItems]) return;
+  const Item it = items[blockIdx.x];
   const int lane = threadIdx.x & 31;
-  const int64_t q = int64_t(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
-  if (q >= T) return;
-  const int64_t i = int64_t(uint32_t(keys[q]));
-  const uint4* src = reinterpret_cast<const uint4*>(x + i * d);
-  uint4* dst = reinterpret_cast<uint4*>(xs + q * d);
-  for (int c = lane; c < d / 8; c += 32) dst[c] = __ldg(src + c);
+  for (int j = threadIdx.x >> 5; j < it.nt; j += blockDim.x >> 5) {
+    const int64_t q = it.q0 + j;
+    const int64_t i = int64_t(uint32_t(keys[q]));
+    const uint4* src = reinterpret_cast<const uint4*>(x + i * d);
+    uint4* dst = reinterpret_cast<uint4*>(xs + q * d);
+    for (int c = lane; c < d / 8; c += 32) dst[c] = __ldg(src + c);
+  }
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -546,28 +490,26 @@ int sm_count() {
 
 }  // namespace
 
-bool attend_tc_supported(int64_t T, int d, int d_v, int dtype) {
-  return dtype == L3_BF16 && T >= 1024 && d % 64 == 0 && d_v % 128 == 0 && d_v <= 512;
+int attend_tc_threshold(int64_t T, int d, int d_v, int dtype) {
+  // Segments of fewer tokens have too little arithmetic per table byte for tensor cores:
+  // the split-row CUDA-core kernel streams them at memory speed.
+  const bool ok = dtype == L3_BF16 && T >= 1024 && d % 64 == 0 && d_v % 128 == 0 && d_v <= 512;
+  return ok ? 8 : 0;
 }
 
-size_t attend_tc_items_bytes(int64_t T) { return size_t(2 * T + 1) * sizeof(Item); }
-
 cudaError_t launch_attend_tc(const AttendTcArgs& a, cudaStream_t stream) {
-  if (a.T <= 0) return cudaSuccess;
-  gather_rows_kernel<<<unsigned((a.T + 7) / 8), 256, 0, stream>>>(
-      a.sorted_keys, a.T, static_cast<const __nv_bfloat16*>(a.x), a.d, a.x_sorted);
+  if (a.T <= 0 || a.max_items <= 0) return cudaSuccess;
+  gather_rows_kernel<<<unsigned(a.max_items), 256, 0, stream>>>(
+      a.items, a.hdr, a.sorted_keys, static_cast<const __nv_bfloat16*>(a.x), a.d, a.x_sorted);
   count_launch();
-  Item* items = static_cast<Item*>(a.items);
-  attend_items_kernel<<<1, 1024, 0, stream>>>(a.seg_start, a.n_seg, a.sorted_keys, items,
-                                               a.n_items);
-  count_launch();
+  const Item* items = a.items;
   CUtensorMap mk, mx, mv;
   if (!make_map16(&mk, a.K, a.v, a.d) || !make_map16(&mx, a.x_sorted, a.T, a.d) ||
       !make_map16(&mv, a.V, a.v, a.d_v))
     return cudaErrorInvalidValue;
   TcAttendParams p{};
   p.items = items;
-  p.n_items = a.n_items;
+  p.n_items = a.hdr + kPlanItems;
   p.sorted_keys = a.sorted_keys;
   p.offs = a.offs;
   p.d = a.d;

@@ -17,36 +17,79 @@ struct RouteOut {
   int32_t* seg_id;     // [T]
   int32_t* n_seg;      // [1]
 };
+// Work plan of the gather-attend, built by the routing pass. Segments of equal ids with
+// fewer than `th` tokens go to the split-row CUDA-core kernel: each is cut into groups of at
+// most kPlanMT tokens, and each group's n_t rows into chunks of `ch` rows; groups are
+// numbered in sorted order and their chunks prefix-summed. Segments of at least `th`
+// tokens go to the tensor-core kernel as items of at most kTcNT tokens.
+constexpr int kPlanMT = 8;
+constexpr int kTcNT = 64;
+struct AttendGroup {
+  int32_t q0;    // first sorted position of the group's tokens
+  int32_t mt;    // tokens in the group (1..mt_max)
+  int32_t t;     // token id
+  int32_t row0;  // offs[t]
+  int32_t n;     // rows n_t (0 if the offsets were invalid for t: the group is skipped)
+  int32_t c0;    // index of the group's first chunk among all chunks
+};
+struct AttendItem {
+  int32_t q0;  // first sorted position
+  int32_t nt;  // tokens (1..kTcNT)
+  int32_t t;   // token id
+  int32_t pad;
+};
+// hdr words written by the plan
+enum { kPlanGroups = 0, kPlanChunks = 1, kPlanItems = 2, kPlanHdrWords = 4 };
+struct PlanOut {
+  AttendGroup* groups;  // [T + 1]; entry n_groups carries only c0 = total chunks
+  int32_t* hdr;         // [kPlanHdrWords]
+  int32_t* counters;    // [T]: zeroed here, counted up by the split-row kernel
+  AttendItem* items;    // [T / th + 1] (may be null when th > T)
+  const int32_t* offs;
+  int64_t v;
+  int k_max;
+  int ch;      // rows per chunk
+  int mt_max;  // tokens per group (<= kPlanMT)
+  int th;      // segments with at least th tokens go to the tensor-core kernel
+};
 size_t route_scratch_bytes(int64_t T);
 cudaError_t launch_route(const int32_t* ids, int64_t T, int64_t vocab, void* scratch,
                          RouteOut out, DevStatus* st, cudaStream_t stream,
-                         const uint64_t** sorted_keys);
+                         const uint64_t** sorted_keys, const PlanOut* plan = nullptr);
 
-// ---- gather-attend (l3_attend.cu) ----------------------------------------------------------
+// ---- gather-attend, split rows (l3_attend.cu) ----------------------------------------------
 struct AttendArgs {
   const uint64_t* sorted_keys;  // [T] (id << 32 | batch index), ascending
   int64_t T;
-  const int32_t* offs;
+  const AttendGroup* groups;
+  const int32_t* hdr;
+  int32_t* counters;
   const void* K;
   const void* V;
   const void* x;
-  int d, d_v, k_max;
+  int64_t v;             // table rows
+  int d, d_v, ch;
   int dtype;             // L3_F32 / L3_BF16
   float* a_f32;          // [T, d_v] nullable, batch order
   __nv_bfloat16* a_bf16; // [T, d_v] nullable, batch order
   float* ml;             // [T, 2] nullable: (max score, softmax denominator)
-  float* part;           // split-row partials, attend_part_floats(...) floats
-  int n_split;           // row splits per token (>= 1)
+  float* part;           // attend_part_floats(T, d_v) floats: partial (m, l, acc) per slot
+  DevStatus* st;
 };
-int attend_choose_split(int64_t T, int k_max);
-size_t attend_part_floats(int64_t T, int n_split, int d_v);
+// Rows per chunk for a layer shape: 8 or 16 for bf16 layers (warp-MMA kernel), else as
+// many as fit 40 KB of K and V rows (at most 8).
+int attend_rows_per_chunk(int d, int d_v, int dtype);
+int attend_mma_rows_per_chunk(int d, int d_v);
+// Tokens per group of the split-row plan for a layer dtype.
+int attend_group_tokens(int dtype);
+size_t attend_part_floats(int d_v);
 cudaError_t launch_attend_fwd(const AttendArgs& a, cudaStream_t stream);
 
-// ---- gather-attend on tensor cores (l3_attend_tc.cu), bf16 prefill batches -----------------
+// ---- gather-attend on tensor cores (l3_attend_tc.cu), the long segments of bf16 batches ----
 struct AttendTcArgs {
   const uint64_t* sorted_keys;
-  const int32_t* seg_start;
-  const int32_t* n_seg;
+  const AttendItem* items;
+  const int32_t* hdr;       // plan header (item count)
   int64_t T;
   const int32_t* offs;
   const void* K;
@@ -54,16 +97,15 @@ struct AttendTcArgs {
   const void* x;
   int64_t v;
   int d, d_v;
-  __nv_bfloat16* x_sorted;  // [T, d] scratch
-  void* items;              // attend_tc_items_bytes(T) scratch
-  int32_t* n_items;         // [1] scratch
+  int max_items;            // upper bound of the item count (grid of the x gather)
+  __nv_bfloat16* x_sorted;  // [T, d] scratch: rows of the items' tokens in sorted order
   __nv_bfloat16* a_bf16;    // [T, d_v]
   float* a_f32;             // nullable
   float* ml;                // nullable
   DevStatus* st;
 };
-bool attend_tc_supported(int64_t T, int d, int d_v, int dtype);
-size_t attend_tc_items_bytes(int64_t T);
+// Tokens per segment from which the tensor-core kernel takes a segment (0: never).
+int attend_tc_threshold(int64_t T, int d, int d_v, int dtype);
 cudaError_t launch_attend_tc(const AttendTcArgs& a, cudaStream_t stream);
 
 // ---- SIMT GEMM and row kernels (l3_gemm_simt.cu) -------------------------------------------

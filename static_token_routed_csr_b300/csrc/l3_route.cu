@@ -6,7 +6,8 @@
 // is the stable sort of the ids. Batches up to kSmallT tokens are sorted by one CTA in
 // shared memory (bitonic); larger ones are cut into kChunk-key runs sorted the same way,
 // then merged pairwise (each key finds its rank in the other run by binary search).
-// A last pass marks segment starts and numbers the segments.
+// A last pass marks segment starts and numbers the segments, and (for the forward) lays out
+// the work plan of the split-row gather-attend.
 #include "l3_internal.h"
 
 namespace l3 {
@@ -74,13 +75,80 @@ __device__ int block_exclusive_scan(int v, int* warp_tot, int* total) {
   return r;
 }
 
-// Segment pass over sorted keys: perm, seg_start, seg_id, n_seg. One CTA of 1024 threads
-// walks the batch in tiles of 1024*kItems keys, carrying the segment count across tiles.
+// Work plan of the gather-attend (see PlanOut), from the finished segment table.
+__device__ void plan_pass(const uint64_t* keys, int64_t T, const int32_t* seg_start, int S,
+                          const PlanOut& pl, DevStatus* st, int* warp_tot, int* total) {
+  int gcarry = 0, ccarry = 0, icarry = 0;
+  for (int base = 0; base < S; base += blockDim.x) {
+    const int s = base + threadIdx.x;
+    int ng = 0, nc = 0, ni = 0, q0 = 0, m = 0, t = 0, row0 = 0, n = 0, per = 0;
+    if (s < S) {
+      q0 = seg_start[s];
+      m = seg_start[s + 1] - q0;
+      t = int(keys[q0] >> 32);
+      row0 = pl.offs[t];
+      n = pl.offs[t + 1] - row0;
+      if (n < 1 || n > pl.k_max || row0 < 0 || int64_t(row0) + n > pl.v) {
+        atomicOr(&st->layer_bad, 1);
+        n = 0;  // no rows are read for this id; its tokens' outputs are unspecified
+      }
+      if (m >= pl.th) {
+        ni = n > 0 ? (m + kTcNT - 1) / kTcNT : 0;
+      } else {
+        ng = (m + pl.mt_max - 1) / pl.mt_max;
+        per = n > 0 ? (n + pl.ch - 1) / pl.ch : 0;
+        nc = ng * per;
+      }
+    }
+    const int gex = block_exclusive_scan(ng, warp_tot, total);
+    const int gtot = *total;
+    const int cex = block_exclusive_scan(nc, warp_tot, total);
+    const int ctot = *total;
+    const int iex = block_exclusive_scan(ni, warp_tot, total);
+    const int itot = *total;
+    for (int k = 0; k < ng; ++k) {
+      AttendGroup g;
+      g.q0 = q0 + k * pl.mt_max;
+      g.mt = m - k * pl.mt_max < pl.mt_max ? m - k * pl.mt_max : pl.mt_max;
+      g.t = t;
+      g.row0 = row0;
+      g.n = n;
+      g.c0 = ccarry + cex + k * per;
+      pl.groups[gcarry + gex + k] = g;
+      pl.counters[gcarry + gex + k] = 0;
+    }
+    for (int k = 0; k < ni; ++k) {
+      AttendItem it;
+      it.q0 = q0 + k * kTcNT;
+      it.nt = m - k * kTcNT < kTcNT ? m - k * kTcNT : kTcNT;
+      it.t = t;
+      it.pad = 0;
+      pl.items[icarry + iex + k] = it;
+    }
+    gcarry += gtot;
+    ccarry += ctot;
+    icarry += itot;
+  }
+  if (threadIdx.x == 0) {
+    AttendGroup end{};
+    end.q0 = int32_t(T);
+    end.c0 = ccarry;
+    pl.groups[gcarry] = end;
+    pl.hdr[kPlanGroups] = gcarry;
+    pl.hdr[kPlanChunks] = ccarry;
+    pl.hdr[kPlanItems] = icarry;
+    pl.hdr[3] = 0;
+  }
+}
+
+// Segment pass over sorted keys: perm, seg_start, seg_id, n_seg (and the attend plan).
+// One CTA of 1024 threads walks the batch in tiles of 1024*kItems keys, carrying the
+// segment count across tiles.
 constexpr int kItems = 4;
 
 __device__ void segment_pass(const uint64_t* keys, int64_t T, int32_t* perm,
                              int32_t* seg_start, int32_t* seg_id, int32_t* n_seg,
-                             int* warp_tot, int* total) {
+                             const PlanOut* plan, DevStatus* st, int* warp_tot, int* total) {
   int carry = 0;
   const int64_t tile = int64_t(blockDim.x) * kItems;
   for (int64_t base = 0; base < T; base += tile) {
@@ -115,13 +183,18 @@ __device__ void segment_pass(const uint64_t* keys, int64_t T, int32_t* perm,
     if (seg_start) seg_start[carry] = int32_t(T);
     if (n_seg) *n_seg = carry;
   }
+  if (plan && seg_start) {
+    __syncthreads();  // seg_start complete and visible to the whole CTA
+    plan_pass(keys, T, seg_start, carry, *plan, st, warp_tot, total);
+  }
 }
 
 __global__ void __launch_bounds__(1024) route_small_kernel(const int32_t* __restrict__ ids,
                                                            int64_t T, int64_t vocab,
                                                            uint64_t* keys_out, int32_t* perm,
                                                            int32_t* seg_start, int32_t* seg_id,
-                                                           int32_t* n_seg, DevStatus* st) {
+                                                           int32_t* n_seg, DevStatus* st,
+                                                           const PlanOut plan, int with_plan) {
   __shared__ uint64_t s[kChunk];
   __shared__ int warp_tot[32];
   __shared__ int total;
@@ -132,7 +205,8 @@ __global__ void __launch_bounds__(1024) route_small_kernel(const int32_t* __rest
   block_bitonic(s, n);
   for (int i = threadIdx.x; i < T; i += blockDim.x) keys_out[i] = s[i];
   __syncthreads();
-  segment_pass(s, T, perm, seg_start, seg_id, n_seg, warp_tot, &total);
+  segment_pass(s, T, perm, seg_start, seg_id, n_seg, with_plan ? &plan : nullptr, st, warp_tot,
+               &total);
 }
 
 __global__ void __launch_bounds__(1024) route_chunk_kernel(const int32_t* __restrict__ ids,
@@ -180,10 +254,12 @@ __global__ void route_merge_kernel(const uint64_t* __restrict__ in, uint64_t* __
 __global__ void __launch_bounds__(1024) route_segment_kernel(const uint64_t* __restrict__ keys,
                                                              int64_t T, int32_t* perm,
                                                              int32_t* seg_start, int32_t* seg_id,
-                                                             int32_t* n_seg) {
+                                                             int32_t* n_seg, DevStatus* st,
+                                                             const PlanOut plan, int with_plan) {
   __shared__ int warp_tot[32];
   __shared__ int total;
-  segment_pass(keys, T, perm, seg_start, seg_id, n_seg, warp_tot, &total);
+  segment_pass(keys, T, perm, seg_start, seg_id, n_seg, with_plan ? &plan : nullptr, st,
+               warp_tot, &total);
 }
 
 }  // namespace
@@ -195,13 +271,15 @@ size_t route_scratch_bytes(int64_t T) {
 // Sorted keys end up in the returned buffer (one of the two scratch halves).
 cudaError_t launch_route(const int32_t* ids, int64_t T, int64_t vocab, void* scratch,
                          RouteOut out, DevStatus* st, cudaStream_t stream,
-                         const uint64_t** sorted_keys) {
+                         const uint64_t** sorted_keys, const PlanOut* plan) {
+  const PlanOut pl = plan ? *plan : PlanOut{};
+  const int with_plan = plan && out.seg_start ? 1 : 0;
   uint64_t* k0 = static_cast<uint64_t*>(scratch);
   uint64_t* k1 = reinterpret_cast<uint64_t*>(static_cast<char*>(scratch) +
                                              align_up(size_t(T) * sizeof(uint64_t), kAlign));
   if (T <= kChunk) {
     route_small_kernel<<<1, 1024, 0, stream>>>(ids, T, vocab, k0, out.perm, out.seg_start,
-                                               out.seg_id, out.n_seg, st);
+                                               out.seg_id, out.n_seg, st, pl, with_plan);
     count_launch();
     *sorted_keys = k0;
     return cudaGetLastError();
@@ -218,7 +296,7 @@ cudaError_t launch_route(const int32_t* ids, int64_t T, int64_t vocab, void* scr
     dst = t;
   }
   route_segment_kernel<<<1, 1024, 0, stream>>>(src, T, out.perm, out.seg_start, out.seg_id,
-                                               out.n_seg);
+                                               out.n_seg, st, pl, with_plan);
   count_launch();
   *sorted_keys = src;
   return cudaGetLastError();

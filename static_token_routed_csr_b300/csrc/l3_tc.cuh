@@ -77,6 +77,25 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// As mbar_wait, but only watches *stop (never writes it): gives up when *stop becomes
+// non-zero, or after limit_ns (then ORs `code` into the device status).
+__device__ __forceinline__ bool mbar_wait_watch(uint64_t* bar, uint32_t parity,
+                                                const volatile int* stop, DevStatus* st,
+                                                int code, uint64_t limit_ns = 2000000000ull) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63) == 0) {
+      if (*stop) return false;
+      if (global_ns() - t0 > limit_ns) {
+        atomicOr(&st->timeout, code);
+        return false;
+      }
+    }
+  }
+}
+
 // ---- TMA ---------------------------------------------------------------------------------------
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {

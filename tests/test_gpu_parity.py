@@ -274,3 +274,34 @@ def test_tensor_core_attend_one_long_segment_and_mixed_ranges():
     a = to_np(c.saved_views(sv)[0])[toks]
     assert np.abs(a - fw.a).max() / np.abs(fw.a).max() < 1e-2
     assert l3.l3_get_error(c.ws) == 0
+
+
+def test_split_attend_one_token_spread_over_many_ctas_and_long_segments():
+    # decode shapes: one token of the id with the most rows (512 rows = 64 chunks, one per
+    # CTA, merged by the last CTA), then a batch where one id fills several 8-token groups
+    for ids in (np.array([0], np.int32),
+                np.concatenate([np.zeros(19, np.int32), np.arange(1, 46, dtype=np.int32)])):
+        c = Case(3, ids=ids)
+        y, sv = c.forward(saved=True)
+        fw = c.oracle_forward()
+        assert_close(c.p, to_np(y), fw.y, "y")
+        a, ml, _, _ = c.saved_views(sv)
+        assert_fp32_close(to_np(a), fw.a, "a (fp32 copy)")
+        np.testing.assert_allclose(to_np(ml[:, 0]), fw.m, rtol=1e-5, atol=1e-6)
+        np.testing.assert_allclose(to_np(ml[:, 1]), fw.l, rtol=1e-5)
+        assert l3.l3_get_error(c.ws) == 0
+        del c
+        torch.cuda.empty_cache()
+
+
+def test_single_row_tokens_return_value_row_exactly_bf16():
+    # bf16 storage: p = exp(0) / 1 = 1 exactly, and the weights enter the tensor-core
+    # product as bf16 hi + lo terms (1 and 0), so a is the value row bit for bit
+    c = Case(5)
+    n = np.diff(c.offs_np)
+    ones = np.nonzero(n == 1)[0][:40].astype(np.int32)
+    c2 = Case(5, ids=ones)
+    _, sv = c2.forward(saved=True)
+    a = c2.saved_views(sv)[0].cpu().numpy()
+    V = W.table_rows_to_numpy(c2.V, c2.offs_np[ones])
+    assert np.array_equal(a, V)
