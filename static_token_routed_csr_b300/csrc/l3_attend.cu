@@ -207,7 +207,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_split_kernel(const AttendA
         pe[1] = ms->l_run[par][j];
       }
     }
-    arrive_and_merge(a, cg, c0, c1, C, G, q0, mt, &ms->last, kThreads, [] { __syncthreads(); });
+    arrive_and_merge(a, cg, c0, c1, C, G, q0, mt, &ms->last, int(threadIdx.x), kThreads,
+                     [] { __syncthreads(); });
   };
 
   for (; k < nk; ++k) {

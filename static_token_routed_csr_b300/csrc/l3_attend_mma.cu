@@ -7,7 +7,8 @@
 // tokens of one id shares every row it reads).
 //
 // Work list: the routing pass's plan (groups of <= 8 tokens, each group's rows in chunks of
-// `ch` = 8 or 16 rows), split evenly over one persistent CTA per SM.
+// `ch` = 8 or 16 rows), split evenly over one persistent CTA per SM. With 8-row chunks a
+// consumer step takes two consecutive chunks of a group as the mma's 16 rows.
 //
 // Data movement: a chunk's K rows and V rows are each one TMA copy. The tables are viewed
 // as 3-D tensors [column block of 64][row][64 columns] with the 128-byte swizzle, so a copy
@@ -19,8 +20,8 @@
 // Per chunk (8 consumer warps, synchronised by a named barrier the producer is not in):
 //   scores  Sᵀ[rows][tokens] = K_chunk Xᵀ with mma.sync m16n8k16 (bf16 in, fp32 out): the
 //           chunk's rows are M, the group's 8 token slots are N, and d is dealt to the
-//           warps in 16-wide steps. Each warp holds its steps' Xᵀ fragments in registers
-//           for the whole group, so per chunk only K is read from shared memory. bf16
+//           warps in 16-wide steps. Each warp loads its steps' Xᵀ fragments from x into
+//           registers once per group, so per chunk only K is read from shared memory. bf16
 //           products are exact in fp32: this is fp32 accumulation of the bf16 inputs.
 //   softmax online update of the running max m and denominator l per token, and the
 //           chunk's weights e = exp(s - m) (fp32).
@@ -44,7 +45,7 @@ using namespace split;
 
 constexpr int kWarps = kThreads / 32;       // consumer warps (scores, softmax, values)
 constexpr int kCtaThreads = kThreads + 32;  // + one producer warp (TMA copies)
-constexpr int kMaxStages = 4;
+constexpr int kMaxStages = 6;
 constexpr int kMaxMTiles = 4;   // 16-column value tiles per warp (d_v <= 512)
 constexpr int kMaxKSteps = 16;  // 16-wide k-steps per warp (d <= 2048)
 
@@ -63,22 +64,18 @@ struct Misc {
 
 struct MmaShape {
   int ch;           // rows per chunk: 8 or 16
-  int ks;           // padded row stride of the x tile (bytes)
   int stages;
   int k_bytes;      // K block of a stage: ch rows x d
   int stage_bytes;  // K block, then the V block (ch rows x d_v)
-  int x_bytes;      // kMT token rows of x at stride ks
   int smem;
 };
 
 MmaShape mma_shape(int d, int d_v) {
   MmaShape s{};
   s.ch = 16 * 2 * (d + d_v) <= 49152 ? 16 : 8;
-  s.ks = 2 * d + 16;
   s.k_bytes = s.ch * 2 * d;
   s.stage_bytes = int(align_up(size_t(s.ch) * 2 * (d + d_v), 1024));
-  s.x_bytes = int(align_up(size_t(kMT) * s.ks, 128));
-  const int fixed = 1024 + s.x_bytes + int(align_up(sizeof(Misc), 128));
+  const int fixed = 1024 + int(align_up(sizeof(Misc), 128));
   s.stages = (kSmemLimit - fixed) / s.stage_bytes;
   if (s.stages > kMaxStages) s.stages = kMaxStages;
   s.smem = fixed + s.stages * s.stage_bytes;
@@ -165,8 +162,7 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
   unsigned char* base = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   unsigned char* ring = base;
-  unsigned char* xt = base + sh.stages * sh.stage_bytes;
-  Misc* ms = reinterpret_cast<Misc*>(xt + sh.x_bytes);
+  Misc* ms = reinterpret_cast<Misc*>(base + sh.stages * sh.stage_bytes);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g8 = lane >> 2, t4 = lane & 3;  // mma fragment coordinates
@@ -177,10 +173,10 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
   if (b >= G) return;
   const int64_t cb = int64_t(b) * C / G, ce = int64_t(b + 1) * C / G;
   const int nk = int(ce - cb);
-  const int d = a.d, dv = a.d_v, S = sh.stages, ks = sh.ks;
+  const int d = a.d, dv = a.d_v, S = sh.stages;
   const __nv_bfloat16* __restrict__ Xg = static_cast<const __nv_bfloat16*>(a.x);
   const AttendGroup* __restrict__ groups = a.groups;
-  const uint32_t ring_s = tc::smem_u32(ring), xt_s = tc::smem_u32(xt);
+  const uint32_t ring_s = tc::smem_u32(ring);
 
   if (tid == 0) {
     tc::tma_prefetch_desc(&mapK);
@@ -288,12 +284,15 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
       pe[0] = ms->m_run[par][tid];
       pe[1] = ms->l_run[par][tid];
     }
-    arrive_and_merge(a, cg, c0, c1, C, G, q0, mt, &ms->last, kThreads, [] { cbar(); });
+    arrive_and_merge(a, cg, c0, c1, C, G, q0, mt, &ms->last, tid, kThreads, [] { cbar(); });
   };
 
+  // A consumer step takes one chunk, or, for 8-row chunks, two consecutive chunks of the same
+  // group as the two 8-row halves of the mma's 16 rows (stages k and k+1).
   int64_t c_next = -1;  // first chunk of the group after the current one
   AttendGroup gr{};
-  for (int k = 0; k < nk; ++k) {
+  uint32_t u = 0;  // steps done: (m, l) of the current group live in m_run/l_run[u & 1]
+  for (int k = 0; k < nk;) {
     const int64_t c = cb + k;
     int g = cg;
     if (cg < 0 || c >= c_next) {
@@ -302,7 +301,7 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
     }
     if (g != cg) {
       if (cg >= 0) {
-        finish(k & 1);
+        finish(u & 1);
         cbar();
       }
       cg = g;
@@ -310,67 +309,63 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
       c_next = groups[g + 1].c0;
       q0 = gr.q0;
       mt = gr.mt;
-      // x rows of the group's tokens (rows past mt zero), then each warp's Xᵀ fragments
-      const int npc = d / 8;
-      for (int idx = tid; idx < kMT * npc; idx += kThreads) {
-        const int j = idx / npc, pc = idx - j * npc;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (j < mt) {
-          const int64_t i = int64_t(uint32_t(a.sorted_keys[q0 + j]));
-          v = __ldg(reinterpret_cast<const uint4*>(Xg + i * d) + pc);
+      // each warp's Xᵀ fragments for its k-steps, straight from x (tokens past mt zero):
+      // b0 = x[token g8][16 s + 2 t4 .. +1], b1 = x[token g8][16 s + 8 + 2 t4 .. +1]
+      const unsigned int* xrow = nullptr;
+      if (g8 < mt)
+        xrow = reinterpret_cast<const unsigned int*>(
+            Xg + int64_t(uint32_t(a.sorted_keys[q0 + g8])) * d);
+#pragma unroll
+      for (int i = 0; i < kMaxKSteps; ++i) {
+        const int s16 = warp + kWarps * i;
+        bx[i][0] = bx[i][1] = 0u;
+        if (s16 < nks && xrow) {
+          bx[i][0] = __ldg(xrow + 8 * s16 + t4);
+          bx[i][1] = __ldg(xrow + 8 * s16 + 4 + t4);
         }
-        *reinterpret_cast<uint4*>(xt + j * ks + pc * 16) = v;
       }
 #pragma unroll
       for (int mi = 0; mi < kMaxMTiles; ++mi) acc[mi][0] = acc[mi][1] = acc[mi][2] = acc[mi][3] = 0.f;
       if (tid < kMT) {
-        ms->m_run[k & 1][tid] = -INFINITY;
-        ms->l_run[k & 1][tid] = 0.f;
-      }
-      cbar();
-      // B fragment of step s16: tokens (lanes 0-7) at k 0-7, (lanes 8-15) at k 8-15
-      const uint32_t b_addr = xt_s + uint32_t((lane & 7) * ks + ((lane >> 3) & 1) * 16);
-#pragma unroll
-      for (int i = 0; i < kMaxKSteps; ++i) {
-        const int s16 = warp + kWarps * i;
-        if (s16 < nks) ldsm_x2(b_addr + s16 * 32, bx[i][0], bx[i][1]);
+        ms->m_run[u & 1][tid] = -INFINITY;
+        ms->l_run[u & 1][tid] = 0.f;
       }
     }
     const int j0 = int(c - gr.c0);
-    const int nr = gr.n - j0 * CH < CH ? gr.n - j0 * CH : CH;
+    const int nr0 = gr.n - j0 * CH < CH ? gr.n - j0 * CH : CH;
+    const bool pair = CH == 8 && k + 1 < nk && c + 1 < c_next;
+    const int nr1 = pair ? (gr.n - (j0 + 1) * CH < CH ? gr.n - (j0 + 1) * CH : CH) : 0;
+    const int step = pair ? 2 : 1;
 
     tc::mbar_wait(&ms->full[k % S], (k / S) & 1, abort_flag, a.st, 0x10000);
+    if (pair) tc::mbar_wait(&ms->full[(k + 1) % S], ((k + 1) / S) & 1, abort_flag, a.st, 0x10000);
     cbar();
     if (*abort_flag) {  // some consumer's wait ran out (it set the flag before the barrier)
       ok = false;
       break;
     }
-    const uint32_t st_s = ring_s + uint32_t((k % S) * sh.stage_bytes);
-    const uint32_t v_s = st_s + uint32_t(sh.k_bytes);
+    const uint32_t st0 = ring_s + uint32_t((k % S) * sh.stage_bytes);
+    const uint32_t st1 = pair ? ring_s + uint32_t(((k + 1) % S) * sh.stage_bytes) : st0;
 
-    // scores: Sᵀ = K_chunk Xᵀ
+    // scores: Sᵀ = K Xᵀ over the step's 16 rows
     {
       float sc[8][4];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) sc[u][0] = sc[u][1] = sc[u][2] = sc[u][3] = 0.f;
-      // A: matrix q from lanes 8q..8q+7; rows (lane & 7) (+8 for q odd when CH == 16),
-      // k offset 8 for q >= 2 (CH == 16) or q == 1 (CH == 8, two matrices).
-      const int arow = (lane & 7) + (CH == 16 ? ((lane >> 3) & 1) * 8 : 0);
-      const int akof = CH == 16 ? (lane >> 4) * 8 : ((lane >> 3) & 1) * 8;
+      for (int u8 = 0; u8 < 8; ++u8) sc[u8][0] = sc[u8][1] = sc[u8][2] = sc[u8][3] = 0.f;
+      // A: matrix q from lanes 8q..8q+7 (q = 0: rows 0-7, k 0-7; 1: rows 8-15, k 0-7;
+      // 2: rows 0-7, k 8-15; 3: rows 8-15, k 8-15). Rows 8-15 are the second stage's rows
+      // 0-7 for a pair, the first stage's again (masked) for a lone 8-row chunk.
+      const bool hi_rows = ((lane >> 3) & 1) != 0;
+      const int arow = CH == 16 ? (lane & 7) + (hi_rows ? 8 : 0) : (lane & 7);
+      const uint32_t abase = (CH == 8 && hi_rows) ? st1 : st0;
+      const int akof = (lane >> 4) * 8;
 #pragma unroll
       for (int i = 0; i < kMaxKSteps; ++i) {
         const int s16 = warp + kWarps * i;
         if (s16 < nks) {
-          const uint32_t addr = st_s + sw128(CH, arow, s16 * 16 + akof);
-          if (CH == 16) {
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4(addr, a0, a1, a2, a3);
-            mma16(sc[i & 7], a0, a1, a2, a3, bx[i][0], bx[i][1]);
-          } else {
-            uint32_t a0, a2;
-            ldsm_x2(addr, a0, a2);
-            mma16(sc[i & 7], a0, a0, a2, a2, bx[i][0], bx[i][1]);  // rows 8-15 repeat 0-7
-          }
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(abase + sw128(CH, arow, s16 * 16 + akof), a0, a1, a2, a3);
+          mma16(sc[i & 7], a0, a1, a2, a3, bx[i][0], bx[i][1]);
         }
       }
 #pragma unroll
@@ -383,18 +378,19 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
     cbar();
     // softmax update: thread (token j = tid / 16, row r = tid % 16) sums the warps' partial
     // score, and the 16 lanes of a token reduce max and sum by shuffles.
-    const int par = k & 1;
+    const uint32_t par = u & 1;
     if (tid < 16 * kMT) {
       const int j = tid >> 4, r = tid & 15;
-      float s = 0.f;
+      const bool rv = CH == 16 ? r < nr0 : (r < 8 ? r < nr0 : r - 8 < nr1);
+      float sv = 0.f;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) s += ms->red[w][r][j];
+      for (int w = 0; w < kWarps; ++w) sv += ms->red[w][r][j];
       const float mo = ms->m_run[par][j];
-      float mx = r < nr ? s : -INFINITY;
+      float mx = rv ? sv : -INFINITY;
 #pragma unroll
       for (int o = 8; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
       const float mn = fmaxf(mo, mx);
-      const float e = (r < nr && j < mt) ? expf(s - mn) : 0.f;
+      const float e = (rv && j < mt) ? expf(sv - mn) : 0.f;
       float sum = e;
 #pragma unroll
       for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
@@ -411,15 +407,18 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
       }
     }
     cbar();
-    // values: accᵀ = accᵀ * scale + V_chunkᵀ Pᵀ (P as bf16 hi + lo)
+    // values: accᵀ = accᵀ * scale + Vᵀ Pᵀ over the step's 16 rows (P as bf16 hi + lo)
     {
       const float sc0 = ms->scale[2 * t4], sc1 = ms->scale[2 * t4 + 1];
-      uint32_t bh0, bl0, bh1 = 0, bl1 = 0;
+      uint32_t bh0, bl0, bh1, bl1;
       split_pair(ms->e_buf[2 * t4][g8], ms->e_buf[2 * t4 + 1][g8], bh0, bl0);
-      if (CH == 16) split_pair(ms->e_buf[2 * t4 + 8][g8], ms->e_buf[2 * t4 + 9][g8], bh1, bl1);
-      // Vᵀ tile (16 value columns x CH rows) by transposing loads: lanes 0-7 rows 0-7 at
-      // column 0, lanes 8-15 rows 0-7 at column 8, lanes 16-31 rows 8-15.
-      const int vrow = (lane & 7) + (CH == 16 ? (lane >> 4) * 8 : 0);
+      split_pair(ms->e_buf[2 * t4 + 8][g8], ms->e_buf[2 * t4 + 9][g8], bh1, bl1);
+      // Vᵀ tile (16 value columns x 16 rows) by transposing loads: lanes 0-7 rows 0-7 at
+      // column 0, lanes 8-15 rows 0-7 at column 8, lanes 16-31 rows 8-15 (the second
+      // stage's rows 0-7 for a pair; the first stage's again, with zero weights, otherwise).
+      const bool hi_k = (lane >> 4) != 0;
+      const int vrow = CH == 16 ? (lane & 7) + (hi_k ? 8 : 0) : (lane & 7);
+      const uint32_t vbase = ((CH == 8 && hi_k) ? st1 : st0) + uint32_t(sh.k_bytes);
       const int vcol = ((lane >> 3) & 1) * 8;
       uint32_t va[kMaxMTiles][4];
 #pragma unroll
@@ -430,11 +429,8 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
           acc[mi][1] *= sc1;
           acc[mi][2] *= sc0;
           acc[mi][3] *= sc1;
-          const uint32_t addr = v_s + sw128(CH, vrow, 16 * mtile + vcol);
-          if (CH == 16)
-            ldsm_x4_t(addr, va[mi][0], va[mi][1], va[mi][2], va[mi][3]);
-          else
-            ldsm_x2_t(addr, va[mi][0], va[mi][1]);
+          ldsm_x4_t(vbase + sw128(CH, vrow, 16 * mtile + vcol), va[mi][0], va[mi][1], va[mi][2],
+                    va[mi][3]);
         }
       }
       // all hi products, then all lo products: dependent pairs are kMaxMTiles mmas apart
@@ -442,21 +438,21 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
       for (int h = 0; h < 2; ++h) {
         const uint32_t b0 = h ? bl0 : bh0, b1 = h ? bl1 : bh1;
 #pragma unroll
-        for (int mi = 0; mi < kMaxMTiles; ++mi) {
-          if (warp + kWarps * mi < n_mt) {
-            if (CH == 16)
-              mma16(acc[mi], va[mi][0], va[mi][1], va[mi][2], va[mi][3], b0, b1);
-            else
-              mma8(acc[mi], va[mi][0], va[mi][1], b0);
-          }
-        }
+        for (int mi = 0; mi < kMaxMTiles; ++mi)
+          if (warp + kWarps * mi < n_mt)
+            mma16(acc[mi], va[mi][0], va[mi][1], va[mi][2], va[mi][3], b0, b1);
       }
     }
-    cbar();  // the stage and the score buffers are free again
-    if (tid == 0) tc::mbar_arrive(&ms->empty[k % S]);
+    cbar();  // the stages and the score buffers are free again
+    if (tid == 0) {
+      tc::mbar_arrive(&ms->empty[k % S]);
+      if (pair) tc::mbar_arrive(&ms->empty[(k + 1) % S]);
+    }
+    k += step;
+    ++u;
   }
 
-  if (ok && cg >= 0) finish(nk & 1);
+  if (ok && cg >= 0) finish(u & 1);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {

@@ -61,13 +61,12 @@ __device__ __forceinline__ float* part_entry(const AttendArgs& a, int64_t b, boo
 
 // After this CTA wrote its partial for group g (chunks [c0, c1)): count it and, in the CTA
 // that completes the group, merge all partials in CTA order and write the group's outputs.
-// Called by the CTA's `nthr` working threads (thread indices 0 .. nthr-1); `bar()` is a
+// Called by the CTA's `nthr` working threads, numbered tid = 0 .. nthr-1; `bar()` is a
 // barrier over exactly those threads; `last` is a shared-memory flag.
 template <typename Bar>
 __device__ inline void arrive_and_merge(const AttendArgs& a, int g, int64_t c0, int64_t c1,
                                         int64_t C, int64_t G, int q0, int mt, int* last,
-                                        int nthr, Bar bar) {
-  const int tid = threadIdx.x;
+                                        int tid, int nthr, Bar bar) {
   __threadfence();
   bar();
   const int b0 = cta_of(c0, C, G), b1 = cta_of(c1 - 1, C, G);
