@@ -13,7 +13,9 @@
 //   phase 2   Aᵀ = V_tᵀ Pᵀ           M = 128 value columns per chunk, N tokens, K = rows
 //                                    in 16-row steps (both operands MN-major).
 //   epilogue  a = Aᵀ / l, scattered to batch order (bf16 for the GEMM, fp32 if asked).
-// K_t, V_t rows arrive by TMA in 16-row boxes, so an id with few rows moves few bytes.
+// K_t rows arrive by TMA in 128-row boxes, V_t rows in 64-row boxes and x in 64-token
+// boxes (rows past an item's range are read and masked): few large copies per stage, since
+// each TMA instruction costs tens of nanoseconds to issue.
 // One persistent CTA per SM, 6 warps: TMA producer, MMA issuer, 4 softmax/epilogue
 // warps (one TMEM lane each). All waits are bounded; the softmax warps synchronise on an
 // mbarrier (bounded) rather than a named barrier, so no thread can be left waiting.
@@ -179,8 +181,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int Nt = (item.nt + 15) & ~15;
         const int RC = (n + 127) / 128;
         for (int rc = 0; ok && rc < RC; ++rc) {
-          const int nvalid = n - 128 * rc < 128 ? n - 128 * rc : 128;
-          const int nbox = (nvalid + 15) / 16;
           for (int kb = 0; kb < KB; ++kb) {
             const uint32_t s = it % kStages, ph = (it / kStages) & 1;
             if (!tc::mbar_wait(&empty[s], ph ^ 1, abort_flag, p.st, 0x100)) {
@@ -188,19 +188,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             unsigned char* st = stages + s * kStageBytes;
-            tc::mbar_arrive_expect_tx(&full[s], uint32_t(nbox + Nt / 16) * 2048u);
-            for (int bx = 0; bx < nbox; ++bx)
-              tc::tma_load_2d(&mapK, &full[s], st + bx * 2048, kb * 64, r0 + 128 * rc + 16 * bx);
-            for (int bx = 0; bx < Nt / 16; ++bx)
-              tc::tma_load_2d(&mapX, &full[s], st + kKTile + bx * 2048, kb * 64,
-                              item.q0 + 16 * bx);
+            // one 128-row box of K (rows past the item's range are read and masked) and one
+            // 64-token box of x: few, large copies keep the TMA unit's issue rate off the
+            // critical path
+            tc::mbar_arrive_expect_tx(&full[s], uint32_t(kStageBytes));
+            tc::tma_load_2d(&mapK, &full[s], st, kb * 64, r0 + 128 * rc);
+            tc::tma_load_2d(&mapX, &full[s], st + kKTile, kb * 64, item.q0);
             ++it;
           }
         }
         const int NB = (n + 63) / 64;
         for (int b = 0; ok && b < NB; ++b) {
-          const int vrows = n - 64 * b < 64 ? n - 64 * b : 64;
-          const int nbox = (vrows + 15) / 16;
           for (int dc = 0; dc < DC; ++dc) {
             const uint32_t s = it % kStages, ph = (it / kStages) & 1;
             if (!tc::mbar_wait(&empty[s], ph ^ 1, abort_flag, p.st, 0x100)) {
@@ -208,11 +206,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             unsigned char* st = stages + s * kStageBytes;
-            tc::mbar_arrive_expect_tx(&full[s], uint32_t(2 * nbox) * 2048u);
+            tc::mbar_arrive_expect_tx(&full[s], 2u * 8192u);
             for (int h = 0; h < 2; ++h)
-              for (int bx = 0; bx < nbox; ++bx)
-                tc::tma_load_2d(&mapV, &full[s], st + h * 8192 + bx * 2048, dc * 128 + h * 64,
-                                r0 + 64 * b + 16 * bx);
+              tc::tma_load_2d(&mapV, &full[s], st + h * 8192, dc * 128 + h * 64, r0 + 64 * b);
             ++it;
           }
         }
@@ -464,13 +460,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// bf16 [rows, cols] row-major; box 16 rows x 64 columns, 128-byte swizzle.
-bool make_map16(CUtensorMap* map, const void* base, int64_t rows, int64_t cols) {
+// bf16 [rows, cols] row-major; box box_rows rows x 64 columns, 128-byte swizzle.
+bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
   cuuint64_t strides[1] = {cuuint64_t(cols) * 2};
-  cuuint32_t box[2] = {64, 16};
+  cuuint32_t box[2] = {64, cuuint32_t(box_rows)};
   cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -504,8 +500,8 @@ cudaError_t launch_attend_tc(const AttendTcArgs& a, cudaStream_t stream) {
   count_launch();
   const Item* items = a.items;
   CUtensorMap mk, mx, mv;
-  if (!make_map16(&mk, a.K, a.v, a.d) || !make_map16(&mx, a.x_sorted, a.T, a.d) ||
-      !make_map16(&mv, a.V, a.v, a.d_v))
+  if (!make_map(&mk, a.K, a.v, a.d, 128) || !make_map(&mx, a.x_sorted, a.T, a.d, kNT) ||
+      !make_map(&mv, a.V, a.v, a.d_v, 64))
     return cudaErrorInvalidValue;
   TcAttendParams p{};
   p.items = items;
