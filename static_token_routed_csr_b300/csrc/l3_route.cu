@@ -3,9 +3,10 @@
 // layer's attention mask block-diagonal).
 //
 // Keys are (id << 32) | batch position. They are unique, so any correct sort of the keys
-// is the stable sort of the ids. Batches up to kSmallT tokens are sorted by one CTA in
-// shared memory (bitonic); larger ones are cut into kChunk-key runs sorted the same way,
-// then merged pairwise (each key finds its rank in the other run by binary search).
+// is the stable sort of the ids. With ids below 2^19, blocks of 8192 tokens are sorted by
+// one CTA each with a stable radix sort on the ids; otherwise blocks of 4096 keys are
+// sorted by a shared-memory bitonic network. Blocks are then merged pairwise (each key
+// finds its rank in the other run by binary search).
 // A last pass marks segment starts and numbers the segments, and (for the forward) lays out
 // the work plan of the split-row gather-attend.
 #include "l3_internal.h"
@@ -221,6 +222,140 @@ __global__ void __launch_bounds__(1024) route_chunk_kernel(const int32_t* __rest
     if (base + i < T) keys_out[base + i] = s[i];
 }
 
+// ---- one-CTA stable radix sort of up to 8192 ids ----------------------------------------------
+//
+// 32-bit keys (id << 13 | index within the CTA's block of 8192); an LSD radix sort on the
+// id bits, 8 bits per pass, keeps equal ids in index order. Per pass each warp ranks its
+// 256 keys in index order (warp w holds indices 256 w + 32 e + lane, e = 0..7) with
+// __match_any_sync over the digit, a per-digit prefix over the 32 warps and a scan over the
+// 256 digits place every key, and the keys are scattered to the other buffer.
+constexpr int kRadixN = 8192;
+constexpr int kIdxBits = 13;
+
+struct RadixSmem {
+  uint32_t buf[2][kRadixN];
+  uint32_t cnt[32][256];
+  uint32_t dstart[256];
+  int warp_tot[32];
+};
+
+// Sorts buf[0][0 .. 8192) by key >> 13 (stable); returns the buffer that holds the result.
+__device__ int block_radix_sort(RadixSmem& sm, int passes) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t lt = (1u << lane) - 1u;
+  int cur = 0;
+  for (int p = 0; p < passes; ++p) {
+    const int sh = kIdxBits + 8 * p;
+    for (int i = tid; i < 32 * 256; i += 1024) (&sm.cnt[0][0])[i] = 0;
+    __syncthreads();
+    uint32_t key[8];
+    int dig[8], rank[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      key[e] = sm.buf[cur][warp * 256 + e * 32 + lane];
+      dig[e] = int((key[e] >> sh) & 255u);
+      const uint32_t peers = __match_any_sync(0xffffffffu, dig[e]);
+      const uint32_t before = sm.cnt[warp][dig[e]];
+      rank[e] = int(before + __popc(peers & lt));
+      __syncwarp();
+      if ((peers & lt) == 0) sm.cnt[warp][dig[e]] = before + __popc(peers);  // lowest lane
+      __syncwarp();
+    }
+    __syncthreads();
+    int tot = 0, incl = 0;
+    if (tid < 256) {
+      uint32_t run = 0;
+      for (int w = 0; w < 32; ++w) {
+        const uint32_t c = sm.cnt[w][tid];
+        sm.cnt[w][tid] = run;
+        run += c;
+      }
+      tot = int(run);
+      incl = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
+      }
+      if (lane == 31) sm.warp_tot[warp] = incl;
+    }
+    __syncthreads();
+    if (tid < 256) {
+      int off = 0;
+      for (int w = 0; w < warp; ++w) off += sm.warp_tot[w];
+      sm.dstart[tid] = uint32_t(off + incl - tot);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      sm.buf[cur ^ 1][sm.dstart[dig[e]] + sm.cnt[warp][dig[e]] + rank[e]] = key[e];
+    __syncthreads();
+    cur ^= 1;
+  }
+  return cur;
+}
+
+// Keys of the block [base, base + 8192) of the batch: (id << 13 | local index); past T all
+// bits set (they sort last). Ids outside [0, vocab) are reported and treated as id 0.
+__device__ void radix_load(RadixSmem& sm, const int32_t* ids, int64_t T, int64_t vocab,
+                           int64_t base, DevStatus* st) {
+  for (int i = threadIdx.x; i < kRadixN; i += blockDim.x) {
+    uint32_t key = 0xffffffffu;
+    if (base + i < T) {
+      int32_t id = ids[base + i];
+      if (id < 0 || int64_t(id) >= vocab) {
+        atomicOr(&st->token_range, 1);
+        id = 0;
+      }
+      key = (uint32_t(id) << kIdxBits) | uint32_t(i);
+    }
+    sm.buf[0][i] = key;
+  }
+  __syncthreads();
+}
+
+__device__ __forceinline__ uint64_t wide_key(uint32_t k, int64_t base) {
+  return (uint64_t(k >> kIdxBits) << 32) | uint64_t(base + (k & (kRadixN - 1)));
+}
+
+// T <= 8192: sort, segments and plan in one CTA.
+__global__ void __launch_bounds__(1024) route_radix_small_kernel(
+    const int32_t* __restrict__ ids, int64_t T, int64_t vocab, int passes, uint64_t* keys_out,
+    int32_t* perm, int32_t* seg_start, int32_t* seg_id, int32_t* n_seg, DevStatus* st,
+    const PlanOut plan, int with_plan) {
+  extern __shared__ __align__(16) unsigned char dyn[];
+  RadixSmem& sm = *reinterpret_cast<RadixSmem*>(dyn);
+  uint64_t* k64 = reinterpret_cast<uint64_t*>(dyn + sizeof(RadixSmem));
+  __shared__ int warp_tot[32];
+  __shared__ int total;
+  radix_load(sm, ids, T, vocab, 0, st);
+  const int cur = block_radix_sort(sm, passes);
+  for (int i = threadIdx.x; i < T; i += blockDim.x) {
+    const uint64_t k = wide_key(sm.buf[cur][i], 0);
+    k64[i] = k;
+    keys_out[i] = k;
+  }
+  __syncthreads();
+  segment_pass(k64, T, perm, seg_start, seg_id, n_seg, with_plan ? &plan : nullptr, st, warp_tot,
+               &total);
+}
+
+// T > 8192: each CTA sorts one block of 8192 keys (merged afterwards).
+__global__ void __launch_bounds__(1024) route_radix_chunk_kernel(const int32_t* __restrict__ ids,
+                                                                 int64_t T, int64_t vocab,
+                                                                 int passes, uint64_t* keys_out,
+                                                                 DevStatus* st) {
+  extern __shared__ __align__(16) unsigned char dyn[];
+  RadixSmem& sm = *reinterpret_cast<RadixSmem*>(dyn);
+  const int64_t base = int64_t(blockIdx.x) * kRadixN;
+  radix_load(sm, ids, T, vocab, base, st);
+  const int cur = block_radix_sort(sm, passes);
+  for (int i = threadIdx.x; i < kRadixN; i += blockDim.x)
+    if (base + i < T) keys_out[base + i] = wide_key(sm.buf[cur][i], base);
+}
+
+constexpr size_t kRadixSmallSmem = sizeof(RadixSmem) + kRadixN * sizeof(uint64_t);
+
 // Number of keys in a[0..n) smaller than key (a sorted ascending).
 __device__ inline int64_t lower_bound(const uint64_t* a, int64_t n, uint64_t key) {
   int64_t lo = 0, hi = n;
@@ -277,6 +412,43 @@ cudaError_t launch_route(const int32_t* ids, int64_t T, int64_t vocab, void* scr
   uint64_t* k0 = static_cast<uint64_t*>(scratch);
   uint64_t* k1 = reinterpret_cast<uint64_t*>(static_cast<char*>(scratch) +
                                              align_up(size_t(T) * sizeof(uint64_t), kAlign));
+  // bits of the largest id; the radix path packs (id, index) into 32 bits
+  int idbits = 1;
+  while (idbits < 31 && (int64_t(1) << idbits) < vocab) ++idbits;
+  if (idbits + kIdxBits <= 32) {
+    static cudaError_t a1 = cudaFuncSetAttribute(
+        route_radix_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kRadixSmallSmem));
+    static cudaError_t a2 = cudaFuncSetAttribute(
+        route_radix_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sizeof(RadixSmem)));
+    if (a1 != cudaSuccess) return a1;
+    if (a2 != cudaSuccess) return a2;
+    const int passes = (idbits + 7) / 8;
+    if (T <= kRadixN) {
+      route_radix_small_kernel<<<1, 1024, kRadixSmallSmem, stream>>>(
+          ids, T, vocab, passes, k0, out.perm, out.seg_start, out.seg_id, out.n_seg, st, pl,
+          with_plan);
+      count_launch();
+      *sorted_keys = k0;
+      return cudaGetLastError();
+    }
+    const int64_t nblk = (T + kRadixN - 1) / kRadixN;
+    route_radix_chunk_kernel<<<unsigned(nblk), 1024, sizeof(RadixSmem), stream>>>(
+        ids, T, vocab, passes, k0, st);
+    count_launch();
+    uint64_t *src = k0, *dst = k1;
+    for (int64_t w = kRadixN; w < T; w *= 2) {
+      route_merge_kernel<<<unsigned((T + 255) / 256), 256, 0, stream>>>(src, dst, T, w);
+      count_launch();
+      uint64_t* t = src;
+      src = dst;
+      dst = t;
+    }
+    route_segment_kernel<<<1, 1024, 0, stream>>>(src, T, out.perm, out.seg_start, out.seg_id,
+                                                 out.n_seg, st, pl, with_plan);
+    count_launch();
+    *sorted_keys = src;
+    return cudaGetLastError();
+  }
   if (T <= kChunk) {
     route_small_kernel<<<1, 1024, 0, stream>>>(ids, T, vocab, k0, out.perm, out.seg_start,
                                                out.seg_id, out.n_seg, st, pl, with_plan);
