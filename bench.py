@@ -43,20 +43,39 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0}
 # ---- host-side workload accounting ---------------------------------------------------------------
 
 def workload_bytes(p, ids: np.ndarray, offs: np.ndarray) -> dict:
-    """Algorithmic bytes and FLOPs of one forward over the batch (per kernel stage)."""
+    """Algorithmic bytes and FLOPs of one forward over the batch (per kernel stage).
+
+    A distinct id's table rows are read once, each token's x row once and its a row
+    written once. Ids held by at least ``long_th`` tokens of the batch go to the
+    tensor-core kernel ("attend_long"), the rest to the split-row kernel ("attend");
+    ``long_th`` is 8 for bf16 batches of at least 1024 tokens and 0 (no split) otherwise,
+    the same rule the library applies.
+    """
     b = 2 if p.dtype == "bf16" else 4
-    uniq = np.unique(ids)
-    n = np.diff(offs.astype(np.int64))
-    uniq_rows = int(n[uniq].sum())
     T = len(ids)
-    attend = uniq_rows * (p.d + p.d_v) * b + T * p.d * b + T * p.d_v * b
+    long_th = 8 if (p.dtype == "bf16" and T >= 1024 and p.d % 64 == 0
+                    and p.d_v % 128 == 0 and p.d_v <= 512) else 0
+    uniq, cnt = np.unique(ids, return_counts=True)
+    n = np.diff(offs.astype(np.int64))
+    is_long = cnt >= long_th if long_th > 0 else np.zeros(len(uniq), bool)
+
+    def part(mask):
+        rows = int(n[uniq[mask]].sum())
+        tok = int(cnt[mask].sum())
+        return rows * (p.d + p.d_v) * b + tok * (p.d + p.d_v) * b
+
+    uniq_rows = int(n[uniq].sum())
     logical = int(n[ids].sum()) * (p.d + p.d_v) * b + 2 * T * p.d * b
     return {
         "unique_rows": uniq_rows,
         "distinct_ids": int(len(uniq)),
-        "attend_bytes": attend,
+        "long_threshold": long_th,
+        "long_ids": int(is_long.sum()),
+        "attend_bytes": part(np.ones(len(uniq), bool)),
+        "attend_short_bytes": part(~is_long),
+        "attend_long_bytes": part(is_long),
+        "route_bytes": T * 4 * 3 + 2 * len(uniq) * 8,
         "logical_bytes": logical,
-        "unique_bytes": uniq_rows * (p.d + p.d_v) * b + 2 * T * p.d * b + (p.d * p.d_v + 2 * p.d * p.d) * b,
         "up_flops": 2 * T * p.d * p.d_v,
         "mix_flops": 4 * T * p.d * p.d,
     }
@@ -394,9 +413,13 @@ def run_ours(args, rank, world, local_rank):
     names = l3.STAGE_NAMES
     dom = int(np.argmax(stage_ms))
     dom_s = stage_ms[dom] / 1e3
-    if names[dom] in ("route", "attend"):
-        achieved = acct["attend_bytes"] / dom_s / 1e9
-        roof = {"kernel": "gather-attend", "bound": "hbm", "achieved": achieved,
+    hbm_bytes = {"route": acct["route_bytes"], "attend": acct["attend_short_bytes"],
+                 "attend_long": acct["attend_long_bytes"]}
+    if names[dom] in hbm_bytes:
+        achieved = hbm_bytes[names[dom]] / dom_s / 1e9
+        kern = {"route": "route", "attend": "gather-attend (split-row)",
+                "attend_long": "gather-attend (tensor-core)"}[names[dom]]
+        roof = {"kernel": kern, "bound": "hbm", "achieved": achieved,
                 "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                 "traffic": None}
     else:
@@ -406,7 +429,7 @@ def run_ours(args, rank, world, local_rank):
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": achieved / peaks["bf16_tflops"], "traffic": None}
     roof["peak_source"] = peaks["source"]
-    attend_s = stage_ms[1] / 1e3
+    attend_s = (stage_ms[names.index("attend")] + stage_ms[names.index("attend_long")]) / 1e3
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
@@ -418,7 +441,11 @@ def run_ours(args, rank, world, local_rank):
                        "logical_gbs": acct["logical_bytes"] / attend_s / 1e9,
                        "frac_of_8tbs": acct["attend_bytes"] / attend_s / 8e12,
                        "frac_of_measured": acct["attend_bytes"] / attend_s / 1e9 / peaks["hbm_gbs"],
-                       "unique_rows": acct["unique_rows"], "distinct_ids": acct["distinct_ids"]},
+                       "unique_rows": acct["unique_rows"], "distinct_ids": acct["distinct_ids"],
+                       "long_threshold": acct["long_threshold"], "long_ids": acct["long_ids"],
+                       "short_gbs": acct["attend_short_bytes"] / (stage_ms[names.index("attend")] / 1e3) / 1e9,
+                       "long_gbs": (acct["attend_long_bytes"] / (stage_ms[names.index("attend_long")] / 1e3) / 1e9
+                                    if stage_ms[names.index("attend_long")] > 0 else None)},
         "roofline": roof,
         "e2e": {"value": world * T * args.steps / (e2e_ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": T * 4 + T * p.d * esz, "d2h_bytes_per_step": T * p.d * esz},

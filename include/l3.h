@@ -40,7 +40,7 @@
 extern "C" {
 #endif
 
-#define L3_ABI_VERSION 1
+#define L3_ABI_VERSION 2
 
 typedef struct CUstream_st* l3_stream_t; /* = cudaStream_t */
 typedef struct CUevent_st* l3_event_t;   /* = cudaEvent_t  */
@@ -95,11 +95,12 @@ enum { L3_PASS_FORWARD = 0, L3_PASS_BACKWARD = 1, L3_PASS_FORWARD_HOST = 2 };
 
 /* Stages of l3_forward, for l3_forward_timed. */
 enum {
-  L3_STAGE_ROUTE = 0,  /* sort the batch by token id, build segments             */
-  L3_STAGE_ATTEND = 1, /* a = V_tᵀ softmax(K_t x) for every token                 */
-  L3_STAGE_UP = 2,     /* u = W_up a, LayerNorm statistics                         */
-  L3_STAGE_MIX = 3,    /* y = W_mix [LayerNorm(u); x]                              */
-  L3_FWD_STAGES = 4
+  L3_STAGE_ROUTE = 0,       /* sort the batch by token id, build segments and work plan */
+  L3_STAGE_ATTEND = 1,      /* a = V_tᵀ softmax(K_t x), tokens of short segments        */
+  L3_STAGE_ATTEND_LONG = 2, /* the same for tokens of long segments (large bf16 batches) */
+  L3_STAGE_UP = 3,          /* u = W_up a, LayerNorm statistics                         */
+  L3_STAGE_MIX = 4,         /* y = W_mix [LayerNorm(u); x]                              */
+  L3_FWD_STAGES = 5
 };
 
 /*

@@ -26,8 +26,8 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libl3.so")
 
 L3_F32, L3_BF16 = 0, 1
 L3_PASS_FORWARD, L3_PASS_BACKWARD, L3_PASS_FORWARD_HOST = 0, 1, 2
-L3_FWD_STAGES = 4
-STAGE_NAMES = ("route", "attend", "up", "mix")
+L3_FWD_STAGES = 5
+STAGE_NAMES = ("route", "attend", "attend_long", "up", "mix")
 STATUS = {0: "L3_OK", 1: "L3_ERR_INVALID_ARG", 2: "L3_ERR_INFEASIBLE", 3: "L3_ERR_UNSUPPORTED",
           4: "L3_ERR_WORKSPACE", 5: "L3_ERR_TOKEN_RANGE", 6: "L3_ERR_CUDA", 7: "L3_ERR_LAYER",
           8: "L3_ERR_TIMEOUT"}

@@ -238,6 +238,7 @@ l3_status forward_impl(const l3_layer* L, const int32_t* ids, int64_t T, const v
     aa.st = w.st;
     L3_CUDA(launch_attend_fwd(aa, s));
   }
+  if (ev) L3_CUDA(record_stage(ev[L3_STAGE_ATTEND_LONG], s));
   if (w.tc_th > 0) {
     AttendTcArgs at{};
     at.sorted_keys = keys;

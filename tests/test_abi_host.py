@@ -39,7 +39,7 @@ def test_exports_every_declared_symbol(lib):
     assert len(names) >= 12
     for n in names:
         assert hasattr(lib, n), n
-    assert l3.l3_abi_version() == 1
+    assert l3.l3_abi_version() == 2
     assert l3.l3_status_string(5) == "L3_ERR_TOKEN_RANGE"
 
 
