@@ -56,6 +56,9 @@ struct FwdWs {
   AttendGroup* groups;
   int32_t* plan_hdr;
   int32_t* counters;
+  int32_t* cta_start;  // the plan's split of the chunk list over the split-row kernel's CTAs
+  int32_t* cta_group;
+  int n_cta;
   AttendItem* items;
   float* a_f32;
   __nv_bfloat16* a_bf16;
@@ -89,6 +92,9 @@ FwdWs carve_fwd(Carve& c, const l3_layer* L, int64_t T) {
   w.groups = c.take<AttendGroup>(t + 1);
   w.plan_hdr = c.take<int32_t>(kPlanHdrWords);
   w.counters = c.take<int32_t>(t);
+  w.n_cta = attend_split_ctas(int(d), int(dv), L->dtype);
+  w.cta_start = c.take<int32_t>(size_t(kPlanMaxCtas) + 1);
+  w.cta_group = c.take<int32_t>(size_t(kPlanMaxCtas));
   w.tc_th = attend_tc_threshold(T, int(d), int(dv), L->dtype);
   if (w.tc_th > 0) {
     w.max_items = int(T / w.tc_th + 1);
@@ -209,7 +215,9 @@ l3_status forward_impl(const l3_layer* L, const int32_t* ids, int64_t T, const v
   const uint64_t* keys = nullptr;
   const int ch = attend_rows_per_chunk(d, dv, L->dtype);
   PlanOut plan{w.groups, w.plan_hdr, w.counters, w.items, L->offs, L->v, L->k_max, ch,
-               attend_group_tokens(L->dtype), w.tc_th > 0 ? w.tc_th : INT32_MAX};
+               attend_group_tokens(L->dtype), w.tc_th > 0 ? w.tc_th : INT32_MAX,
+               w.cta_start, w.cta_group, w.n_cta, 0, 0};
+  attend_split_weights(d, dv, L->dtype, &plan.w_chunk, &plan.w_group);
   L3_CUDA(launch_route(ids, T, L->vocab, w.route_scratch,
                        RouteOut{w.perm, w.seg_start, w.seg_id, w.n_seg}, w.st, s, &keys, &plan));
 
@@ -235,6 +243,9 @@ l3_status forward_impl(const l3_layer* L, const int32_t* ids, int64_t T, const v
     aa.a_bf16 = w.a_bf16;
     aa.ml = ml;
     aa.part = w.part;
+    aa.cta_start = w.cta_start;
+    aa.cta_group = w.cta_group;
+    aa.n_cta = w.n_cta;
     aa.st = w.st;
     L3_CUDA(launch_attend_fwd(aa, s));
   }

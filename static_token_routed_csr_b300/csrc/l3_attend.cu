@@ -42,7 +42,7 @@ struct Misc {
   float m_run[2][kMT];
   float l_run[2][kMT];
   float scale[kMT];
-  int last;
+  MergeSmem merge;
   int abort;
 };
 
@@ -130,12 +130,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_split_kernel(const AttendA
   Misc* ms = reinterpret_cast<Misc*>(base + sh.stages * sh.stage_bytes + sh.x_bytes);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n_groups = a.hdr[kPlanGroups];
-  const int64_t C = a.hdr[kPlanChunks];
-  const int64_t G = int64_t(gridDim.x) < C ? int64_t(gridDim.x) : C;
   const int b = blockIdx.x;
-  if (b >= G) return;
-  const int64_t cb = int64_t(b) * C / G, ce = int64_t(b + 1) * C / G;
+  const int64_t cb = a.cta_start[b], ce = a.cta_start[b + 1];
+  if (cb >= ce) return;
   const int nk = int(ce - cb);
   const int d = a.d, dv = a.d_v, ch = sh.ch, S = sh.stages;
   const int npk = d / P;  // 16-byte pieces of a K or x row
@@ -154,7 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_split_kernel(const AttendA
 
   // Producer state (thread 0): next chunk to issue and its group.
   int issued = 0;
-  int pg = find_group(groups, n_groups, cb);
+  int pg = a.cta_group[b];
   auto issue = [&](int k) {
     const int64_t c = cb + k;
     while (groups[pg + 1].c0 <= c) ++pg;
@@ -207,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_split_kernel(const AttendA
         pe[1] = ms->l_run[par][j];
       }
     }
-    arrive_and_merge(a, cg, c0, c1, C, G, q0, mt, &ms->last, int(threadIdx.x), kThreads,
+    arrive_and_merge(a, cg, c0, c1, cb, ce, q0, mt, &ms->merge, int(threadIdx.x), kThreads,
                      [] { __syncthreads(); });
   };
 
@@ -217,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_split_kernel(const AttendA
       issue(issued++);
     }
     const int64_t c = cb + k;
-    int g = cg < 0 ? find_group(groups, n_groups, c) : cg;
+    int g = cg < 0 ? a.cta_group[b] : cg;
     while (groups[g + 1].c0 <= c) ++g;
     if (g != cg) {
       if (cg >= 0) {
@@ -341,9 +338,8 @@ cudaError_t launch_split(const AttendArgs& a, cudaStream_t stream) {
   static cudaError_t attr = cudaFuncSetAttribute(
       attend_split_kernel<TE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
   if (attr != cudaSuccess) return attr;
-  int grid = sm_count();
-  if (grid > kMaxCtas) grid = kMaxCtas;
-  attend_split_kernel<TE><<<grid, kThreads, sh.smem, stream>>>(a, sh);
+  if (a.n_cta < 1 || a.n_cta > kMaxCtas) return cudaErrorInvalidValue;
+  attend_split_kernel<TE><<<a.n_cta, kThreads, sh.smem, stream>>>(a, sh);
   count_launch();
   return cudaGetLastError();
 }
@@ -364,6 +360,19 @@ int sm_count() {
 }  // namespace split
 
 cudaError_t launch_attend_mma(const AttendArgs& a, cudaStream_t stream);
+int attend_mma_ctas(int d, int d_v);
+
+int attend_split_ctas(int d, int d_v, int dtype) {
+  if (dtype == L3_BF16) return attend_mma_ctas(d, d_v);
+  return sm_count() < kMaxCtas ? sm_count() : kMaxCtas;
+}
+
+// Cost units of the plan's CTA split, in about 0.2 us of one CTA's time: a chunk, and the
+// extra work of a group (its x rows, its outputs, and an unpaired last chunk).
+void attend_split_weights(int, int, int, int* w_chunk, int* w_group) {
+  *w_chunk = 4;
+  *w_group = 5;
+}
 
 int attend_group_tokens(int) { return kPlanMT; }
 

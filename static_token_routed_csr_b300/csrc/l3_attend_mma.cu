@@ -48,17 +48,29 @@ constexpr int kCtaThreads = kThreads + 32;  // + one producer warp (TMA copies)
 constexpr int kMaxStages = 6;
 constexpr int kMaxMTiles = 4;   // 16-column value tiles per warp (d_v <= 512)
 constexpr int kMaxKSteps = 16;  // 16-wide k-steps per warp (d <= 2048)
+constexpr int kRedLd = 36;      // row stride of red (32 rows + 4)
+constexpr int kEld = 40;        // row stride of e_buf (32 rows + 8, pairs 8-byte aligned)
+
+// Group of a stage's chunk, written by the producer before it arms the stage's full
+// barrier: the consumers take a new group's description and token indices from here.
+struct StageMeta {
+  int32_t g, q0, mt, n, c0, c1, pad0, pad1;
+  int32_t tok[kMT];  // batch index of each of the group's tokens
+};
 
 struct Misc {
+  StageMeta meta[kMaxStages];
+  uint64_t meta_full[kMaxStages];  // the stage's StageMeta is written (before its copies land)
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
-  float red[kWarps][32][kMT];  // per-warp score partials (up to 32 rows per step)
-  float e_buf[32][kMT];
+  // Token-major, rows padded so that the softmax threads (one row each) read a token's row
+  // partials from distinct banks, and the MMA lanes store theirs without conflicts.
+  float red[kWarps][kMT][kRedLd];  // per-warp score partials (up to 32 rows per step)
+  float e_buf[kMT][kEld];          // the step's weights e = exp(s - m) per token and row
   float m_run[2][kMT];
   float l_run[2][kMT];
   float scale[kMT];
-  int first_group;
-  int last;
+  MergeSmem merge;
   int abort;
 };
 
@@ -169,12 +181,9 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g8 = lane >> 2, t4 = lane & 3;  // mma fragment coordinates
-  const int n_groups = a.hdr[kPlanGroups];
-  const int64_t C = a.hdr[kPlanChunks];
-  const int64_t G = int64_t(gridDim.x) < C ? int64_t(gridDim.x) : C;
   const int b = blockIdx.x;
-  if (b >= G) return;
-  const int64_t cb = int64_t(b) * C / G, ce = int64_t(b + 1) * C / G;
+  const int64_t cb = a.cta_start[b], ce = a.cta_start[b + 1];
+  if (cb >= ce) return;
   const int nk = int(ce - cb);
   const int d = a.d, dv = a.d_v, S = sh.stages;
   const __nv_bfloat16* __restrict__ Xg = static_cast<const __nv_bfloat16*>(a.x);
@@ -185,11 +194,11 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
     tc::tma_prefetch_desc(&mapK);
     tc::tma_prefetch_desc(&mapV);
     for (int s = 0; s < S; ++s) {
+      tc::mbar_init(&ms->meta_full[s], 1);
       tc::mbar_init(&ms->full[s], 1);
       tc::mbar_init(&ms->empty[s], 1);
     }
     ms->abort = 0;
-    ms->first_group = find_group(groups, n_groups, cb);
     tc::fence_barrier_init();
   }
   __syncthreads();
@@ -201,14 +210,15 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
   // group's x rows into L2, several chunks before the consumers load them. The group being
   // fetched is kept in registers.
   if (warp == kWarps) {
-    int pg = ms->first_group;
+    int pg = a.cta_group[b];
     AttendGroup pgr = groups[pg];
     int64_t p_next = groups[pg + 1].c0;
+    int ptok = lane < pgr.mt ? int(uint32_t(a.sorted_keys[pgr.q0 + lane])) : 0;
     const uint32_t tx = uint32_t(CH) * 2u * uint32_t(d + dv);
     auto prefetch_x = [&]() {
       for (int j = 0; j < pgr.mt; ++j) {
         const char* row = reinterpret_cast<const char*>(
-            Xg + int64_t(uint32_t(a.sorted_keys[pgr.q0 + j])) * d);
+            Xg + int64_t(__shfl_sync(0xffffffffu, ptok, j)) * d);
         for (int off = lane * 128; off < 2 * d; off += 32 * 128)
           asm volatile("prefetch.global.L2 [%0];" ::"l"(row + off));
       }
@@ -232,7 +242,21 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
         p_next = groups[pg + 1].c0;
         fresh = true;
       }
+      if (fresh) ptok = lane < pgr.mt ? int(uint32_t(a.sorted_keys[pgr.q0 + lane])) : 0;
+      // the stage's group description (the consumers read it once the stage is full)
+      StageMeta* m = &ms->meta[s];
+      if (lane < kMT) m->tok[lane] = ptok;
       if (lane == 0) {
+        m->g = pg;
+        m->q0 = pgr.q0;
+        m->mt = pgr.mt;
+        m->n = pgr.n;
+        m->c0 = pgr.c0;
+        m->c1 = int32_t(p_next);
+      }
+      __syncwarp();
+      if (lane == 0) {
+        tc::mbar_arrive(&ms->meta_full[s]);
         const int r0 = pgr.row0 + int(c - pgr.c0) * CH;
         const uint32_t st = ring_s + uint32_t(s * sh.stage_bytes);
         tc::mbar_arrive_expect_tx(&ms->full[s], tx);
@@ -258,16 +282,18 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
   constexpr int MS = RS / 16;
   float acc[MT][4];
   uint32_t bx[KS][2];  // Xᵀ fragments of this warp's k-steps
-  int cg = -1, q0 = 0, mt = 0;
+  // current group: index, first sorted position, tokens, rows, chunk range [gc0, c_next)
+  int cg = -1, q0 = 0, mt = 0, gn = 0;
+  int64_t gc0 = 0, c_next = -1;
+  // batch indices of this lane's two token slots (2 t4, 2 t4 + 1) and of token tid
+  int64_t i0 = 0, i1 = 0, itid = 0;
   bool ok = true;
 
   auto finish = [&](int par) {
-    const int64_t c0 = groups[cg].c0, c1 = groups[cg + 1].c0;
+    const int64_t c0 = gc0, c1 = c_next;
     const bool whole = c0 >= cb && c1 <= ce;
     const bool second = c0 > cb;
     const int n0 = 2 * t4, n1 = 2 * t4 + 1;  // this lane's token slots
-    const int64_t i0 = n0 < mt ? int64_t(uint32_t(a.sorted_keys[q0 + n0])) : 0;
-    const int64_t i1 = n1 < mt ? int64_t(uint32_t(a.sorted_keys[q0 + n1])) : 0;
     const float inv0 = n0 < mt ? 1.f / ms->l_run[par][n0] : 0.f;
     const float inv1 = n1 < mt ? 1.f / ms->l_run[par][n1] : 0.f;
 #pragma unroll
@@ -299,9 +325,8 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
     }
     if (whole) {
       if (a.ml && tid < mt) {
-        const int64_t i = int64_t(uint32_t(a.sorted_keys[q0 + tid]));
-        a.ml[2 * i] = ms->m_run[par][tid];
-        a.ml[2 * i + 1] = ms->l_run[par][tid];
+        a.ml[2 * itid] = ms->m_run[par][tid];
+        a.ml[2 * itid + 1] = ms->l_run[par][tid];
       }
       return;
     }
@@ -310,46 +335,58 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
       pe[0] = ms->m_run[par][tid];
       pe[1] = ms->l_run[par][tid];
     }
-    arrive_and_merge(a, cg, c0, c1, C, G, q0, mt, &ms->last, tid, kThreads, [] { cbar(); });
+    arrive_and_merge(a, cg, c0, c1, cb, ce, q0, mt, &ms->merge, tid, kThreads, [] { cbar(); });
   };
 
   // A consumer step takes one chunk, or two consecutive chunks of the same group (stages k
   // and k+1): RS = 2 CH rows, row R of the step is row R % CH of chunk R / CH.
-  int64_t c_next = -1;  // first chunk of the group after the current one
-  AttendGroup gr{};
-  uint32_t u = 0;  // steps done: (m, l) of the current group live in m_run/l_run[u & 1]
+  // Xᵀ fragments of this warp's k-steps for the group of stage meta m, straight from x
+  // (tokens past mt zero): b0 = x[token g8][16 s + 2 t4 .. +1], b1 = x[token g8][16 s + 8 + ..]
+  auto load_x = [&](const StageMeta* m, int m_mt) {
+    const unsigned int* xrow = nullptr;
+    if (g8 < m_mt) xrow = reinterpret_cast<const unsigned int*>(Xg + int64_t(m->tok[g8]) * d);
+#pragma unroll
+    for (int i = 0; i < KS; ++i) {
+      const int s16 = warp + kWarps * i;
+      bx[i][0] = bx[i][1] = 0u;
+      if ((KSW || s16 < nks) && xrow) {
+        bx[i][0] = __ldg(xrow + 8 * s16 + t4);
+        bx[i][1] = __ldg(xrow + 8 * s16 + 4 + t4);
+      }
+    }
+  };
+  bool pre = false;  // bx already holds the fragments of the group that opens at chunk cb + k
+  uint32_t u = 0;    // steps done: (m, l) of the current group live in m_run/l_run[u & 1]
   for (int k = 0; k < nk;) {
     const int64_t c = cb + k;
-    int g = cg;
-    if (cg < 0 || c >= c_next) {
-      g = cg < 0 ? ms->first_group : cg;
-      while (groups[g + 1].c0 <= c) ++g;
-    }
-    if (g != cg) {
+    if (c >= c_next) {  // the chunk opens the next group
       if (cg >= 0) {
         finish(u & 1);
         cbar();
       }
-      cg = g;
-      gr = groups[g];
-      c_next = groups[g + 1].c0;
-      q0 = gr.q0;
-      mt = gr.mt;
-      // each warp's Xᵀ fragments for its k-steps, straight from x (tokens past mt zero):
-      // b0 = x[token g8][16 s + 2 t4 .. +1], b1 = x[token g8][16 s + 8 + 2 t4 .. +1]
-      const unsigned int* xrow = nullptr;
-      if (g8 < mt)
-        xrow = reinterpret_cast<const unsigned int*>(
-            Xg + int64_t(uint32_t(a.sorted_keys[q0 + g8])) * d);
-#pragma unroll
-      for (int i = 0; i < KS; ++i) {
-        const int s16 = warp + kWarps * i;
-        bx[i][0] = bx[i][1] = 0u;
-        if ((KSW || s16 < nks) && xrow) {
-          bx[i][0] = __ldg(xrow + 8 * s16 + t4);
-          bx[i][1] = __ldg(xrow + 8 * s16 + 4 + t4);
-        }
+      // the group's description travels with its first stage in this CTA (published before
+      // the stage's copies are issued, so x is fetched while they are in flight)
+      const bool got =
+          pre || tc::mbar_wait(&ms->meta_full[k % S], (k / S) & 1, abort_flag, a.st, 0x10000);
+      const StageMeta* m = &ms->meta[k % S];
+      if (got) {
+        cg = m->g;
+        q0 = m->q0;
+        mt = m->mt;
+        gn = m->n;
+        gc0 = m->c0;
+        c_next = m->c1;
+      } else {  // stopping: the barrier check below ends the loop
+        mt = 0;
+        gn = 0;
+        gc0 = c;
+        c_next = c + 1;
       }
+      i0 = 2 * t4 < mt ? int64_t(m->tok[2 * t4]) : 0;
+      i1 = 2 * t4 + 1 < mt ? int64_t(m->tok[2 * t4 + 1]) : 0;
+      itid = tid < mt ? int64_t(m->tok[tid]) : 0;
+      if (!pre) load_x(m, mt);
+      pre = false;
 #pragma unroll
       for (int mi = 0; mi < MT; ++mi) acc[mi][0] = acc[mi][1] = acc[mi][2] = acc[mi][3] = 0.f;
       if (tid < kMT) {
@@ -357,10 +394,10 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
         ms->l_run[u & 1][tid] = 0.f;
       }
     }
-    const int j0 = int(c - gr.c0);
-    const int nr0 = gr.n - j0 * CH < CH ? gr.n - j0 * CH : CH;
+    const int j0 = int(c - gc0);
+    const int nr0 = gn - j0 * CH < CH ? gn - j0 * CH : CH;
     const bool pair = k + 1 < nk && c + 1 < c_next;
-    const int nr1 = pair ? (gr.n - (j0 + 1) * CH < CH ? gr.n - (j0 + 1) * CH : CH) : 0;
+    const int nr1 = pair ? (gn - (j0 + 1) * CH < CH ? gn - (j0 + 1) * CH : CH) : 0;
 
     tc::mbar_wait(&ms->full[k % S], (k / S) & 1, abort_flag, a.st, 0x10000);
     if (pair) tc::mbar_wait(&ms->full[(k + 1) % S], ((k + 1) / S) & 1, abort_flag, a.st, 0x10000);
@@ -411,9 +448,20 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
 #pragma unroll
         for (int i = 0; i < 4; ++i)
           r4[i] = (sc[t][0][i] + sc[t][1][i]) + (sc[t][2][i] + sc[t][3][i]);
-        *reinterpret_cast<float2*>(&ms->red[warp][16 * t + g8][2 * t4]) = make_float2(r4[0], r4[1]);
-        *reinterpret_cast<float2*>(&ms->red[warp][16 * t + g8 + 8][2 * t4]) =
-            make_float2(r4[2], r4[3]);
+        ms->red[warp][2 * t4][16 * t + g8] = r4[0];
+        ms->red[warp][2 * t4 + 1][16 * t + g8] = r4[1];
+        ms->red[warp][2 * t4][16 * t + g8 + 8] = r4[2];
+        ms->red[warp][2 * t4 + 1][16 * t + g8 + 8] = r4[3];
+      }
+      // Last step of the group: fetch the next group's x fragments now (bx is free), so the
+      // loads fly during this step's softmax and values. Its stage is already issued when it
+      // lies within S stages of this one (the producer needs no stage released by this step).
+      const int kn = k + (pair ? 2 : 1);
+      if (c + (pair ? 2 : 1) >= c_next && kn < nk && kn - k < S &&
+          tc::mbar_wait(&ms->meta_full[kn % S], (kn / S) & 1, abort_flag, a.st, 0x10000)) {
+        const StageMeta* m = &ms->meta[kn % S];
+        load_x(m, m->mt);
+        pre = true;
       }
     }
     cbar();
@@ -425,7 +473,7 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
       const bool rv = r < CH ? r < nr0 : r - CH < nr1;
       float sv = 0.f;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) sv += ms->red[w][r][j];
+      for (int w = 0; w < kWarps; ++w) sv += ms->red[w][j][r];
       const float mo = ms->m_run[par][j];
       float mx = rv ? sv : -INFINITY;
 #pragma unroll
@@ -435,7 +483,7 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
       float sum = e;
 #pragma unroll
       for (int o = RS / 2; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-      ms->e_buf[r][j] = e;
+      ms->e_buf[j][r] = e;
       if (r == 0) {
         if (j < mt) {
           const float scl = expf(mo - mn);
@@ -455,10 +503,10 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
       uint32_t bh[MS][2], bl[MS][2];
 #pragma unroll
       for (int t = 0; t < MS; ++t) {
-        split_pair(ms->e_buf[16 * t + 2 * t4][g8], ms->e_buf[16 * t + 2 * t4 + 1][g8], bh[t][0],
-                   bl[t][0]);
-        split_pair(ms->e_buf[16 * t + 2 * t4 + 8][g8], ms->e_buf[16 * t + 2 * t4 + 9][g8],
-                   bh[t][1], bl[t][1]);
+        const float2 e0 = *reinterpret_cast<const float2*>(&ms->e_buf[g8][16 * t + 2 * t4]);
+        const float2 e1 = *reinterpret_cast<const float2*>(&ms->e_buf[g8][16 * t + 2 * t4 + 8]);
+        split_pair(e0.x, e0.y, bh[t][0], bl[t][0]);
+        split_pair(e1.x, e1.y, bh[t][1], bl[t][1]);
       }
       // Vᵀ tile (16 value columns x 16 rows) by transposing loads: lanes 0-7 rows 0-7 at
       // column 0, lanes 8-15 rows 0-7 at column 8, lanes 16-31 rows 8-15
@@ -552,9 +600,8 @@ cudaError_t launch_ch(const AttendArgs& a, const MmaShape& sh, cudaStream_t stre
   static cudaError_t attr = cudaFuncSetAttribute(
       attend_mma_kernel<CH, KSW, MTW>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
   if (attr != cudaSuccess) return attr;
-  int grid = sm_count();
-  if (grid > kMaxCtas) grid = kMaxCtas;
-  attend_mma_kernel<CH, KSW, MTW><<<grid, kCtaThreads, sh.smem, stream>>>(mk, mv, a, sh);
+  if (a.n_cta < 1 || a.n_cta > kMaxCtas) return cudaErrorInvalidValue;
+  attend_mma_kernel<CH, KSW, MTW><<<a.n_cta, kCtaThreads, sh.smem, stream>>>(mk, mv, a, sh);
   count_launch();
   return cudaGetLastError();
 }
@@ -562,6 +609,8 @@ cudaError_t launch_ch(const AttendArgs& a, const MmaShape& sh, cudaStream_t stre
 }  // namespace
 
 int attend_mma_rows_per_chunk(int d, int d_v) { return mma_shape(d, d_v).ch; }
+
+int attend_mma_ctas(int, int) { return sm_count() < kMaxCtas ? sm_count() : kMaxCtas; }
 
 cudaError_t launch_attend_mma(const AttendArgs& a, cudaStream_t stream) {
   const MmaShape sh = mma_shape(a.d, a.d_v);

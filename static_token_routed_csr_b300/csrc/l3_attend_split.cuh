@@ -17,7 +17,7 @@ namespace split {
 
 constexpr int kThreads = 256;
 constexpr int kMT = kPlanMT;
-constexpr int kMaxCtas = 256;
+constexpr int kMaxCtas = kPlanMaxCtas;
 constexpr int kSmemLimit = 232448;  // 227 KB of opt-in shared memory per CTA
 
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
@@ -29,9 +29,17 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
-// CTA b of G covers chunks [b C / G, (b+1) C / G); the CTA that holds chunk c:
-__device__ __forceinline__ int cta_of(int64_t c, int64_t C, int64_t G) {
-  return int(((c + 1) * G - 1) / C);
+// The CTA whose (non-empty) chunk range holds chunk c: the largest b with cta_start[b] <= c.
+__device__ __forceinline__ int cta_of(const int32_t* cta_start, int n_cta, int64_t c) {
+  int lo = 0, hi = n_cta - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (cta_start[mid] <= c)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo;
 }
 
 // Largest group g in [0, n_groups) with groups[g].c0 <= c.
@@ -59,46 +67,114 @@ __device__ __forceinline__ float* part_entry(const AttendArgs& a, int64_t b, boo
   return a.part + ((2 * b + (second ? 1 : 0)) * kMT + j) * int64_t(a.d_v + 2);
 }
 
-// After this CTA wrote its partial for group g (chunks [c0, c1)): count it and, in the CTA
-// that completes the group, merge all partials in CTA order and write the group's outputs.
-// Called by the CTA's `nthr` working threads, numbered tid = 0 .. nthr-1; `bar()` is a
-// barrier over exactly those threads; `last` is a shared-memory flag.
+// Shared memory of a merge: the CTAs holding chunks of the group (in CTA order) and, for up
+// to kMergeW of them, each token's weight e^(m_b - M) / L.
+constexpr int kMergeCap = 128;  // holders of a group: at most k_max / ch <= 128 chunks
+constexpr int kMergeW = 16;
+struct MergeSmem {
+  int hold[kMergeCap];
+  float w[kMT][kMergeW];
+  float M[kMT], inv_l[kMT];
+  int nh, first_second, last;
+};
+
+// After this CTA (chunks [cb, ce)) wrote its partial for group g (chunks [c0, c1)): count
+// the group's chunks done and, in the CTA that completes the count, merge all partials in
+// CTA order and write the group's outputs. Called by the CTA's `nthr` working threads,
+// numbered tid = 0 .. nthr-1 (nthr >= 32); `bar()` is a barrier over exactly those threads.
+// Kept out of line: the merge is rare and its registers must not weigh on the caller's loop.
 template <typename Bar>
-__device__ inline void arrive_and_merge(const AttendArgs& a, int g, int64_t c0, int64_t c1,
-                                        int64_t C, int64_t G, int q0, int mt, int* last,
+__device__ __noinline__ void arrive_and_merge(const AttendArgs& a, int g, int64_t c0, int64_t c1,
+                                        int64_t cb, int64_t ce, int q0, int mt, MergeSmem* sm,
                                         int tid, int nthr, Bar bar) {
+  const int32_t* cs = a.cta_start;
   __threadfence();
   bar();
-  const int b0 = cta_of(c0, C, G), b1 = cta_of(c1 - 1, C, G);
-  if (tid == 0) *last = atomicAdd(&a.counters[g], 1) == b1 - b0;
+  if (tid == 0) {
+    const int mine = int((c1 < ce ? c1 : ce) - (c0 > cb ? c0 : cb));
+    sm->last = atomicAdd(&a.counters[g], mine) + mine == int(c1 - c0) ? 1 : 0;
+  }
   bar();
-  if (!*last) return;
+  if (!sm->last) return;
   __threadfence();
-  const int64_t cs0 = int64_t(b0) * C / G;  // first chunk of CTA b0
-  const bool first_second = c0 > cs0;       // the group is CTA b0's second slot
-  for (int j = 0; j < mt; ++j) {
-    float M = -INFINITY;
-    for (int bb = b0; bb <= b1; ++bb)
-      M = fmaxf(M, __ldcg(part_entry(a, bb, bb == b0 && first_second, j)));
-    float L = 0.f;
-    for (int bb = b0; bb <= b1; ++bb) {
-      const float* pp = part_entry(a, bb, bb == b0 && first_second, j);
-      L = fmaf(__ldcg(pp + 1), expf(__ldcg(pp) - M), L);
-    }
-    const int64_t i = int64_t(uint32_t(a.sorted_keys[q0 + j]));
-    const float inv = 1.f / L;
-    for (int col = tid; col < a.d_v; col += nthr) {
-      float s = 0.f;
-      for (int bb = b0; bb <= b1; ++bb) {
-        const float* pp = part_entry(a, bb, bb == b0 && first_second, j);
-        s = fmaf(__ldcg(pp + 2 + col), expf(__ldcg(pp) - M), s);
+  // Holders: the CTAs whose non-empty range meets [c0, c1), contiguous around this one.
+  // Warp 0 looks at the 32 CTAs on each side at once; a longer run is walked one by one.
+  if (tid < 32) {
+    const int b = int(blockIdx.x), n = a.n_cta;
+    auto holds = [&](int bb) {
+      return bb >= 0 && bb < n && cs[bb] < cs[bb + 1] && cs[bb] < c1 && cs[bb + 1] > c0;
+    };
+    const unsigned lo = __ballot_sync(0xffffffffu, holds(b - 32 + tid));  // b-32 .. b-1
+    const unsigned hi = __ballot_sync(0xffffffffu, holds(b + 1 + tid));   // b+1 .. b+32
+    if (tid == 0) {
+      int b0 = b, b1 = b;
+      // holders are contiguous among the non-empty ranges; empty ranges may sit between
+      if (c0 < cb) {
+        b0 = -1;
+        for (int k = 31; k >= 0; --k)
+          if (lo >> k & 1u) b0 = b - 32 + k;  // lowest holder in the window
+        // until the holder of chunk c0 is found, step down past the window
+        for (int bb = (b0 < 0 ? b - 33 : b0 - 1); bb >= 0 && (b0 < 0 || cs[b0] > c0); --bb)
+          if (cs[bb] < cs[bb + 1]) b0 = bb;
       }
-      write_a(a, i, col, s * inv);
+      if (c1 > ce) {
+        b1 = -1;
+        for (int k = 0; k < 32; ++k)
+          if (hi >> k & 1u) b1 = b + 1 + k;  // highest holder in the window
+        // until the holder of chunk c1 - 1 is found, step up past the window
+        for (int bb = (b1 < 0 ? b + 33 : b1 + 1); bb < n && (b1 < 0 || cs[b1 + 1] < c1); ++bb)
+          if (cs[bb] < cs[bb + 1]) b1 = bb;
+      }
+      int nh = 0;
+      for (int bb = b0; bb <= b1; ++bb)
+        if (cs[bb] < cs[bb + 1] && nh < kMergeCap) sm->hold[nh++] = bb;
+      sm->nh = nh;
+      sm->first_second = c0 > cs[b0] ? 1 : 0;  // the group is CTA b0's second slot
     }
-    if (a.ml && tid == 0) {
+  }
+  bar();
+  const int nh = sm->nh;
+  const bool fs = sm->first_second != 0;
+  auto entry = [&](int h, int j) { return part_entry(a, sm->hold[h], h == 0 && fs, j); };
+  // token j: running max and denominator over the holders, then the holders' weights
+  if (tid < mt) {
+    const int j = tid;
+    float M = -INFINITY, L = 0.f;
+    for (int h = 0; h < nh; ++h) {
+      const float* pp = entry(h, j);
+      const float m = __ldcg(pp), l = __ldcg(pp + 1);
+      const float Mn = fmaxf(M, m);
+      L = L * expf(M - Mn) + l * expf(m - Mn);
+      M = Mn;
+      if (h < kMergeW) sm->w[j][h] = m;
+    }
+    const float inv = 1.f / L;
+    for (int h = 0; h < nh && h < kMergeW; ++h) sm->w[j][h] = expf(sm->w[j][h] - M) * inv;
+    sm->M[j] = M;
+    sm->inv_l[j] = inv;
+    if (a.ml) {
+      const int64_t i = int64_t(uint32_t(a.sorted_keys[q0 + j]));
       a.ml[2 * i] = M;
       a.ml[2 * i + 1] = L;
     }
+  }
+  bar();
+  // a = sum_h w_h acc_h, two columns per thread and token
+  const int half = a.d_v / 2;
+  for (int idx = tid; idx < mt * half; idx += nthr) {
+    const int j = idx / half, col = 2 * (idx - j * half);
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll 4
+    for (int h = 0; h < nh; ++h) {
+      const float* pp = entry(h, j);
+      const float wt = h < kMergeW ? sm->w[j][h] : expf(__ldcg(pp) - sm->M[j]) * sm->inv_l[j];
+      const float2 v = __ldcg(reinterpret_cast<const float2*>(pp + 2 + col));
+      s0 = fmaf(v.x, wt, s0);
+      s1 = fmaf(v.y, wt, s1);
+    }
+    const int64_t i = int64_t(uint32_t(a.sorted_keys[q0 + j]));
+    write_a(a, i, col, s0);
+    write_a(a, i, col + 1, s1);
   }
 }
 

@@ -31,6 +31,8 @@ struct AttendGroup {
   int32_t row0;  // offs[t]
   int32_t n;     // rows n_t (0 if the offsets were invalid for t: the group is skipped)
   int32_t c0;    // index of the group's first chunk among all chunks
+  int32_t w0;    // cost units of all chunks before c0 (see PlanOut::w_chunk)
+  int32_t pad;
 };
 struct AttendItem {
   int32_t q0;  // first sorted position
@@ -51,6 +53,14 @@ struct PlanOut {
   int ch;      // rows per chunk
   int mt_max;  // tokens per group (<= kPlanMT)
   int th;      // segments with at least th tokens go to the tensor-core kernel
+  // Split of the chunk list over the n_cta CTAs of the split-row kernel, balanced by cost:
+  // a chunk costs w_chunk units and each group start w_group more (the per-group work of
+  // loading x and writing a). CTA b takes chunks [cta_start[b], cta_start[b+1]), which may
+  // be empty; cta_group[b] is the group holding chunk cta_start[b].
+  int32_t* cta_start;  // [n_cta + 1]
+  int32_t* cta_group;  // [n_cta]
+  int n_cta;
+  int w_chunk, w_group;
 };
 size_t route_scratch_bytes(int64_t T);
 cudaError_t launch_route(const int32_t* ids, int64_t T, int64_t vocab, void* scratch,
@@ -74,6 +84,9 @@ struct AttendArgs {
   __nv_bfloat16* a_bf16; // [T, d_v] nullable, batch order
   float* ml;             // [T, 2] nullable: (max score, softmax denominator)
   float* part;           // attend_part_floats(T, d_v) floats: partial (m, l, acc) per slot
+  const int32_t* cta_start;  // the plan's split of the chunk list (PlanOut)
+  const int32_t* cta_group;
+  int n_cta;                 // grid of the split-row kernel
   DevStatus* st;
 };
 // Rows per chunk for a layer shape: 8 or 16 for bf16 layers (warp-MMA kernel), else as
@@ -83,6 +96,10 @@ int attend_mma_rows_per_chunk(int d, int d_v);
 // Tokens per group of the split-row plan for a layer dtype.
 int attend_group_tokens(int dtype);
 size_t attend_part_floats(int d_v);
+// Grid of the split-row kernel (at most kPlanMaxCtas) and the plan's cost weights for it.
+constexpr int kPlanMaxCtas = 512;
+int attend_split_ctas(int d, int d_v, int dtype);
+void attend_split_weights(int d, int d_v, int dtype, int* w_chunk, int* w_group);
 cudaError_t launch_attend_fwd(const AttendArgs& a, cudaStream_t stream);
 
 // ---- gather-attend on tensor cores (l3_attend_tc.cu), the long segments of bf16 batches ----

@@ -76,13 +76,59 @@ __device__ int block_exclusive_scan(int v, int* warp_tot, int* total) {
   return r;
 }
 
+// Exclusive scan of four ints per thread at once (blockDim.x == 1024); *total gets the sums.
+__device__ int4 block_exclusive_scan4(int4 v, int4* warp_tot, int4* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int4 incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int ux = __shfl_up_sync(0xffffffffu, incl.x, o);
+    const int uy = __shfl_up_sync(0xffffffffu, incl.y, o);
+    const int uz = __shfl_up_sync(0xffffffffu, incl.z, o);
+    const int uw = __shfl_up_sync(0xffffffffu, incl.w, o);
+    if (lane >= o) {
+      incl.x += ux;
+      incl.y += uy;
+      incl.z += uz;
+      incl.w += uw;
+    }
+  }
+  if (lane == 31) warp_tot[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    const int4 w = lane < (int)(blockDim.x >> 5) ? warp_tot[lane] : make_int4(0, 0, 0, 0);
+    int4 wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int ux = __shfl_up_sync(0xffffffffu, wi.x, o);
+      const int uy = __shfl_up_sync(0xffffffffu, wi.y, o);
+      const int uz = __shfl_up_sync(0xffffffffu, wi.z, o);
+      const int uw = __shfl_up_sync(0xffffffffu, wi.w, o);
+      if (lane >= o) {
+        wi.x += ux;
+        wi.y += uy;
+        wi.z += uz;
+        wi.w += uw;
+      }
+    }
+    warp_tot[lane] = make_int4(wi.x - w.x, wi.y - w.y, wi.z - w.z, wi.w - w.w);
+    if (lane == 31) *total = wi;
+  }
+  __syncthreads();
+  const int4 b = warp_tot[wid];
+  const int4 r = make_int4(b.x + incl.x - v.x, b.y + incl.y - v.y, b.z + incl.z - v.z,
+                           b.w + incl.w - v.w);
+  __syncthreads();
+  return r;
+}
+
 // Work plan of the gather-attend (see PlanOut), from the finished segment table.
 __device__ void plan_pass(const uint64_t* keys, int64_t T, const int32_t* seg_start, int S,
                           const PlanOut& pl, DevStatus* st, int* warp_tot, int* total) {
-  int gcarry = 0, ccarry = 0, icarry = 0;
+  int gcarry = 0, ccarry = 0, icarry = 0, wcarry = 0;
   for (int base = 0; base < S; base += blockDim.x) {
     const int s = base + threadIdx.x;
-    int ng = 0, nc = 0, ni = 0, q0 = 0, m = 0, t = 0, row0 = 0, n = 0, per = 0;
+    int ng = 0, nc = 0, ni = 0, nw = 0, q0 = 0, m = 0, t = 0, row0 = 0, n = 0, per = 0;
     if (s < S) {
       q0 = seg_start[s];
       m = seg_start[s + 1] - q0;
@@ -99,14 +145,14 @@ __device__ void plan_pass(const uint64_t* keys, int64_t T, const int32_t* seg_st
         ng = (m + pl.mt_max - 1) / pl.mt_max;
         per = n > 0 ? (n + pl.ch - 1) / pl.ch : 0;
         nc = ng * per;
+        nw = per > 0 ? ng : 0;  // groups with chunks
       }
     }
-    const int gex = block_exclusive_scan(ng, warp_tot, total);
-    const int gtot = *total;
-    const int cex = block_exclusive_scan(nc, warp_tot, total);
-    const int ctot = *total;
-    const int iex = block_exclusive_scan(ni, warp_tot, total);
-    const int itot = *total;
+    __shared__ int4 wt4[32], tot4;
+    const int4 ex = block_exclusive_scan4(make_int4(ng, nc, ni, nw), wt4, &tot4);
+    const int4 tot = tot4;
+    const int gex = ex.x, cex = ex.y, iex = ex.z, wex = ex.w;
+    const int gtot = tot.x, ctot = tot.y, itot = tot.z, wtot = tot.w;
     for (int k = 0; k < ng; ++k) {
       AttendGroup g;
       g.q0 = q0 + k * pl.mt_max;
@@ -115,6 +161,8 @@ __device__ void plan_pass(const uint64_t* keys, int64_t T, const int32_t* seg_st
       g.row0 = row0;
       g.n = n;
       g.c0 = ccarry + cex + k * per;
+      g.w0 = g.c0 * pl.w_chunk + (per > 0 ? wcarry + wex + k : 0) * pl.w_group;
+      g.pad = 0;
       pl.groups[gcarry + gex + k] = g;
       pl.counters[gcarry + gex + k] = 0;
     }
@@ -129,16 +177,60 @@ __device__ void plan_pass(const uint64_t* keys, int64_t T, const int32_t* seg_st
     gcarry += gtot;
     ccarry += ctot;
     icarry += itot;
+    wcarry += wtot;
   }
   if (threadIdx.x == 0) {
     AttendGroup end{};
     end.q0 = int32_t(T);
     end.c0 = ccarry;
+    end.w0 = ccarry * pl.w_chunk + wcarry * pl.w_group;
     pl.groups[gcarry] = end;
     pl.hdr[kPlanGroups] = gcarry;
     pl.hdr[kPlanChunks] = ccarry;
     pl.hdr[kPlanItems] = icarry;
     pl.hdr[3] = 0;
+  }
+  if (!pl.cta_start) return;
+  // Cost-balanced split of the chunk list. Chunk c covers the cost units
+  // [UB(c), UB(c + 1)), UB(c) = c w_chunk + (groups with chunks that start before c) w_group,
+  // so the group holding chunk c0 of its first chunk covers [w0, w0 + w_group + n_c w_chunk).
+  // CTA b starts at the first chunk with UB(c) >= tau_b = b U / n_cta (U = UB(C)): chunk 0
+  // if tau_b = 0, else one past the chunk covering unit tau_b - 1. Each group fills in the
+  // CTAs whose unit tau_b - 1 it covers.
+  __syncthreads();
+  const int NG = gcarry;
+  const int64_t C = ccarry;
+  const int64_t n = pl.n_cta;
+  const int64_t U = C * pl.w_chunk + int64_t(wcarry) * pl.w_group;
+  if (U == 0) {
+    for (int b = threadIdx.x; b <= n; b += blockDim.x) {
+      pl.cta_start[b] = 0;
+      if (b < n) pl.cta_group[b] = 0;
+    }
+    return;
+  }
+  // CTAs with tau_b = 0: b U < n
+  const int64_t b_zero = (n + U - 1) / U;  // smallest b with b U >= n
+  for (int64_t b = threadIdx.x; b < b_zero && b <= n; b += blockDim.x) {
+    pl.cta_start[b] = 0;
+    if (b < n) pl.cta_group[b] = 0;
+  }
+  for (int g = threadIdx.x; g < NG; g += blockDim.x) {
+    const int64_t c0 = pl.groups[g].c0, c1 = pl.groups[g + 1].c0;
+    if (c1 <= c0) continue;
+    const int64_t W0 = pl.groups[g].w0;
+    const int64_t W1 = W0 + pl.w_group + (c1 - c0) * pl.w_chunk;
+    // b with W0 <= tau_b - 1 < W1, i.e. W0 + 1 <= floor(b U / n) <= W1
+    const int64_t b_lo = ((W0 + 1) * n + U - 1) / U;
+    const int64_t b_hi = ((W1 + 1) * n + U - 1) / U - 1;
+    for (int64_t b = b_lo; b <= b_hi && b <= n; ++b) {
+      const int64_t u1 = b * U / n - 1;  // the unit tau_b - 1
+      const int64_t r = u1 - W0 - pl.w_group;
+      const int64_t cs = r < 0 ? c0 : c0 + r / pl.w_chunk;  // chunk covering u1
+      pl.cta_start[b] = int32_t(cs + 1);
+      // group holding chunk cs + 1: this one, or (at its end) the search starts at the next
+      if (b < n) pl.cta_group[b] = cs + 1 < c1 ? g : g + 1;
+    }
   }
 }
 
