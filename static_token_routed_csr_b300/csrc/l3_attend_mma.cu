@@ -7,15 +7,19 @@
 // tokens of one id shares every row it reads).
 //
 // Work list: the routing pass's plan (groups of <= 8 tokens, each group's rows in chunks of
-// `ch` = 8 or 16 rows), split evenly over one persistent CTA per SM. A consumer step takes
-// two consecutive chunks of a group (16 or 32 rows) when it can.
+// `ch` = 8 or 16 rows), cut into one contiguous chunk range per persistent CTA (one per SM)
+// so that the ranges cost about the same: the plan weighs each chunk and, on top, each
+// group start, since a group's x loads and output writes take about as long as a chunk.
+// A consumer step takes two consecutive chunks of a group (16 or 32 rows) when it can.
 //
 // Data movement: a chunk's K rows and V rows are each one TMA copy. The tables are viewed
 // as 3-D tensors [column block of 64][row][64 columns] with the 128-byte swizzle, so a copy
 // lands the chunk as ch-row by 128-byte atoms whose 16-byte pieces are XOR-permuted by row:
 // the matrix loads below read them without shared-memory bank conflicts. A producer warp
-// keeps a ring of up to 4 stages in flight: it waits for a stage to be free, then issues
-// its two copies; full/empty mbarriers per stage, all waits bounded.
+// keeps a ring of up to 6 stages in flight: it waits for a stage to be free, writes the
+// stage's group description (token indices included, read from the plan 32 groups at a
+// time), arms a metadata barrier, then issues the two copies; metadata/full/empty
+// mbarriers per stage, all waits bounded. The consumers never walk the plan themselves.
 //
 // Per chunk (8 consumer warps, synchronised by a named barrier the producer is not in):
 //   scores  Sᵀ[rows][tokens] = K_chunk Xᵀ with mma.sync m16n8k16 (bf16 in, fp32 out): the
@@ -210,13 +214,35 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
   // group's x rows into L2, several chunks before the consumers load them. The group being
   // fetched is kept in registers.
   if (warp == kWarps) {
-    int pg = a.cta_group[b];
-    AttendGroup pgr = groups[pg];
-    int64_t p_next = groups[pg + 1].c0;
-    int ptok = lane < pgr.mt ? int(uint32_t(a.sorted_keys[pgr.q0 + lane])) : 0;
+    // The plan's group list is read 32 groups at a time (lane l holds group w0 + l) and the
+    // current group's fields are taken from the window by shuffles.
+    const int n_groups = a.hdr[kPlanGroups];
+    int w0 = a.cta_group[b];
+    AttendGroup wg{};
+    auto load_window = [&]() {
+      if (w0 + lane <= n_groups) wg = groups[w0 + lane];
+    };
+    load_window();
+    int pg = w0, g_q0 = 0, g_mt = 0, g_n = 0, g_row0 = 0, g_c0 = 0, ptok = 0;
+    int64_t p_next = 0;
+    auto take = [&]() {  // fields of group pg; pg and pg + 1 lie in the window
+      const int src = pg - w0;
+      g_q0 = __shfl_sync(0xffffffffu, wg.q0, src);
+      g_mt = __shfl_sync(0xffffffffu, wg.mt, src);
+      g_n = __shfl_sync(0xffffffffu, wg.n, src);
+      g_row0 = __shfl_sync(0xffffffffu, wg.row0, src);
+      g_c0 = __shfl_sync(0xffffffffu, wg.c0, src);
+      p_next = __shfl_sync(0xffffffffu, wg.c0, src + 1);
+#pragma unroll
+      for (int j = 0; j < kMT; ++j) {
+        const int v = __shfl_sync(0xffffffffu, wg.tok[j], src);
+        if (lane == j) ptok = v;
+      }
+    };
+    take();
     const uint32_t tx = uint32_t(CH) * 2u * uint32_t(d + dv);
     auto prefetch_x = [&]() {
-      for (int j = 0; j < pgr.mt; ++j) {
+      for (int j = 0; j < g_mt; ++j) {
         const char* row = reinterpret_cast<const char*>(
             Xg + int64_t(__shfl_sync(0xffffffffu, ptok, j)) * d);
         for (int off = lane * 128; off < 2 * d; off += 32 * 128)
@@ -238,26 +264,28 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
       bool fresh = false;
       while (p_next <= c) {
         ++pg;
-        pgr = groups[pg];
-        p_next = groups[pg + 1].c0;
+        if (pg + 1 - w0 > 31) {
+          w0 = pg;
+          load_window();
+        }
+        take();
         fresh = true;
       }
-      if (fresh) ptok = lane < pgr.mt ? int(uint32_t(a.sorted_keys[pgr.q0 + lane])) : 0;
-      // the stage's group description (the consumers read it once the stage is full)
+      // the stage's group description (the consumers read it once meta_full is armed)
       StageMeta* m = &ms->meta[s];
       if (lane < kMT) m->tok[lane] = ptok;
       if (lane == 0) {
         m->g = pg;
-        m->q0 = pgr.q0;
-        m->mt = pgr.mt;
-        m->n = pgr.n;
-        m->c0 = pgr.c0;
+        m->q0 = g_q0;
+        m->mt = g_mt;
+        m->n = g_n;
+        m->c0 = g_c0;
         m->c1 = int32_t(p_next);
       }
       __syncwarp();
       if (lane == 0) {
         tc::mbar_arrive(&ms->meta_full[s]);
-        const int r0 = pgr.row0 + int(c - pgr.c0) * CH;
+        const int r0 = g_row0 + int(c - g_c0) * CH;
         const uint32_t st = ring_s + uint32_t(s * sh.stage_bytes);
         tc::mbar_arrive_expect_tx(&ms->full[s], tx);
         tma_load_3d(&mapK, &ms->full[s], st, 0, r0, 0);
@@ -355,8 +383,7 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
       }
     }
   };
-  bool pre = false;  // bx already holds the fragments of the group that opens at chunk cb + k
-  uint32_t u = 0;    // steps done: (m, l) of the current group live in m_run/l_run[u & 1]
+  uint32_t u = 0;  // steps done: (m, l) of the current group live in m_run/l_run[u & 1]
   for (int k = 0; k < nk;) {
     const int64_t c = cb + k;
     if (c >= c_next) {  // the chunk opens the next group
@@ -367,7 +394,7 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
       // the group's description travels with its first stage in this CTA (published before
       // the stage's copies are issued, so x is fetched while they are in flight)
       const bool got =
-          pre || tc::mbar_wait(&ms->meta_full[k % S], (k / S) & 1, abort_flag, a.st, 0x10000);
+          tc::mbar_wait(&ms->meta_full[k % S], (k / S) & 1, abort_flag, a.st, 0x10000);
       const StageMeta* m = &ms->meta[k % S];
       if (got) {
         cg = m->g;
@@ -385,8 +412,7 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
       i0 = 2 * t4 < mt ? int64_t(m->tok[2 * t4]) : 0;
       i1 = 2 * t4 + 1 < mt ? int64_t(m->tok[2 * t4 + 1]) : 0;
       itid = tid < mt ? int64_t(m->tok[tid]) : 0;
-      if (!pre) load_x(m, mt);
-      pre = false;
+      load_x(m, mt);
 #pragma unroll
       for (int mi = 0; mi < MT; ++mi) acc[mi][0] = acc[mi][1] = acc[mi][2] = acc[mi][3] = 0.f;
       if (tid < kMT) {
@@ -452,16 +478,6 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
         ms->red[warp][2 * t4 + 1][16 * t + g8] = r4[1];
         ms->red[warp][2 * t4][16 * t + g8 + 8] = r4[2];
         ms->red[warp][2 * t4 + 1][16 * t + g8 + 8] = r4[3];
-      }
-      // Last step of the group: fetch the next group's x fragments now (bx is free), so the
-      // loads fly during this step's softmax and values. Its stage is already issued when it
-      // lies within S stages of this one (the producer needs no stage released by this step).
-      const int kn = k + (pair ? 2 : 1);
-      if (c + (pair ? 2 : 1) >= c_next && kn < nk && kn - k < S &&
-          tc::mbar_wait(&ms->meta_full[kn % S], (kn / S) & 1, abort_flag, a.st, 0x10000)) {
-        const StageMeta* m = &ms->meta[kn % S];
-        load_x(m, m->mt);
-        pre = true;
       }
     }
     cbar();

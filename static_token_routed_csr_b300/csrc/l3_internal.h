@@ -24,7 +24,7 @@ struct RouteOut {
 // tokens go to the tensor-core kernel as items of at most kTcNT tokens.
 constexpr int kPlanMT = 8;
 constexpr int kTcNT = 64;
-struct AttendGroup {
+struct alignas(16) AttendGroup {
   int32_t q0;    // first sorted position of the group's tokens
   int32_t mt;    // tokens in the group (1..mt_max)
   int32_t t;     // token id
@@ -33,6 +33,7 @@ struct AttendGroup {
   int32_t c0;    // index of the group's first chunk among all chunks
   int32_t w0;    // cost units of all chunks before c0 (see PlanOut::w_chunk)
   int32_t pad;
+  int32_t tok[kPlanMT];  // batch index of each token (0 past mt)
 };
 struct AttendItem {
   int32_t q0;  // first sorted position

@@ -163,6 +163,9 @@ __device__ void plan_pass(const uint64_t* keys, int64_t T, const int32_t* seg_st
       g.c0 = ccarry + cex + k * per;
       g.w0 = g.c0 * pl.w_chunk + (per > 0 ? wcarry + wex + k : 0) * pl.w_group;
       g.pad = 0;
+#pragma unroll
+      for (int j = 0; j < kPlanMT; ++j)
+        g.tok[j] = j < g.mt ? int32_t(uint32_t(keys[g.q0 + j])) : 0;
       pl.groups[gcarry + gex + k] = g;
       pl.counters[gcarry + gex + k] = 0;
     }
