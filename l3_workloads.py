@@ -60,6 +60,8 @@ PRESETS = {
     3: Preset(3, "decode-bf16", 128256, 1048576, 2048, 512, 64, 512, 0.7, "bf16", False),
     4: Preset(4, "large-prefill-bf16", 128256, 4194304, 2048, 512, 65536, 512, 0.7, "bf16", False),
     5: Preset(5, "fwd-bwd-bf16", 256, 1024, 64, 64, 128, 16, 1.0, "bf16", True),
+    # parity-only shape whose GEMM tiles and attend chunks all end ragged (d = 5 x 64)
+    6: Preset(6, "ragged-tiles-bf16", 4096, 65536, 320, 128, 1100, 64, 0.7, "bf16", False),
 }
 
 

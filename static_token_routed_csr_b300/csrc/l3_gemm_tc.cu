@@ -196,37 +196,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ncols = p.N - n0 < BN ? p.N - n0 : BN;
       const uint32_t acc0 = lane_base + uint32_t(int(b) * NACC * BN);
       if (p.mode == 0) {
-        float sum = 0.f;
-        for (int c = 0; c < BN / 32; ++c) {
-          if (c * 32 >= ncols) break;
-          float v[32];
-          tc::tmem_ld32(acc0 + c * 32, v);
+        // One pass over the tile row, 64 columns per TMEM load: round to bf16, store, and
+        // fold each 64-column block's (mean, squared deviations) into the row's running
+        // pair by the pairwise rule.
+        float mean = 0.f, m2 = 0.f;
+        int cnt = 0;
+        for (int c = 0; c < BN / 64; ++c) {
+          if (c * 64 >= ncols) break;
+          float v[64];
+          tc::tmem_ld64(acc0 + c * 64, v);
+          float bs = 0.f;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) sum += round_bf16(v[j]);
-        }
-        const float mean_t = sum / float(ncols);
-        float m2 = 0.f;
-        for (int c = 0; c < BN / 32; ++c) {
-          if (c * 32 >= ncols) break;
-          float v[32];
-          tc::tmem_ld32(acc0 + c * 32, v);
-          uint32_t w[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float a = round_bf16(v[2 * j]), bb = round_bf16(v[2 * j + 1]);
-            m2 = fmaf(a - mean_t, a - mean_t, m2);
-            m2 = fmaf(bb - mean_t, bb - mean_t, m2);
-            w[j] = pack_bf16(a, bb);
+          for (int j = 0; j < 64; ++j) {
+            v[j] = round_bf16(v[j]);
+            bs += v[j];
           }
-          if (row_ok) {
-            uint4* dst = reinterpret_cast<uint4*>(p.U + int64_t(m) * p.N + n0 + c * 32);
+          const float bmean = bs * (1.f / 64.f);
+          float bm2 = 0.f;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) dst[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+          for (int j = 0; j < 64; ++j) bm2 = fmaf(v[j] - bmean, v[j] - bmean, bm2);
+          const float delta = bmean - mean;
+          const float wb = 64.f / float(cnt + 64);
+          mean = fmaf(delta, wb, mean);
+          m2 += bm2 + delta * delta * float(cnt) * wb;
+          cnt += 64;
+          if (row_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(p.U + int64_t(m) * p.N + n0 + c * 64);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              dst[j] = make_uint4(pack_bf16(v[8 * j], v[8 * j + 1]), pack_bf16(v[8 * j + 2], v[8 * j + 3]),
+                                  pack_bf16(v[8 * j + 4], v[8 * j + 5]),
+                                  pack_bf16(v[8 * j + 6], v[8 * j + 7]));
           }
         }
         if (row_ok) {
           float* st = p.stats + (int64_t(n_blk) * p.M + m) * 2;
-          st[0] = sum;
+          st[0] = mean * float(cnt);
           st[1] = m2;
         }
       } else {
@@ -299,7 +304,21 @@ __global__ void rowsum_kernel(const __nv_bfloat16* __restrict__ W, int64_t rows,
   const int64_t r = int64_t(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
   if (r >= rows) return;
   float s = 0.f;
-  for (int c = lane; c < ncols; c += 32) s += __bfloat162float(W[r * ld + c]);
+  if ((reinterpret_cast<uintptr_t>(W) & 15) == 0 && ld % 8 == 0 && ncols % 8 == 0) {
+    // 8 columns per 16-byte load, the row's loads all in flight together
+    const uint4* row = reinterpret_cast<const uint4*>(W + r * ld);
+#pragma unroll 4
+    for (int c = lane; c < ncols / 8; c += 32) {
+      const uint4 q = __ldg(row + c);
+      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        s += __bfloat162float(__ushort_as_bfloat16(uint16_t(w[i] & 0xffffu))) +
+             __bfloat162float(__ushort_as_bfloat16(uint16_t(w[i] >> 16)));
+    }
+  } else {
+    for (int c = lane; c < ncols; c += 32) s += __bfloat162float(W[r * ld + c]);
+  }
   s = warp_sum(s);
   if (lane == 0) out[r] = s;
 }

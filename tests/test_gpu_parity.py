@@ -126,6 +126,16 @@ def test_forward_small_all_tokens(cid, T):
     assert l3.l3_get_error(c.ws) == 0
 
 
+def test_forward_ragged_tile_shapes_all_tokens():
+    # d = 320: odd column-tile counts in both GEMMs (spare tiles in the 2 x 2 cluster mode),
+    # 1100 tokens: odd row-tile count, long segments on tensor cores, short ones split
+    c = Case(6)
+    y, _ = c.forward()
+    fw = c.oracle_forward()
+    assert_close(c.p, to_np(y), fw.y, "y")
+    assert l3.l3_get_error(c.ws) == 0
+
+
 def test_forward_bf16_fp32_output():
     c = Case(2, T=512)
     y, _ = c.forward(y_dtype=torch.float32)
