@@ -16,9 +16,13 @@
 // K_t rows arrive by TMA in 128-row boxes, V_t rows in 64-row boxes and x in 64-token
 // boxes (rows past an item's range are read and masked): few large copies per stage, since
 // each TMA instruction costs tens of nanoseconds to issue.
-// One persistent CTA per SM, 6 warps: TMA producer, MMA issuer, 4 softmax/epilogue
-// warps (one TMEM lane each). All waits are bounded; the softmax warps synchronise on an
-// mbarrier (bounded) rather than a named barrier, so no thread can be left waiting.
+// Phase 1 walks the 64-wide K blocks outermost: an x block is copied once into its own
+// small ring and serves all row chunks of the item (released after the last chunk's MMAs),
+// so the K ring holds only K boxes and more bytes are in flight.
+// One persistent CTA per SM, 10 warps: TMA producer, MMA issuer, 8 softmax/epilogue warps
+// (two per TMEM lane quarter, each taking 32 of the item's 64 token columns). All waits
+// are bounded; the softmax warps synchronise on an mbarrier (bounded) rather than a named
+// barrier, so no thread can be left waiting.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -30,17 +34,20 @@ namespace l3 {
 
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kSoftWarps = 8;  // warps 2 .. 9
 constexpr int kNT = 64;            // tokens per item
-constexpr int kStages = 6;
+constexpr int kStages = 8;         // K / V ring (16 KB stages)
+constexpr int kXSlots = 2;         // x boxes (8 KB), one per K block in flight
 constexpr int kKTile = 128 * 128;  // 128 rows x 64 bf16
 constexpr int kXTile = kNT * 128;  // 64 tokens x 64 bf16
-constexpr int kStageBytes = kKTile + kXTile;
+constexpr int kStageBytes = kKTile;
 constexpr int kPBytes = 512 * 128;  // Pᵀ: up to 512 rows x 64 tokens bf16
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSCol = 0;    // Sᵀ chunk rc at columns 64 rc
 constexpr uint32_t kACol = 256;  // Aᵀ chunk dc at columns 256 + 64 dc
-constexpr int kSmemBytes = kStages * kStageBytes + kPBytes + 7 * kNT * 4 + 256 + 1024;
+constexpr int kSmemBytes =
+    kStages * kStageBytes + kXSlots * kXTile + kPBytes + 7 * kNT * 4 + 256 + 1024;
 
 static_assert(kNT == kTcNT, "item size of the plan");
 using Item = AttendItem;
@@ -84,23 +91,24 @@ __device__ __forceinline__ bool wait_own(uint64_t* bar, uint32_t parity, volatil
   return false;
 }
 
-// Barrier of the 128 softmax threads on an mbarrier (count 128), bounded.
+// Barrier of the softmax warps on an mbarrier (one arrival per warp), bounded.
 __device__ __forceinline__ bool group_sync(uint64_t* bar, uint32_t& phase, volatile int* abort,
                                            DevStatus* st) {
-  tc::mbar_arrive(bar);
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) tc::mbar_arrive(bar);
   const bool ok = wait_own(bar, phase, abort, st, 0x4000);
   phase ^= 1;
   return ok;
 }
 
-// Butterfly reduce-scatter over 32 lanes of a 64-vector: afterwards v[0], v[1] hold the
-// reduction for entries 2*lane and 2*lane + 1.
+// Butterfly reduce-scatter over 32 lanes of a 32-vector: afterwards v[0] holds the
+// reduction for entry `lane`.
 template <bool kMax>
-__device__ __forceinline__ void reduce_scatter64(float (&v)[64], int lane) {
+__device__ __forceinline__ void reduce_scatter32(float (&v)[32], int lane) {
 #pragma unroll
   for (int step = 0; step < 5; ++step) {
     const int o = 16 >> step;
-    const int half = 32 >> step;
+    const int half = 16 >> step;
     const bool up = (lane & o) != 0;
 #pragma unroll
     for (int i = 0; i < half; ++i) {
@@ -121,14 +129,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   unsigned char* stages = smem;
-  unsigned char* pbuf = smem + kStages * kStageBytes;
+  unsigned char* xbuf = smem + kStages * kStageBytes;
+  unsigned char* pbuf = xbuf + kXSlots * kXTile;
   float* red = reinterpret_cast<float*>(pbuf + kPBytes);    // [4][64]
   float* fin_m = red + 4 * kNT;                              // [64]
   float* fin_l = fin_m + kNT;                                // [64]
   int32_t* orig = reinterpret_cast<int32_t*>(fin_l + kNT);  // [64]
   uint64_t* full = reinterpret_cast<uint64_t*>(orig + kNT);
   uint64_t* empty = full + kStages;
-  uint64_t* s_full = empty + kStages;
+  uint64_t* xfull = empty + kStages;
+  uint64_t* xempty = xfull + kXSlots;
+  uint64_t* s_full = xempty + kXSlots;
   uint64_t* s_free = s_full + 1;
   uint64_t* a_full = s_free + 1;
   uint64_t* a_free = a_full + 1;
@@ -140,19 +151,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // Stage buffers start zeroed so that rows a partial TMA box leaves untouched are finite.
-  for (int i = threadIdx.x; i < kStages * kStageBytes / 16; i += kThreads)
+  for (int i = threadIdx.x; i < (kStages * kStageBytes + kXSlots * kXTile) / 16; i += kThreads)
     reinterpret_cast<uint4*>(stages)[i] = make_uint4(0, 0, 0, 0);
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       tc::mbar_init(&full[s], 1);
       tc::mbar_init(&empty[s], 1);
     }
+    for (int s = 0; s < kXSlots; ++s) {
+      tc::mbar_init(&xfull[s], 1);
+      tc::mbar_init(&xempty[s], 1);
+    }
     tc::mbar_init(s_full, 1);
-    tc::mbar_init(s_free, 4);
+    tc::mbar_init(s_free, kSoftWarps);
     tc::mbar_init(a_full, 1);
-    tc::mbar_init(a_free, 4);
+    tc::mbar_init(a_free, kSoftWarps);
     tc::mbar_init(drain, 1);
-    tc::mbar_init(grp, 128);
+    tc::mbar_init(grp, kSoftWarps);
     *abort_flag = 0;
     tc::fence_barrier_init();
   }
@@ -172,28 +187,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::tma_prefetch_desc(&mapK);
       tc::tma_prefetch_desc(&mapX);
       tc::tma_prefetch_desc(&mapV);
-      uint32_t it = 0;
+      uint32_t it = 0, xt = 0;
       bool ok = true;
       for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
         const Item item = p.items[i];
         const int r0 = p.offs[item.t];
         const int n = p.offs[item.t + 1] - r0;
-        const int Nt = (item.nt + 15) & ~15;
         const int RC = (n + 127) / 128;
-        for (int rc = 0; ok && rc < RC; ++rc) {
-          for (int kb = 0; kb < KB; ++kb) {
+        for (int kb = 0; ok && kb < KB; ++kb, ++xt) {
+          {
+            const uint32_t xs = xt % kXSlots, xph = (xt / kXSlots) & 1;
+            if (!tc::mbar_wait(&xempty[xs], xph ^ 1, abort_flag, p.st, 0x100)) {
+              ok = false;
+              break;
+            }
+            tc::mbar_arrive_expect_tx(&xfull[xs], uint32_t(kXTile));
+            tc::tma_load_2d(&mapX, &xfull[xs], xbuf + xs * kXTile, kb * 64, item.q0);
+          }
+          for (int rc = 0; rc < RC; ++rc) {
             const uint32_t s = it % kStages, ph = (it / kStages) & 1;
             if (!tc::mbar_wait(&empty[s], ph ^ 1, abort_flag, p.st, 0x100)) {
               ok = false;
               break;
             }
             unsigned char* st = stages + s * kStageBytes;
-            // one 128-row box of K (rows past the item's range are read and masked) and one
-            // 64-token box of x: few, large copies keep the TMA unit's issue rate off the
-            // critical path
-            tc::mbar_arrive_expect_tx(&full[s], uint32_t(kStageBytes));
+            // one 128-row box of K (rows past the item's range are read and masked): few,
+            // large copies keep the TMA unit's issue rate off the critical path
+            tc::mbar_arrive_expect_tx(&full[s], uint32_t(kKTile));
             tc::tma_load_2d(&mapK, &full[s], st, kb * 64, r0 + 128 * rc);
-            tc::tma_load_2d(&mapX, &full[s], st + kKTile, kb * 64, item.q0);
             ++it;
           }
         }
@@ -220,11 +241,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (uint32_t j = first; j < it; ++j)
           tc::mbar_wait(&full[j % kStages], (j / kStages) & 1, &no_abort, p.st, 0x1000,
                         100000000ull);
+        for (uint32_t j = xt > uint32_t(kXSlots) ? xt - kXSlots : 0; j < xt; ++j)
+          tc::mbar_wait(&xfull[j % kXSlots], (j / kXSlots) & 1, &no_abort, p.st, 0x1000,
+                        100000000ull);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      uint32_t it = 0, item_no = 0;
+      uint32_t it = 0, xt = 0, item_no = 0;
       bool ok = true;
       for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x, ++item_no) {
         const Item item = p.items[i];
@@ -235,8 +259,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t id1 = idesc_bf16(128, Nt, 0, 0);
         const uint32_t id2 = idesc_bf16(128, Nt, 1, 1);
         // phase 1: Sᵀ = K_t Xᵀ
-        for (int rc = 0; ok && rc < RC; ++rc) {
-          for (int kb = 0; kb < KB; ++kb) {
+        for (int kb = 0; ok && kb < KB; ++kb, ++xt) {
+          const uint32_t xs = xt % kXSlots;
+          if (!tc::mbar_wait(&xfull[xs], (xt / kXSlots) & 1, abort_flag, p.st, 0x200)) {
+            ok = false;
+            break;
+          }
+          const uint32_t b_addr = tc::smem_u32(xbuf + xs * kXTile);
+          for (int rc = 0; rc < RC; ++rc) {
             const uint32_t s = it % kStages, ph = (it / kStages) & 1;
             if (!tc::mbar_wait(&full[s], ph, abort_flag, p.st, 0x200)) {
               ok = false;
@@ -244,7 +274,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc::tc_fence_after();
             const uint32_t a_addr = tc::smem_u32(stages + s * kStageBytes);
-            const uint32_t b_addr = a_addr + kKTile;
 #pragma unroll
             for (int k = 0; k < 4; ++k)
               tc::mma_bf16(tmem + kSCol + 64 * rc, tc::desc_kmajor_sw128(a_addr + 32 * k),
@@ -253,6 +282,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mma_commit(&empty[s]);
             ++it;
           }
+          if (!ok) break;
+          tc::mma_commit(&xempty[xs]);  // after every chunk's MMAs have read the x box
         }
         if (!ok) break;
         tc::mma_commit(s_full);
@@ -289,9 +320,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_wait(drain, 0, &no_abort, p.st, 0x2000, 100000000ull);
     }
   } else {
+    // softmax / epilogue warp (q, h): TMEM lane quarter q (hardware rule: warp % 4), token
+    // columns [32 h, 32 h + 32) of the item
     const int q = warp & 3;
+    const int h = (warp - 2) >> 2;
     const int L = q * 32 + lane;  // TMEM lane: table row in a chunk / value column in a chunk
     const uint32_t lane_base = tmem + (uint32_t(q * 32) << 16);
+    const int j0 = 32 * h;        // first token column of this warp
     uint32_t item_no = 0, gph = 0;
     for (int i = blockIdx.x; i < n_items; i += gridDim.x, ++item_no) {
       const Item item = p.items[i];
@@ -299,117 +334,107 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n = p.offs[item.t + 1] - r0;
       const int nt = item.nt;
       const int RC = (n + 127) / 128;
-      const int NC = (nt + 31) / 32;  // 32-column TMEM loads per chunk
+      const bool cols = j0 < nt;  // this warp has tokens of the item
       if (!wait_own(s_full, item_no & 1, abort_flag, p.st, 0x800)) break;
       tc::tc_fence_after();
-      if (L < nt) orig[L] = int32_t(uint32_t(p.sorted_keys[item.q0 + L]));
+      if (h == 0 && L < nt) orig[L] = int32_t(uint32_t(p.sorted_keys[item.q0 + L]));
       // pass 1: per-token max over the rows
-      float v[64];
+      float v[32];
 #pragma unroll
-      for (int j = 0; j < 64; ++j) v[j] = -INFINITY;
-      for (int rc = 0; rc < RC; ++rc) {
-        const bool valid = 128 * rc + L < n;
+      for (int j = 0; j < 32; ++j) v[j] = -INFINITY;
+      if (cols) {
+        for (int rc = 0; rc < RC; ++rc) {
+          float sv[32];
+          tc::tmem_ld32(lane_base + kSCol + 64 * rc + j0, sv);
+          if (128 * rc + L < n)
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          if (c < NC) {
-            float s[32];
-            tc::tmem_ld32(lane_base + kSCol + 64 * rc + 32 * c, s);
-            if (valid)
-#pragma unroll
-              for (int j = 0; j < 32; ++j) v[32 * c + j] = fmaxf(v[32 * c + j], s[j]);
-          }
+            for (int j = 0; j < 32; ++j) v[j] = fmaxf(v[j], sv[j]);
         }
       }
-      reduce_scatter64<true>(v, lane);
-      red[q * kNT + 2 * lane] = v[0];
-      red[q * kNT + 2 * lane + 1] = v[1];
+      reduce_scatter32<true>(v, lane);
+      red[q * kNT + j0 + lane] = v[0];
       if (!group_sync(grp, gph, abort_flag, p.st)) break;
       if (q == 0) {
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int j = 2 * lane + u;
-          fin_m[j] = fmaxf(fmaxf(red[j], red[kNT + j]), fmaxf(red[2 * kNT + j], red[3 * kNT + j]));
-        }
+        const int j = j0 + lane;
+        fin_m[j] = fmaxf(fmaxf(red[j], red[kNT + j]), fmaxf(red[2 * kNT + j], red[3 * kNT + j]));
       }
       if (!group_sync(grp, gph, abort_flag, p.st)) break;
       // pass 2: e = exp(s - m) as bf16 into Pᵀ, and its sum
 #pragma unroll
-      for (int j = 0; j < 64; ++j) v[j] = 0.f;
+      for (int j = 0; j < 32; ++j) v[j] = 0.f;
       const int rows_written = ((n + 63) / 64) * 64;
+      float mj[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) mj[j] = fin_m[j0 + j];
       for (int rc = 0; rc < RC; ++rc) {
         const int row = 128 * rc + L;
         const bool valid = row < n;
-        uint32_t packed[32];
+        uint32_t packed[16];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) packed[j] = 0;
+        for (int j = 0; j < 16; ++j) packed[j] = 0;
+        if (cols) {
+          float sv[32];
+          tc::tmem_ld32(lane_base + kSCol + 64 * rc + j0, sv);
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          if (c < NC) {
-            float s[32];
-            tc::tmem_ld32(lane_base + kSCol + 64 * rc + 32 * c, s);
-#pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-              const int t0 = 32 * c + j, t1 = t0 + 1;
-              const float e0 = (valid && t0 < nt) ? expf(s[j] - fin_m[t0]) : 0.f;
-              const float e1 = (valid && t1 < nt) ? expf(s[j + 1] - fin_m[t1]) : 0.f;
-              const __nv_bfloat16 b0 = __float2bfloat16_rn(e0), b1 = __float2bfloat16_rn(e1);
-              v[t0] += __bfloat162float(b0);
-              v[t1] += __bfloat162float(b1);
-              packed[16 * c + j / 2] =
-                  uint32_t(__bfloat16_as_ushort(b0)) | (uint32_t(__bfloat16_as_ushort(b1)) << 16);
-            }
+          for (int j = 0; j < 32; j += 2) {
+            const int t0 = j0 + j, t1 = t0 + 1;
+            const float e0 = (valid && t0 < nt) ? expf(sv[j] - mj[j]) : 0.f;
+            const float e1 = (valid && t1 < nt) ? expf(sv[j + 1] - mj[j + 1]) : 0.f;
+            const __nv_bfloat16 b0 = __float2bfloat16_rn(e0), b1 = __float2bfloat16_rn(e1);
+            v[j] += __bfloat162float(b0);
+            v[j + 1] += __bfloat162float(b1);
+            packed[j / 2] =
+                uint32_t(__bfloat16_as_ushort(b0)) | (uint32_t(__bfloat16_as_ushort(b1)) << 16);
           }
         }
         if (row < rows_written) {
-          // row of Pᵀ: 64 tokens = 8 chunks of 16 B, 128-byte swizzle within 8-row groups
+          // this warp's half of a Pᵀ row: tokens j0 .. j0 + 31 = 16-byte chunks 4 h .. 4 h + 3
+          // of the row's 128 bytes, 128-byte swizzle within 8-row groups
           unsigned char* prow = pbuf + row * 128;
 #pragma unroll
-          for (int c16 = 0; c16 < 8; ++c16)
+          for (int c = 0; c < 4; ++c) {
+            const int c16 = 4 * h + c;
             *reinterpret_cast<uint4*>(prow + ((c16 ^ (row & 7)) << 4)) =
-                make_uint4(packed[4 * c16], packed[4 * c16 + 1], packed[4 * c16 + 2],
-                           packed[4 * c16 + 3]);
+                make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+          }
         }
       }
       tc::fence_proxy_async();
-      reduce_scatter64<false>(v, lane);
-      red[q * kNT + 2 * lane] = v[0];
-      red[q * kNT + 2 * lane + 1] = v[1];
+      reduce_scatter32<false>(v, lane);
+      red[q * kNT + j0 + lane] = v[0];
       if (!group_sync(grp, gph, abort_flag, p.st)) break;
       if (q == 0) {
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int j = 2 * lane + u;
-          fin_l[j] = (red[j] + red[kNT + j]) + (red[2 * kNT + j] + red[3 * kNT + j]);
-        }
+        const int j = j0 + lane;
+        fin_l[j] = (red[j] + red[kNT + j]) + (red[2 * kNT + j] + red[3 * kNT + j]);
       }
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(s_free);
-      if (!group_sync(grp, gph, abort_flag, p.st)) break;  // fin_l visible to all four warps
+      if (!group_sync(grp, gph, abort_flag, p.st)) break;  // fin_l visible to all warps
       // epilogue: a = Aᵀ / l, batch order
       if (!wait_own(a_full, item_no & 1, abort_flag, p.st, 0x800)) break;
       tc::tc_fence_after();
-      for (int dc = 0; dc < DC; ++dc) {
-        const int col = 128 * dc + L;
+      if (cols) {
+        float inv[32];
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          if (c < NC) {
-            float acc[32];
-            tc::tmem_ld32(lane_base + kACol + 64 * dc + 32 * c, acc);
+        for (int j = 0; j < 32; ++j) inv[j] = 1.f / fin_l[j0 + j];
+        for (int dc = 0; dc < DC; ++dc) {
+          const int col = 128 * dc + L;
+          float acc[32];
+          tc::tmem_ld32(lane_base + kACol + 64 * dc + j0, acc);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int tok = 32 * c + j;
-              if (tok < nt) {
-                const float a = acc[j] / fin_l[tok];
-                const int64_t o = int64_t(orig[tok]) * p.d_v + col;
-                p.a_bf16[o] = __float2bfloat16_rn(a);
-                if (p.a_f32) p.a_f32[o] = a;
-              }
+          for (int j = 0; j < 32; ++j) {
+            const int tok = j0 + j;
+            if (tok < nt) {
+              const float a = acc[j] * inv[j];
+              const int64_t o = int64_t(orig[tok]) * p.d_v + col;
+              p.a_bf16[o] = __float2bfloat16_rn(a);
+              if (p.a_f32) p.a_f32[o] = a;
             }
           }
         }
       }
-      if (p.ml && L < nt) {
+      if (p.ml && h == 0 && L < nt) {
         p.ml[2 * int64_t(orig[L])] = fin_m[L];
         p.ml[2 * int64_t(orig[L]) + 1] = fin_l[L];
       }
