@@ -81,6 +81,17 @@ def workload_bytes(p, ids: np.ndarray, offs: np.ndarray) -> dict:
     }
 
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of a stage's main
+# kernel, from one ncu capture of the current kernel code on that workload (cold cache);
+# an entry is removed when its kernel changes, and the roofline then reports null.
+NCU_TRAFFIC = {
+    ("prefill-bf16", "attend"): 206.075648e6 + 3.959040e6,       # attend_mma_kernel<16,8,2>
+    ("prefill-bf16", "attend_long"): 99.070976e6 + 2.930944e6,   # attend_tc_kernel
+    ("prefill-bf16", "mix"): 38.057472e6 + 0.060928e6,           # tc_gemm_kernel<128,2,6>
+    ("prefill-bf16", "up"): 4.762624e6 + 0.003072e6,             # tc_gemm_kernel<256,1,4>
+}
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -428,6 +439,7 @@ def run_ours(args, rank, world, local_rank):
         roof = {"kernel": "gemm-" + names[dom], "bound": "tensor", "achieved": achieved,
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": achieved / peaks["bf16_tflops"], "traffic": None}
+    roof["traffic"] = NCU_TRAFFIC.get((p.name, names[dom]))
     roof["peak_source"] = peaks["source"]
     attend_s = (stage_ms[names.index("attend")] + stage_ms[names.index("attend_long")]) / 1e3
     line = {
