@@ -71,6 +71,8 @@ struct FwdWs {
   __nv_bfloat16* U16;
   float* stats;
   float* colsum;
+  float* slab;  // split-K parts of the GEMMs (decode-sized batches)
+  size_t slab_floats;
   // tensor-core gather-attend of the long segments
   __nv_bfloat16* x_sorted;
   int tc_th;      // segments with at least this many tokens go to tensor cores (0: none)
@@ -106,6 +108,8 @@ FwdWs carve_fwd(Carve& c, const l3_layer* L, int64_t T) {
     w.U16 = c.take<__nv_bfloat16>(t * d);
     w.stats = c.take<float>(size_t(tc_up_stat_tiles(int(d))) * t * 2);
     w.colsum = c.take<float>(d);
+    w.slab_floats = tc_splitk_floats(T, int(d), int(dv));
+    if (w.slab_floats) w.slab = c.take<float>(w.slab_floats);
   } else {
     w.a_f32 = c.take<float>(t * dv);
     w.U = c.take<float>(t * d);
@@ -277,13 +281,12 @@ l3_status forward_impl(const l3_layer* L, const int32_t* ids, int64_t T, const v
     // Tensor cores: U = bf16(A W_upᵀ) with partial LayerNorm statistics, then
     // y = rstd (U W1ᵀ - mu c) + x W2ᵀ with the statistics merged in the epilogue.
     const auto* Wmix = static_cast<const __nv_bfloat16*>(L->W_mix);
-    L3_CUDA(launch_rowsum(Wmix, d, 2 * d, d, w.colsum, s));
     L3_CUDA(launch_tc_up(w.a_bf16, static_cast<const __nv_bfloat16*>(L->W_up), T, d, dv, w.U16,
-                         w.stats, w.st, s));
+                         w.stats, w.slab, w.slab_floats, Wmix, w.colsum, w.st, s));
     if (ev) L3_CUDA(record_stage(ev[L3_STAGE_MIX], s));
     L3_CUDA(launch_tc_mix(w.U16, static_cast<const __nv_bfloat16*>(x), Wmix, T, d, w.stats,
                           w.colsum, L->ln_eps, y, y_dtype, saved ? sv.mu : nullptr,
-                          saved ? sv.rstd : nullptr, w.st, s));
+                          saved ? sv.rstd : nullptr, w.slab, w.slab_floats, w.st, s));
     if (ev) L3_CUDA(record_stage(ev[L3_FWD_STAGES], s));
     return L3_OK;
   }

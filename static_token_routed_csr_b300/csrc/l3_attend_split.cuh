@@ -73,7 +73,8 @@ constexpr int kMergeCap = 128;  // holders of a group: at most k_max / ch <= 128
 constexpr int kMergeW = 16;
 struct MergeSmem {
   int hold[kMergeCap];
-  float w[kMT][kMergeW];
+  float w[kMT][kMergeW];  // a holder's m, then its weight
+  float l[kMT][kMergeW];
   float M[kMT], inv_l[kMT];
   int nh, first_second, last;
 };
@@ -136,20 +137,28 @@ __device__ __noinline__ void arrive_and_merge(const AttendArgs& a, int g, int64_
   const int nh = sm->nh;
   const bool fs = sm->first_second != 0;
   auto entry = [&](int h, int j) { return part_entry(a, sm->hold[h], h == 0 && fs, j); };
-  // token j: running max and denominator over the holders, then the holders' weights
+  // every holder's (m, l) for every token, loaded at once (the first kMergeW holders)
+  const int nw = nh < kMergeW ? nh : kMergeW;
+  for (int e = tid; e < mt * nw; e += nthr) {
+    const int j = e / nw, h = e - j * nw;
+    const float* pp = entry(h, j);
+    sm->w[j][h] = __ldcg(pp);
+    sm->l[j][h] = __ldcg(pp + 1);
+  }
+  bar();
+  // token j: max and denominator over the holders, then the holders' weights
   if (tid < mt) {
     const int j = tid;
-    float M = -INFINITY, L = 0.f;
+    float M = -INFINITY;
+    for (int h = 0; h < nh; ++h) M = fmaxf(M, h < kMergeW ? sm->w[j][h] : __ldcg(entry(h, j)));
+    float L = 0.f;
     for (int h = 0; h < nh; ++h) {
-      const float* pp = entry(h, j);
-      const float m = __ldcg(pp), l = __ldcg(pp + 1);
-      const float Mn = fmaxf(M, m);
-      L = L * expf(M - Mn) + l * expf(m - Mn);
-      M = Mn;
-      if (h < kMergeW) sm->w[j][h] = m;
+      const float m = h < kMergeW ? sm->w[j][h] : __ldcg(entry(h, j));
+      const float l = h < kMergeW ? sm->l[j][h] : __ldcg(entry(h, j) + 1);
+      L = fmaf(l, expf(m - M), L);
     }
     const float inv = 1.f / L;
-    for (int h = 0; h < nh && h < kMergeW; ++h) sm->w[j][h] = expf(sm->w[j][h] - M) * inv;
+    for (int h = 0; h < nw; ++h) sm->w[j][h] = expf(sm->w[j][h] - M) * inv;
     sm->M[j] = M;
     sm->inv_l[j] = inv;
     if (a.ml) {

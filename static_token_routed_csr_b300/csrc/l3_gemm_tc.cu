@@ -48,8 +48,34 @@ struct TcParams {
   int y_dtype;
   float* mu_out;
   float* rstd_out;
+  // split-K (few output tiles): unit u = tile u % tiles, K part u / tiles of `splits`; the
+  // epilogue then stores raw fp32 accumulators to slab[(split * NACC + acc) * M + row][N]
+  // and a finishing kernel applies the mode's epilogue to their sum
+  int splits;
+  float* slab;
+  // optional side job of the epilogue warps before their first tile (GEMM-up): the row sums
+  // cs_out[r] = sum_{c < cs_cols} cs_W[r, c] of a bf16 matrix (row stride cs_ld)
+  const __nv_bfloat16* cs_W;
+  int cs_rows, cs_ld, cs_cols;
+  float* cs_out;
   DevStatus* st;
 };
+
+// Sum of the bf16 row `row` (ncols columns, a multiple of 8, 16-byte aligned) by one warp.
+__device__ __forceinline__ float warp_row_sum(const __nv_bfloat16* row, int ncols, int lane) {
+  const uint4* r4 = reinterpret_cast<const uint4*>(row);
+  float s = 0.f;
+#pragma unroll 4
+  for (int c = lane; c < ncols / 8; c += 32) {
+    const uint4 q = __ldg(r4 + c);
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      s += __bfloat162float(__ushort_as_bfloat16(uint16_t(w[i] & 0xffffu))) +
+           __bfloat162float(__ushort_as_bfloat16(uint16_t(w[i] >> 16)));
+  }
+  return warp_sum(s);
+}
 
 __device__ __forceinline__ float round_bf16(float v) {
   return __bfloat162float(__float2bfloat16_rn(v));
@@ -61,7 +87,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return lo | (hi << 16);
 }
 
-template <int BN, int NACC, int STAGES>
+template <int BN, int NACC, int STAGES, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA1,
                    const __grid_constant__ CUtensorMap mapA2,
@@ -85,7 +111,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int m_tiles = (p.M + kBM - 1) / kBM;
   const int n_tiles = (p.N + BN - 1) / BN;
   const int tiles = m_tiles * n_tiles;
+  const int splits = SPLIT ? p.splits : 1;
+  const int units = tiles * splits;
   const int kbt = p.kb1 + p.kb2;
+  // unit -> output tile and K range [k_lo, k_hi)
+  auto unit_of = [&](int u, int& m_blk, int& n_blk, int& k_lo, int& k_hi) {
+    const int tile = u % tiles, part = u / tiles;
+    m_blk = tile / n_tiles;
+    n_blk = tile % n_tiles;
+    k_lo = SPLIT ? int(int64_t(part) * kbt / splits) : 0;
+    k_hi = SPLIT ? int(int64_t(part + 1) * kbt / splits) : kbt;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -114,9 +150,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::tma_prefetch_desc(&mapB);
       uint32_t it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < tiles; tile += gridDim.x) {
-        const int m_blk = tile / n_tiles, n_blk = tile % n_tiles;
-        for (int kb = 0; kb < kbt; ++kb) {
+      for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+        int m_blk, n_blk, k_lo, k_hi;
+        unit_of(u, m_blk, n_blk, k_lo, k_hi);
+        for (int kb = k_lo; kb < k_hi; ++kb) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
           if (!tc::mbar_wait(&empty[s], ph ^ 1, abort_flag, p.st, 0x1)) {
             ok = false;
@@ -146,14 +183,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc = tc::idesc_bf16_f32(kBM, BN);
       uint32_t it = 0, lt = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < tiles; tile += gridDim.x, ++lt) {
+      for (int u = blockIdx.x; ok && u < units; u += gridDim.x, ++lt) {
+        int m_blk, n_blk, k_lo, k_hi;
+        unit_of(u, m_blk, n_blk, k_lo, k_hi);
         const uint32_t b = lt & 1, tph = (lt >> 1) & 1;
         if (!tc::mbar_wait(&tempty[b], tph ^ 1, abort_flag, p.st, 0x2)) {
           ok = false;
           break;
         }
         tc::tc_fence_after();
-        for (int kb = 0; kb < kbt; ++kb) {
+        for (int kb = k_lo; kb < k_hi; ++kb) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
           if (!tc::mbar_wait(&full[s], ph, abort_flag, p.st, 0x4)) {
             ok = false;
@@ -161,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc::tc_fence_after();
           const int acc = (NACC == 2 && kb >= p.kb1) ? 1 : 0;
-          const bool first = kb == 0 || (NACC == 2 && kb == p.kb1);
+          const bool first = kb == k_lo || (NACC == 2 && kb == p.kb1);
           const uint32_t d_tmem = tmem + uint32_t((int(b) * NACC + acc) * BN);
           const uint32_t a_addr = tc::smem_u32(smem + s * STAGE_BYTES);
           const uint32_t b_addr = a_addr + A_BYTES;
@@ -184,9 +223,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const uint32_t lane_base = tmem + (uint32_t(q * 32) << 16);
+    if (p.cs_W) {  // while the first accumulator fills
+      for (int64_t r = int64_t(blockIdx.x) * 4 + (warp - 2); r < p.cs_rows;
+           r += int64_t(gridDim.x) * 4) {
+        const float sum = warp_row_sum(p.cs_W + r * p.cs_ld, p.cs_cols, lane);
+        if (lane == 0) p.cs_out[r] = sum;
+      }
+    }
     uint32_t lt = 0;
-    for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++lt) {
-      const int m_blk = tile / n_tiles, n_blk = tile % n_tiles;
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++lt) {
+      int m_blk, n_blk, k_lo, k_hi;
+      unit_of(u, m_blk, n_blk, k_lo, k_hi);
       const uint32_t b = lt & 1, tph = (lt >> 1) & 1;
       if (!tc::mbar_wait(&tfull[b], tph, abort_flag, p.st, 0x8)) break;
       tc::tc_fence_after();
@@ -195,7 +242,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n0 = n_blk * BN;
       const int ncols = p.N - n0 < BN ? p.N - n0 : BN;
       const uint32_t acc0 = lane_base + uint32_t(int(b) * NACC * BN);
-      if (p.mode == 0) {
+      if (SPLIT) {
+        // split-K part: raw accumulators (zeros for an accumulator this K range missed)
+        const int part = u / tiles;
+#pragma unroll
+        for (int acc = 0; acc < NACC; ++acc) {
+          const bool has = NACC == 1 || (acc == 0 ? k_lo < p.kb1 : k_hi > p.kb1);
+          float* dst = p.slab + ((int64_t(part) * NACC + acc) * p.M + m) * p.N + n0;
+          for (int c = 0; c < BN / 32; ++c) {
+            if (c * 32 >= ncols) break;
+            float v[32];
+            if (has) {
+              tc::tmem_ld32(acc0 + uint32_t(acc * BN + c * 32), v);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = 0.f;
+            }
+            if (row_ok) {
+              float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                d4[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            }
+          }
+        }
+      } else if (p.mode == 0) {
         // One pass over the tile row, 64 columns per TMEM load: round to bf16, store, and
         // fold each 64-column block's (mean, squared deviations) into the row's running
         // pair by the pairwise rule.
@@ -297,32 +368,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// sum_k W[n, k] for k < ncols of rows with stride ld (bf16), fp32.
-__global__ void rowsum_kernel(const __nv_bfloat16* __restrict__ W, int64_t rows, int ld,
-                              int ncols, float* out) {
-  const int lane = threadIdx.x & 31;
-  const int64_t r = int64_t(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
-  if (r >= rows) return;
-  float s = 0.f;
-  if ((reinterpret_cast<uintptr_t>(W) & 15) == 0 && ld % 8 == 0 && ncols % 8 == 0) {
-    // 8 columns per 16-byte load, the row's loads all in flight together
-    const uint4* row = reinterpret_cast<const uint4*>(W + r * ld);
-#pragma unroll 4
-    for (int c = lane; c < ncols / 8; c += 32) {
-      const uint4 q = __ldg(row + c);
-      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        s += __bfloat162float(__ushort_as_bfloat16(uint16_t(w[i] & 0xffffu))) +
-             __bfloat162float(__ushort_as_bfloat16(uint16_t(w[i] >> 16)));
-    }
-  } else {
-    for (int c = lane; c < ncols; c += 32) s += __bfloat162float(W[r * ld + c]);
-  }
-  s = warp_sum(s);
-  if (lane == 0) out[r] = s;
-}
-
 // ---- host side ----------------------------------------------------------------------------------
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -363,19 +408,20 @@ int num_sms() {
   return n;
 }
 
-template <int BN, int NACC, int STAGES>
+template <int BN, int NACC, int STAGES, bool SPLIT>
 cudaError_t launch_tc(const CUtensorMap& a1, const CUtensorMap& a2, const CUtensorMap& b,
                       const TcParams& p, cudaStream_t stream) {
   constexpr int kSmem = STAGES * (kBM + BN) * kBK * 2 + 1024 + 256;
-  auto kern = tc_gemm_kernel<BN, NACC, STAGES>;
+  auto kern = tc_gemm_kernel<BN, NACC, STAGES, SPLIT>;
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, [&] {
     attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   });
   if (attr != cudaSuccess) return attr;
-  const int tiles = ((p.M + kBM - 1) / kBM) * ((p.N + BN - 1) / BN);
-  const int grid = tiles < num_sms() ? tiles : num_sms();
+  const int units = ((p.M + kBM - 1) / kBM) * ((p.N + BN - 1) / BN) * (SPLIT ? p.splits : 1);
+  // a side job (row sums) is spread over every SM even when there are fewer tiles
+  const int grid = units < num_sms() && !p.cs_W ? units : num_sms();
   kern<<<grid, kThreads, kSmem, stream>>>(a1, a2, b, p);
   count_launch();
   return cudaGetLastError();
@@ -383,13 +429,133 @@ cudaError_t launch_tc(const CUtensorMap& a1, const CUtensorMap& a2, const CUtens
 
 constexpr int kUpBN = 256, kMixBN = 128;
 
+// K parts of a GEMM with too few output tiles to fill the GPU (a decode batch): enough to
+// give every SM a unit, at most one per 64-wide k-block and 16 in all.
+int splitk_parts(int64_t M, int N, int BN, int kbt) {
+  const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + BN - 1) / BN);
+  if (tiles < 1 || tiles * 2 > num_sms()) return 1;
+  int s = int(num_sms() / tiles);
+  if (s > kbt) s = kbt;
+  if (s > 16) s = 16;
+  return s < 1 ? 1 : s;
+}
+
+// Split-K finish of GEMM-up: U = bf16(sum of the parts), and per 256-column tile the
+// row's (sum, squared deviations from the tile mean) of the rounded values, as the fused
+// epilogue writes them. One warp per (row, tile), 8 columns per lane.
+__global__ void splitk_up_finish_kernel(const float* __restrict__ slab, int parts, int M, int N,
+                                        __nv_bfloat16* __restrict__ U, float* __restrict__ stats) {
+  const int lane = threadIdx.x & 31;
+  const int64_t w = int64_t(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
+  const int n_tiles = (N + kUpBN - 1) / kUpBN;
+  if (w >= int64_t(M) * n_tiles) return;
+  const int m = int(w / n_tiles), tile = int(w % n_tiles);
+  const int n0 = tile * kUpBN, ncols = N - n0 < kUpBN ? N - n0 : kUpBN;
+  const int c0 = n0 + 8 * lane;
+  const bool on = 8 * lane < ncols;
+  float v[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) v[j] = 0.f;
+  if (on)
+    for (int s = 0; s < parts; ++s) {
+      const float4* src = reinterpret_cast<const float4*>(slab + (int64_t(s) * M + m) * N + c0);
+      const float4 a = __ldcg(src), b = __ldcg(src + 1);
+      v[0] += a.x; v[1] += a.y; v[2] += a.z; v[3] += a.w;
+      v[4] += b.x; v[5] += b.y; v[6] += b.z; v[7] += b.w;
+    }
+  float sum = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    v[j] = round_bf16(v[j]);
+    sum += on ? v[j] : 0.f;
+  }
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  const float mean = sum / float(ncols);
+  float m2 = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) m2 += on ? (v[j] - mean) * (v[j] - mean) : 0.f;
+  for (int o = 16; o > 0; o >>= 1) m2 += __shfl_xor_sync(0xffffffffu, m2, o);
+  if (on)
+    *reinterpret_cast<uint4*>(U + int64_t(m) * N + c0) =
+        make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]),
+                   pack_bf16(v[6], v[7]));
+  if (lane == 0) {
+    stats[(int64_t(tile) * M + m) * 2] = sum;
+    stats[(int64_t(tile) * M + m) * 2 + 1] = m2;
+  }
+}
+
+// Split-K finish of GEMM-mix: y = rstd (sum acc0 - mu colsum) + sum acc1 with the row's
+// mu / rstd merged from the up GEMM's partial statistics (the fused epilogue's rule).
+// One warp per (row, 256 columns), 8 columns per lane.
+__global__ void splitk_mix_finish_kernel(const float* __restrict__ slab, int parts, int M, int N,
+                                         const float* __restrict__ stats_in, int stat_tiles,
+                                         int stat_bn, const float* __restrict__ colsum, float eps,
+                                         void* Y, int y_dtype, float* mu_out, float* rstd_out) {
+  const int lane = threadIdx.x & 31;
+  const int64_t w = int64_t(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
+  const int n_chunks = (N + 255) / 256;
+  if (w >= int64_t(M) * n_chunks) return;
+  const int m = int(w / n_chunks), chunk = int(w % n_chunks);
+  float tot = 0.f;
+  for (int j = 0; j < stat_tiles; ++j) tot += stats_in[(int64_t(j) * M + m) * 2];
+  const float mean = tot / float(N);
+  float m2 = 0.f;
+  for (int j = 0; j < stat_tiles; ++j) {
+    const float* st = stats_in + (int64_t(j) * M + m) * 2;
+    const int cnt = N - j * stat_bn < stat_bn ? N - j * stat_bn : stat_bn;
+    const float dm = st[0] / float(cnt) - mean;
+    m2 += st[1] + float(cnt) * dm * dm;
+  }
+  const float rstd = 1.f / sqrtf(m2 / float(N) + eps);
+  if (chunk == 0 && lane == 0 && mu_out) {
+    mu_out[m] = mean;
+    rstd_out[m] = rstd;
+  }
+  const int c0 = chunk * 256 + 8 * lane;
+  if (c0 >= N) return;
+  float v0[8], v1[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) v0[j] = v1[j] = 0.f;
+  for (int s = 0; s < parts; ++s) {
+    const float4* a = reinterpret_cast<const float4*>(slab + ((int64_t(s) * 2) * M + m) * N + c0);
+    const float4* b = reinterpret_cast<const float4*>(slab + ((int64_t(s) * 2 + 1) * M + m) * N + c0);
+    const float4 a0 = __ldcg(a), a1 = __ldcg(a + 1), b0 = __ldcg(b), b1 = __ldcg(b + 1);
+    v0[0] += a0.x; v0[1] += a0.y; v0[2] += a0.z; v0[3] += a0.w;
+    v0[4] += a1.x; v0[5] += a1.y; v0[6] += a1.z; v0[7] += a1.w;
+    v1[0] += b0.x; v1[1] += b0.y; v1[2] += b0.z; v1[3] += b0.w;
+    v1[4] += b1.x; v1[5] += b1.y; v1[6] += b1.z; v1[7] += b1.w;
+  }
+  float y[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) y[j] = fmaf(rstd, v0[j] - mean * __ldg(colsum + c0 + j), v1[j]);
+  if (y_dtype == L3_BF16) {
+    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(Y) + int64_t(m) * N + c0) =
+        make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]),
+                   pack_bf16(y[6], y[7]));
+  } else {
+    float4* d = reinterpret_cast<float4*>(static_cast<float*>(Y) + int64_t(m) * N + c0);
+    d[0] = make_float4(y[0], y[1], y[2], y[3]);
+    d[1] = make_float4(y[4], y[5], y[6], y[7]);
+  }
+}
+
 }  // namespace
+
+size_t tc_splitk_floats(int64_t T, int d, int d_v) {
+  const size_t up = size_t(splitk_parts(T, d, kUpBN, d_v / kBK));
+  const size_t mix = size_t(splitk_parts(T, d, kMixBN, 2 * d / kBK));
+  const size_t a = up > 1 ? up * size_t(T) * size_t(d) : 0;
+  const size_t b = mix > 1 ? 2 * mix * size_t(T) * size_t(d) : 0;
+  return a > b ? a : b;
+}
 
 int tc_up_stat_tiles(int d) { return (d + kUpBN - 1) / kUpBN; }
 
 cudaError_t launch_tc_up(const __nv_bfloat16* A, const __nv_bfloat16* W_up, int64_t T, int d,
-                         int d_v, __nv_bfloat16* U, float* stats, DevStatus* st,
-                         cudaStream_t stream) {
+                         int d_v, __nv_bfloat16* U, float* stats, float* slab,
+                         size_t slab_floats, const __nv_bfloat16* W_mix, float* colsum,
+                         DevStatus* st, cudaStream_t stream) {
   if (T <= 0) return cudaSuccess;
   CUtensorMap ma, mb;
   if (!make_map(&ma, A, T, d_v, kBM) || !make_map(&mb, W_up, d, d_v, kUpBN))
@@ -403,12 +569,25 @@ cudaError_t launch_tc_up(const __nv_bfloat16* A, const __nv_bfloat16* W_up, int6
   p.U = U;
   p.stats = stats;
   p.st = st;
-  return launch_tc<kUpBN, 1, 4>(ma, ma, mb, p, stream);
-}
-
-cudaError_t launch_rowsum(const __nv_bfloat16* W, int64_t rows, int ld, int ncols, float* out,
-                          cudaStream_t stream) {
-  rowsum_kernel<<<unsigned((rows + 7) / 8), 256, 0, stream>>>(W, rows, ld, ncols, out);
+  if (colsum) {
+    // the mix GEMM's column sums of W_mix[:, :d], in the epilogue warps' idle start
+    if ((reinterpret_cast<uintptr_t>(W_mix) & 15) != 0) return cudaErrorInvalidValue;
+    p.cs_W = W_mix;
+    p.cs_rows = d;
+    p.cs_ld = 2 * d;
+    p.cs_cols = d;
+    p.cs_out = colsum;
+  }
+  p.splits = splitk_parts(T, d, kUpBN, p.kb1);
+  if (p.splits > 1 && (!slab || size_t(p.splits) * size_t(T) * size_t(d) > slab_floats))
+    p.splits = 1;  // no room for the parts: one K range per tile
+  if (p.splits == 1) return launch_tc<kUpBN, 1, 4, false>(ma, ma, mb, p, stream);
+  p.slab = slab;
+  const cudaError_t e = launch_tc<kUpBN, 1, 4, true>(ma, ma, mb, p, stream);
+  if (e != cudaSuccess) return e;
+  const int64_t warps = T * ((d + kUpBN - 1) / kUpBN);
+  splitk_up_finish_kernel<<<unsigned((warps + 7) / 8), 256, 0, stream>>>(slab, p.splits, int(T),
+                                                                        d, U, stats);
   count_launch();
   return cudaGetLastError();
 }
@@ -416,7 +595,8 @@ cudaError_t launch_rowsum(const __nv_bfloat16* W, int64_t rows, int ld, int ncol
 cudaError_t launch_tc_mix(const __nv_bfloat16* U, const __nv_bfloat16* x,
                           const __nv_bfloat16* W_mix, int64_t T, int d, const float* stats,
                           const float* colsum, float eps, void* y, int y_dtype, float* mu_out,
-                          float* rstd_out, DevStatus* st, cudaStream_t stream) {
+                          float* rstd_out, float* slab, size_t slab_floats, DevStatus* st,
+                          cudaStream_t stream) {
   if (T <= 0) return cudaSuccess;
   CUtensorMap mu, mx, mw;
   if (!make_map(&mu, U, T, d, kBM) || !make_map(&mx, x, T, d, kBM) ||
@@ -438,7 +618,19 @@ cudaError_t launch_tc_mix(const __nv_bfloat16* U, const __nv_bfloat16* x,
   p.mu_out = mu_out;
   p.rstd_out = rstd_out;
   p.st = st;
-  return launch_tc<kMixBN, 2, 6>(mu, mx, mw, p, stream);
+  p.splits = splitk_parts(T, d, kMixBN, p.kb1 + p.kb2);
+  if (p.splits > 1 && (!slab || 2 * size_t(p.splits) * size_t(T) * size_t(d) > slab_floats))
+    p.splits = 1;
+  if (p.splits == 1) return launch_tc<kMixBN, 2, 6, false>(mu, mx, mw, p, stream);
+  p.slab = slab;
+  const cudaError_t e = launch_tc<kMixBN, 2, 6, true>(mu, mx, mw, p, stream);
+  if (e != cudaSuccess) return e;
+  const int64_t warps = T * ((d + 255) / 256);
+  splitk_mix_finish_kernel<<<unsigned((warps + 7) / 8), 256, 0, stream>>>(
+      slab, p.splits, int(T), d, stats, p.stat_tiles, p.stat_bn, colsum, eps, y, y_dtype,
+      mu_out, rstd_out);
+  count_launch();
+  return cudaGetLastError();
 }
 
 }  // namespace l3

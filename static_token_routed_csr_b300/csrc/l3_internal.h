@@ -156,18 +156,21 @@ cudaError_t launch_cast(const float* src, void* dst, int dst_dtype, int64_t n,
 // ---- tensor-core GEMMs (l3_gemm_tc.cu), bf16 layers ------------------------------------------
 // Partial LayerNorm statistics per row: tc_up_stat_tiles(d) tiles of (sum, M2).
 int tc_up_stat_tiles(int d);
-// U = bf16(A W_upᵀ) [T, d] and the partial statistics stats [tiles][T][2].
+// fp32 scratch of the split-K form both GEMMs take when T gives too few output tiles to
+// fill the GPU (0 when neither splits).
+size_t tc_splitk_floats(int64_t T, int d, int d_v);
+// U = bf16(A W_upᵀ) [T, d] and the partial statistics stats [tiles][T][2]; with colsum
+// non-null, also colsum[n] = sum_{k < d} W_mix[n, k] (W_mix [d, 2d], 16-byte aligned).
 cudaError_t launch_tc_up(const __nv_bfloat16* A, const __nv_bfloat16* W_up, int64_t T, int d,
-                         int d_v, __nv_bfloat16* U, float* stats, DevStatus* st,
-                         cudaStream_t stream);
-// out[r] = sum_{c < ncols} W[r, c] (row stride ld), fp32.
-cudaError_t launch_rowsum(const __nv_bfloat16* W, int64_t rows, int ld, int ncols, float* out,
-                          cudaStream_t stream);
+                         int d_v, __nv_bfloat16* U, float* stats, float* slab,
+                         size_t slab_floats, const __nv_bfloat16* W_mix, float* colsum,
+                         DevStatus* st, cudaStream_t stream);
 // y = rstd (U W_mix[:, :d]ᵀ - mu colsum) + x W_mix[:, d:]ᵀ, mu/rstd merged from stats.
 cudaError_t launch_tc_mix(const __nv_bfloat16* U, const __nv_bfloat16* x,
                           const __nv_bfloat16* W_mix, int64_t T, int d, const float* stats,
                           const float* colsum, float eps, void* y, int y_dtype, float* mu_out,
-                          float* rstd_out, DevStatus* st, cudaStream_t stream);
+                          float* rstd_out, float* slab, size_t slab_floats, DevStatus* st,
+                          cudaStream_t stream);
 
 // ---- backward (l3_backward.cu) -----------------------------------------------------------
 // du = rstd * (dh - mean(dh) - h * mean(dh * h)), per row; dh has row stride ldh.

@@ -334,19 +334,27 @@ struct RadixSmem {
   int warp_tot[32];
 };
 
-// Sorts buf[0][0 .. 8192) by key >> 13 (stable); returns the buffer that holds the result.
-__device__ int block_radix_sort(RadixSmem& sm, int passes) {
+// Sorts buf[0][0 .. 256 nw) by key >> 13 (stable; warps nw .. 31 sit out: keys past the
+// batch are all-ones and stay last, so the first T results never depend on them); returns
+// the buffer that holds the result.
+__device__ int block_radix_sort(RadixSmem& sm, int passes, int nw) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t lt = (1u << lane) - 1u;
+  const bool active = warp < nw;
   int cur = 0;
   for (int p = 0; p < passes; ++p) {
     const int sh = kIdxBits + 8 * p;
-    for (int i = tid; i < 32 * 256; i += 1024) (&sm.cnt[0][0])[i] = 0;
+    for (int i = tid; i < nw * 256; i += 1024) (&sm.cnt[0][0])[i] = 0;
     __syncthreads();
     uint32_t key[8];
     int dig[8], rank[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
+      if (!active) {
+        key[e] = 0;
+        dig[e] = rank[e] = 0;
+        continue;
+      }
       key[e] = sm.buf[cur][warp * 256 + e * 32 + lane];
       dig[e] = int((key[e] >> sh) & 255u);
       const uint32_t peers = __match_any_sync(0xffffffffu, dig[e]);
@@ -360,7 +368,7 @@ __device__ int block_radix_sort(RadixSmem& sm, int passes) {
     int tot = 0, incl = 0;
     if (tid < 256) {
       uint32_t run = 0;
-      for (int w = 0; w < 32; ++w) {
+      for (int w = 0; w < nw; ++w) {
         const uint32_t c = sm.cnt[w][tid];
         sm.cnt[w][tid] = run;
         run += c;
@@ -381,9 +389,10 @@ __device__ int block_radix_sort(RadixSmem& sm, int passes) {
       sm.dstart[tid] = uint32_t(off + incl - tot);
     }
     __syncthreads();
+    if (active)
 #pragma unroll
-    for (int e = 0; e < 8; ++e)
-      sm.buf[cur ^ 1][sm.dstart[dig[e]] + sm.cnt[warp][dig[e]] + rank[e]] = key[e];
+      for (int e = 0; e < 8; ++e)
+        sm.buf[cur ^ 1][sm.dstart[dig[e]] + sm.cnt[warp][dig[e]] + rank[e]] = key[e];
     __syncthreads();
     cur ^= 1;
   }
@@ -393,8 +402,8 @@ __device__ int block_radix_sort(RadixSmem& sm, int passes) {
 // Keys of the block [base, base + 8192) of the batch: (id << 13 | local index); past T all
 // bits set (they sort last). Ids outside [0, vocab) are reported and treated as id 0.
 __device__ void radix_load(RadixSmem& sm, const int32_t* ids, int64_t T, int64_t vocab,
-                           int64_t base, DevStatus* st) {
-  for (int i = threadIdx.x; i < kRadixN; i += blockDim.x) {
+                           int64_t base, DevStatus* st, int n) {
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
     uint32_t key = 0xffffffffu;
     if (base + i < T) {
       int32_t id = ids[base + i];
@@ -423,8 +432,9 @@ __global__ void __launch_bounds__(1024) route_radix_small_kernel(
   uint64_t* k64 = reinterpret_cast<uint64_t*>(dyn + sizeof(RadixSmem));
   __shared__ int warp_tot[32];
   __shared__ int total;
-  radix_load(sm, ids, T, vocab, 0, st);
-  const int cur = block_radix_sort(sm, passes);
+  const int nw = int((T + 255) / 256);  // warps holding keys of the batch
+  radix_load(sm, ids, T, vocab, 0, st, 256 * nw);
+  const int cur = block_radix_sort(sm, passes, nw);
   for (int i = threadIdx.x; i < T; i += blockDim.x) {
     const uint64_t k = wide_key(sm.buf[cur][i], 0);
     k64[i] = k;
@@ -443,8 +453,8 @@ __global__ void __launch_bounds__(1024) route_radix_chunk_kernel(const int32_t* 
   extern __shared__ __align__(16) unsigned char dyn[];
   RadixSmem& sm = *reinterpret_cast<RadixSmem*>(dyn);
   const int64_t base = int64_t(blockIdx.x) * kRadixN;
-  radix_load(sm, ids, T, vocab, base, st);
-  const int cur = block_radix_sort(sm, passes);
+  radix_load(sm, ids, T, vocab, base, st, kRadixN);
+  const int cur = block_radix_sort(sm, passes, 32);
   for (int i = threadIdx.x; i < kRadixN; i += blockDim.x)
     if (base + i < T) keys_out[base + i] = wide_key(sm.buf[cur][i], base);
 }
