@@ -92,6 +92,23 @@ NCU_TRAFFIC = {
 }
 
 
+def max_over_ranks(ms: float, device) -> float:
+    """The largest of the ranks' times (the job is as slow as its slowest rank)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world: int, T: int, steps: int, total_ms: float) -> float:
+    """Whole-job tokens/s: every rank processes its own T-token batch per step (weak scaling)."""
+    return world * T * steps / (total_ms / 1e3)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -374,16 +391,12 @@ def run_ours(args, rank, world, local_rank):
     clocks = clk.stop()
     step_ms = [a.elapsed_time(b) for a, b in step_ev]
     stage_ms = [statistics.mean(smp[s] for smp in stage_samples) for s in range(nst)]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = world * T * args.steps / (total_ms / 1e3)
+    total_ms = max_over_ranks(sum(step_ms), dev)
+    value = job_rate(world, T, args.steps, total_ms)
 
     if args.fwd_only:
         if rank == 0:
-            print(json.dumps({"metric": METRIC, "value": world * T * args.steps / (total_ms / 1e3),
+            print(json.dumps({"metric": METRIC, "value": value,
                               "unit": "tokens/s", "stage_ms": dict(zip(l3.STAGE_NAMES, stage_ms)),
                               "note": "forward only (profiling run)"}), flush=True)
         return 0
@@ -405,11 +418,7 @@ def run_ours(args, rank, world, local_rank):
         l3.l3_forward_host(L, ids_h, x_h, y_h, ws_h)
         e2e_ev[k][1].record()
     barrier()
-    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e_ev), dev)
     if not torch.equal(y_h.to(dev), y):
         raise RuntimeError("host-buffer forward disagrees with the device forward")
     esz = 2 if p.dtype == "bf16" else 4
@@ -459,7 +468,7 @@ def run_ours(args, rank, world, local_rank):
                        "long_gbs": (acct["attend_long_bytes"] / (stage_ms[names.index("attend_long")] / 1e3) / 1e9
                                     if stage_ms[names.index("attend_long")] > 0 else None)},
         "roofline": roof,
-        "e2e": {"value": world * T * args.steps / (e2e_ms / 1e3), "unit": "tokens/s",
+        "e2e": {"value": job_rate(world, T, args.steps, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": T * 4 + T * p.d * esz, "d2h_bytes_per_step": T * p.d * esz},
         "fwd_bwd": fb,
         "gpu_launches": launches,
