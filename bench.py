@@ -534,6 +534,7 @@ def main(argv=None):
     ap.add_argument("--ref-tokens", type=int, default=128,
                     help="tokens per reference-arm step")
     args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)  # at least three untimed steps before timing
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
