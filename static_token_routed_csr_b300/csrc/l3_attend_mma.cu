@@ -186,6 +186,12 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g8 = lane >> 2, t4 = lane & 3;  // mma fragment coordinates
   const int b = blockIdx.x;
+  if (tid == 0) {
+    tc::tma_prefetch_desc(&mapK);
+    tc::tma_prefetch_desc(&mapV);
+  }
+  grid_dep_wait();  // the routing kernel's plan is complete
+  grid_dep_release();
   const int64_t cb = a.cta_start[b], ce = a.cta_start[b + 1];
   if (cb >= ce) return;
   const int nk = int(ce - cb);
@@ -195,8 +201,6 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
   const uint32_t ring_s = tc::smem_u32(ring);
 
   if (tid == 0) {
-    tc::tma_prefetch_desc(&mapK);
-    tc::tma_prefetch_desc(&mapV);
     for (int s = 0; s < S; ++s) {
       tc::mbar_init(&ms->meta_full[s], 1);
       tc::mbar_init(&ms->full[s], 1);
@@ -617,9 +621,10 @@ cudaError_t launch_ch(const AttendArgs& a, const MmaShape& sh, cudaStream_t stre
       attend_mma_kernel<CH, KSW, MTW>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
   if (attr != cudaSuccess) return attr;
   if (a.n_cta < 1 || a.n_cta > kMaxCtas) return cudaErrorInvalidValue;
-  attend_mma_kernel<CH, KSW, MTW><<<a.n_cta, kCtaThreads, sh.smem, stream>>>(mk, mv, a, sh);
+  const cudaError_t e = launch_pdl(attend_mma_kernel<CH, KSW, MTW>, dim3(a.n_cta),
+                                   dim3(kCtaThreads), size_t(sh.smem), stream, mk, mv, a, sh);
   count_launch();
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace

@@ -177,6 +177,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  grid_dep_wait();  // the previous kernels' outputs (plan, gathered x) are complete
+  grid_dep_release();
 
   const int n_items = *p.n_items;
   const int KB = p.d / 64;
@@ -454,20 +456,36 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // x_sorted[q] = x[perm(q)] (bf16 rows of d elements) for the tokens of the items, one CTA
-// per item, one warp per row.
+// per item: the item's batch indices first, then all its rows' 16-byte pieces spread over
+// the threads, eight loads in flight per thread.
 __global__ void gather_rows_kernel(const Item* __restrict__ items, const int32_t* __restrict__ hdr,
                                    const uint64_t* __restrict__ keys,
                                    const __nv_bfloat16* __restrict__ x, int d,
                                    __nv_bfloat16* __restrict__ xs) {
+  grid_dep_wait();
+  grid_dep_release();
   if (int(blockIdx.x) >= hdr[kPlanItems]) return;
+  __shared__ int32_t row_of[kNT];
   const Item it = items[blockIdx.x];
-  const int lane = threadIdx.x & 31;
-  for (int j = threadIdx.x >> 5; j < it.nt; j += blockDim.x >> 5) {
-    const int64_t q = it.q0 + j;
-    const int64_t i = int64_t(uint32_t(keys[q]));
-    const uint4* src = reinterpret_cast<const uint4*>(x + i * d);
-    uint4* dst = reinterpret_cast<uint4*>(xs + q * d);
-    for (int c = lane; c < d / 8; c += 32) dst[c] = __ldg(src + c);
+  if (int(threadIdx.x) < it.nt) row_of[threadIdx.x] = int32_t(uint32_t(keys[it.q0 + threadIdx.x]));
+  __syncthreads();
+  const int pieces = d / 8;  // 16-byte pieces per row
+  const int total = it.nt * pieces;
+  for (int base = threadIdx.x; base < total; base += 8 * blockDim.x) {
+    uint4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int idx = base + u * int(blockDim.x);
+      if (idx < total)
+        v[u] = __ldg(reinterpret_cast<const uint4*>(x + int64_t(row_of[idx / pieces]) * d) +
+                     idx % pieces);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int idx = base + u * int(blockDim.x);
+      if (idx < total)
+        reinterpret_cast<uint4*>(xs + (int64_t(it.q0) + idx / pieces) * d)[idx % pieces] = v[u];
+    }
   }
 }
 
@@ -520,9 +538,11 @@ int attend_tc_threshold(int64_t T, int d, int d_v, int dtype) {
 
 cudaError_t launch_attend_tc(const AttendTcArgs& a, cudaStream_t stream) {
   if (a.T <= 0 || a.max_items <= 0) return cudaSuccess;
-  gather_rows_kernel<<<unsigned(a.max_items), 256, 0, stream>>>(
-      a.items, a.hdr, a.sorted_keys, static_cast<const __nv_bfloat16*>(a.x), a.d, a.x_sorted);
+  cudaError_t e = launch_pdl(gather_rows_kernel, dim3(unsigned(a.max_items)), dim3(256), 0,
+                             stream, a.items, a.hdr, a.sorted_keys,
+                             static_cast<const __nv_bfloat16*>(a.x), a.d, a.x_sorted);
   count_launch();
+  if (e != cudaSuccess) return e;
   const Item* items = a.items;
   CUtensorMap mk, mx, mv;
   if (!make_map(&mk, a.K, a.v, a.d, 128) || !make_map(&mx, a.x_sorted, a.T, a.d, kNT) ||
@@ -546,9 +566,10 @@ cudaError_t launch_attend_tc(const AttendTcArgs& a, cudaStream_t stream) {
                                 kSmemBytes);
   });
   if (attr != cudaSuccess) return attr;
-  attend_tc_kernel<<<sm_count(), kThreads, kSmemBytes, stream>>>(mk, mx, mv, p);
+  e = launch_pdl(attend_tc_kernel, dim3(sm_count()), dim3(kThreads), size_t(kSmemBytes), stream,
+                 mk, mx, mv, p);
   count_launch();
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace l3

@@ -142,6 +142,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  grid_dep_wait();  // the previous kernels' outputs (A or U, the statistics) are complete
+  grid_dep_release();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -422,9 +424,10 @@ cudaError_t launch_tc(const CUtensorMap& a1, const CUtensorMap& a2, const CUtens
   const int units = ((p.M + kBM - 1) / kBM) * ((p.N + BN - 1) / BN) * (SPLIT ? p.splits : 1);
   // a side job (row sums) is spread over every SM even when there are fewer tiles
   const int grid = units < num_sms() && !p.cs_W ? units : num_sms();
-  kern<<<grid, kThreads, kSmem, stream>>>(a1, a2, b, p);
+  const cudaError_t e = launch_pdl(kern, dim3(grid), dim3(kThreads), size_t(kSmem), stream, a1,
+                                   a2, b, p);
   count_launch();
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 constexpr int kUpBN = 256, kMixBN = 128;
@@ -445,6 +448,8 @@ int splitk_parts(int64_t M, int N, int BN, int kbt) {
 // epilogue writes them. One warp per (row, tile), 8 columns per lane.
 __global__ void splitk_up_finish_kernel(const float* __restrict__ slab, int parts, int M, int N,
                                         __nv_bfloat16* __restrict__ U, float* __restrict__ stats) {
+  grid_dep_wait();
+  grid_dep_release();
   const int lane = threadIdx.x & 31;
   const int64_t w = int64_t(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
   const int n_tiles = (N + kUpBN - 1) / kUpBN;
@@ -492,6 +497,8 @@ __global__ void splitk_mix_finish_kernel(const float* __restrict__ slab, int par
                                          const float* __restrict__ stats_in, int stat_tiles,
                                          int stat_bn, const float* __restrict__ colsum, float eps,
                                          void* Y, int y_dtype, float* mu_out, float* rstd_out) {
+  grid_dep_wait();
+  grid_dep_release();
   const int lane = threadIdx.x & 31;
   const int64_t w = int64_t(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
   const int n_chunks = (N + 255) / 256;
@@ -586,10 +593,10 @@ cudaError_t launch_tc_up(const __nv_bfloat16* A, const __nv_bfloat16* W_up, int6
   const cudaError_t e = launch_tc<kUpBN, 1, 4, true>(ma, ma, mb, p, stream);
   if (e != cudaSuccess) return e;
   const int64_t warps = T * ((d + kUpBN - 1) / kUpBN);
-  splitk_up_finish_kernel<<<unsigned((warps + 7) / 8), 256, 0, stream>>>(slab, p.splits, int(T),
-                                                                        d, U, stats);
+  const cudaError_t e2 = launch_pdl(splitk_up_finish_kernel, dim3(unsigned((warps + 7) / 8)),
+                                    dim3(256), 0, stream, slab, p.splits, int(T), d, U, stats);
   count_launch();
-  return cudaGetLastError();
+  return e2 != cudaSuccess ? e2 : cudaGetLastError();
 }
 
 cudaError_t launch_tc_mix(const __nv_bfloat16* U, const __nv_bfloat16* x,
@@ -626,11 +633,12 @@ cudaError_t launch_tc_mix(const __nv_bfloat16* U, const __nv_bfloat16* x,
   const cudaError_t e = launch_tc<kMixBN, 2, 6, true>(mu, mx, mw, p, stream);
   if (e != cudaSuccess) return e;
   const int64_t warps = T * ((d + 255) / 256);
-  splitk_mix_finish_kernel<<<unsigned((warps + 7) / 8), 256, 0, stream>>>(
-      slab, p.splits, int(T), d, stats, p.stat_tiles, p.stat_bn, colsum, eps, y, y_dtype,
-      mu_out, rstd_out);
+  const cudaError_t e2 = launch_pdl(
+      splitk_mix_finish_kernel, dim3(unsigned((warps + 7) / 8)), dim3(256), 0, stream, slab,
+      p.splits, int(T), d, stats, p.stat_tiles, p.stat_bn, colsum, eps, y, y_dtype, mu_out,
+      rstd_out);
   count_launch();
-  return cudaGetLastError();
+  return e2 != cudaSuccess ? e2 : cudaGetLastError();
 }
 
 }  // namespace l3

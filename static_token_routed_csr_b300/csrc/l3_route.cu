@@ -427,6 +427,9 @@ __global__ void __launch_bounds__(1024) route_radix_small_kernel(
     const int32_t* __restrict__ ids, int64_t T, int64_t vocab, int passes, uint64_t* keys_out,
     int32_t* perm, int32_t* seg_start, int32_t* seg_id, int32_t* n_seg, DevStatus* st,
     const PlanOut plan, int with_plan) {
+  // the attend kernel that follows (launched as a programmatic dependent) may set up its CTAs
+  // now; it reads nothing of this kernel's before this grid completes
+  grid_dep_release();
   extern __shared__ __align__(16) unsigned char dyn[];
   RadixSmem& sm = *reinterpret_cast<RadixSmem*>(dyn);
   uint64_t* k64 = reinterpret_cast<uint64_t*>(dyn + sizeof(RadixSmem));
@@ -496,6 +499,7 @@ __global__ void __launch_bounds__(1024) route_segment_kernel(const uint64_t* __r
                                                              int32_t* seg_start, int32_t* seg_id,
                                                              int32_t* n_seg, DevStatus* st,
                                                              const PlanOut plan, int with_plan) {
+  grid_dep_release();  // as in the one-CTA routing kernel
   __shared__ int warp_tot[32];
   __shared__ int total;
   segment_pass(keys, T, perm, seg_start, seg_id, n_seg, with_plan ? &plan : nullptr, st,
