@@ -365,9 +365,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] = 0.f;
       const int rows_written = ((n + 63) / 64) * 64;
+      // e = 2^(s log2(e) - m log2(e)): one multiply-add and one exp2 per weight (the weights
+      // are rounded to bf16 next, far coarser than exp2f's error)
+      constexpr float kLog2e = 1.4426950408889634f;
       float mj[32];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) mj[j] = fin_m[j0 + j];
+      for (int j = 0; j < 32; ++j) mj[j] = -fin_m[j0 + j] * kLog2e;
       for (int rc = 0; rc < RC; ++rc) {
         const int row = 128 * rc + L;
         const bool valid = row < n;
@@ -380,8 +383,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 32; j += 2) {
             const int t0 = j0 + j, t1 = t0 + 1;
-            const float e0 = (valid && t0 < nt) ? expf(sv[j] - mj[j]) : 0.f;
-            const float e1 = (valid && t1 < nt) ? expf(sv[j + 1] - mj[j + 1]) : 0.f;
+            const float e0 = (valid && t0 < nt) ? exp2f(fmaf(sv[j], kLog2e, mj[j])) : 0.f;
+            const float e1 = (valid && t1 < nt) ? exp2f(fmaf(sv[j + 1], kLog2e, mj[j + 1])) : 0.f;
             const __nv_bfloat16 b0 = __float2bfloat16_rn(e0), b1 = __float2bfloat16_rn(e1);
             v[j] += __bfloat162float(b0);
             v[j + 1] += __bfloat162float(b1);
