@@ -85,10 +85,10 @@ def workload_bytes(p, ids: np.ndarray, offs: np.ndarray) -> dict:
 # kernel, from one ncu capture of the current kernel code on that workload (cold cache);
 # an entry is removed when its kernel changes, and the roofline then reports null.
 NCU_TRAFFIC = {
-    ("prefill-bf16", "attend"): 206.075648e6 + 3.959040e6,       # attend_mma_kernel<16,8,2>
-    ("prefill-bf16", "attend_long"): 99.070976e6 + 2.930944e6,   # attend_tc_kernel
-    ("prefill-bf16", "mix"): 38.057472e6 + 0.060928e6,           # tc_gemm_kernel<128,2,6>
-    ("prefill-bf16", "up"): 4.762624e6 + 0.003072e6,             # tc_gemm_kernel<256,1,4>
+    ("prefill-bf16", "attend"): 206.088448e6 + 4.154624e6,       # attend_mma_kernel<16,8,2>
+    ("prefill-bf16", "attend_long"): 99.066880e6 + 3.440640e6,   # attend_tc_kernel
+    ("prefill-bf16", "mix"): 38.060544e6 + 0.069120e6,           # tc_gemm_kernel<128,2,6,0>
+    ("prefill-bf16", "up"): 6.864896e6 + 0.002816e6,             # tc_gemm_kernel<256,1,4,0>
 }
 
 

@@ -458,36 +458,45 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// x_sorted[q] = x[perm(q)] (bf16 rows of d elements) for the tokens of the items, one CTA
-// per item: the item's batch indices first, then all its rows' 16-byte pieces spread over
-// the threads, eight loads in flight per thread.
+// x_sorted[q] = x[perm(q)] (bf16 rows of d elements) for the tokens of the items, in units
+// of a quarter item (up to 16 tokens) per CTA: the batch indices first, then all the rows'
+// 16-byte pieces spread over the threads, eight loads in flight per thread.
+constexpr int kGatherSplit = 4;
 __global__ void gather_rows_kernel(const Item* __restrict__ items, const int32_t* __restrict__ hdr,
                                    const uint64_t* __restrict__ keys,
                                    const __nv_bfloat16* __restrict__ x, int d,
                                    __nv_bfloat16* __restrict__ xs) {
   grid_dep_wait();
   grid_dep_release();
-  if (int(blockIdx.x) >= hdr[kPlanItems]) return;
-  __shared__ int32_t row_of[kNT];
-  const Item it = items[blockIdx.x];
-  if (int(threadIdx.x) < it.nt) row_of[threadIdx.x] = int32_t(uint32_t(keys[it.q0 + threadIdx.x]));
-  __syncthreads();
+  constexpr int kPart = kNT / kGatherSplit;
+  __shared__ int32_t row_of[kPart];
+  const int units = hdr[kPlanItems] * kGatherSplit;
   const int pieces = d / 8;  // 16-byte pieces per row
-  const int total = it.nt * pieces;
-  for (int base = threadIdx.x; base < total; base += 8 * blockDim.x) {
-    uint4 v[8];
+  for (int unit = blockIdx.x; unit < units; unit += gridDim.x) {
+    const Item it0 = items[unit / kGatherSplit];
+    const int j0 = (unit % kGatherSplit) * kPart;  // tokens j0 .. j0 + nt - 1 of the item
+    if (j0 >= it0.nt) continue;
+    const int64_t q0 = int64_t(it0.q0) + j0;
+    const int nt = it0.nt - j0 < kPart ? it0.nt - j0 : kPart;
+    __syncthreads();  // row_of of the previous unit is no longer read
+    if (int(threadIdx.x) < nt) row_of[threadIdx.x] = int32_t(uint32_t(keys[q0 + threadIdx.x]));
+    __syncthreads();
+    const int total = nt * pieces;
+    for (int base = threadIdx.x; base < total; base += 8 * blockDim.x) {
+      uint4 v[8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int idx = base + u * int(blockDim.x);
-      if (idx < total)
-        v[u] = __ldg(reinterpret_cast<const uint4*>(x + int64_t(row_of[idx / pieces]) * d) +
-                     idx % pieces);
-    }
+      for (int u = 0; u < 8; ++u) {
+        const int idx = base + u * int(blockDim.x);
+        if (idx < total)
+          v[u] = __ldg(reinterpret_cast<const uint4*>(x + int64_t(row_of[idx / pieces]) * d) +
+                       idx % pieces);
+      }
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int idx = base + u * int(blockDim.x);
-      if (idx < total)
-        reinterpret_cast<uint4*>(xs + (int64_t(it.q0) + idx / pieces) * d)[idx % pieces] = v[u];
+      for (int u = 0; u < 8; ++u) {
+        const int idx = base + u * int(blockDim.x);
+        if (idx < total)
+          reinterpret_cast<uint4*>(xs + (q0 + idx / pieces) * d)[idx % pieces] = v[u];
+      }
     }
   }
 }
@@ -541,7 +550,12 @@ int attend_tc_threshold(int64_t T, int d, int d_v, int dtype) {
 
 cudaError_t launch_attend_tc(const AttendTcArgs& a, cudaStream_t stream) {
   if (a.T <= 0 || a.max_items <= 0) return cudaSuccess;
-  cudaError_t e = launch_pdl(gather_rows_kernel, dim3(unsigned(a.max_items)), dim3(256), 0,
+  // the item count is on the device: enough CTAs for every unit of a typical batch, each
+  // walking the units by a stride beyond that
+  int64_t g_units = int64_t(a.max_items) * kGatherSplit;
+  const int64_t g_cap = int64_t(sm_count()) * 8;
+  cudaError_t e = launch_pdl(gather_rows_kernel, dim3(unsigned(g_units < g_cap ? g_units : g_cap)),
+                             dim3(256), 0,
                              stream, a.items, a.hdr, a.sorted_keys,
                              static_cast<const __nv_bfloat16*>(a.x), a.d, a.x_sorted);
   count_launch();
