@@ -81,6 +81,9 @@ def workload_bytes(p, ids: np.ndarray, offs: np.ndarray) -> dict:
     }
 
 
+# fp32 FMA throughput of the part: 148 SMs x 128 lanes x 2 FLOP per FMA x 2.032 GHz (TFLOP/s)
+FP32_FMA_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
+
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of a stage's main
 # kernel, from one ncu capture of the current kernel code on that workload (cold cache);
 # an entry is removed when its kernel changes, and the roofline then reports null.
@@ -457,11 +460,17 @@ def run_ours(args, rank, world, local_rank):
     else:
         flops = acct["up_flops"] if names[dom] == "up" else acct["mix_flops"]
         achieved = flops / dom_s / 1e12
-        roof = {"kernel": "gemm-" + names[dom], "bound": "tensor", "achieved": achieved,
-                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": achieved / peaks["bf16_tflops"], "traffic": None}
+        if p.dtype == "bf16":
+            roof = {"kernel": "gemm-" + names[dom], "bound": "tensor", "achieved": achieved,
+                    "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                    "frac": achieved / peaks["bf16_tflops"], "traffic": None}
+        else:  # fp32 layers: CUDA-core GEMMs against the fp32 FMA rate
+            roof = {"kernel": "gemm-" + names[dom] + " (fp32 CUDA cores)", "bound": "alu",
+                    "achieved": achieved, "peak": FP32_FMA_TFLOPS, "unit": "TFLOP/s",
+                    "frac": achieved / FP32_FMA_TFLOPS, "traffic": None}
     roof["traffic"] = NCU_TRAFFIC.get((p.name, names[dom]))
-    roof["peak_source"] = peaks["source"]
+    roof["peak_source"] = peaks["source"] if roof["bound"] != "alu" else (
+        "derived: 148 SMs x 128 fp32 lanes x 2 FLOP x 2.032 GHz")
     attend_s = (stage_ms[names.index("attend")] + stage_ms[names.index("attend_long")]) / 1e3
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
