@@ -87,12 +87,15 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return lo | (hi << 16);
 }
 
+// NACC * BN TMEM columns per accumulator set; two sets (the epilogue of one tile overlaps
+// the next tile's MMAs) when they fit in the 512 columns, else one.
 template <int BN, int NACC, int STAGES, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA1,
                    const __grid_constant__ CUtensorMap mapA2,
                    const __grid_constant__ CUtensorMap mapB, const TcParams p) {
-  static_assert(2 * NACC * BN <= int(kTmemCols), "TMEM budget");
+  static_assert(NACC * BN <= int(kTmemCols), "TMEM budget");
+  constexpr uint32_t NBUF = 2 * NACC * BN <= int(kTmemCols) ? 2 : 1;
   constexpr int A_BYTES = kBM * kBK * 2;
   constexpr int B_BYTES = BN * kBK * 2;
   constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -188,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = blockIdx.x; ok && u < units; u += gridDim.x, ++lt) {
         int m_blk, n_blk, k_lo, k_hi;
         unit_of(u, m_blk, n_blk, k_lo, k_hi);
-        const uint32_t b = lt & 1, tph = (lt >> 1) & 1;
+        const uint32_t b = lt % NBUF, tph = (lt / NBUF) & 1;
         if (!tc::mbar_wait(&tempty[b], tph ^ 1, abort_flag, p.st, 0x2)) {
           ok = false;
           break;
@@ -236,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++lt) {
       int m_blk, n_blk, k_lo, k_hi;
       unit_of(u, m_blk, n_blk, k_lo, k_hi);
-      const uint32_t b = lt & 1, tph = (lt >> 1) & 1;
+      const uint32_t b = lt % NBUF, tph = (lt / NBUF) & 1;
       if (!tc::mbar_wait(&tfull[b], tph, abort_flag, p.st, 0x8)) break;
       tc::tc_fence_after();
       const int m = m_blk * kBM + q * 32 + lane;
@@ -430,7 +433,8 @@ cudaError_t launch_tc(const CUtensorMap& a1, const CUtensorMap& a2, const CUtens
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-constexpr int kUpBN = 256, kMixBN = 128;
+constexpr int kUpBN = 256, kMixBN = 256;
+constexpr int kMixSplitBN = 128;  // GEMM-mix tile width when K is split (decode-sized T)
 
 // K parts of a GEMM with too few output tiles to fill the GPU (a decode batch): enough to
 // give every SM a unit, at most one per 64-wide k-block and 16 in all.
@@ -549,9 +553,18 @@ __global__ void splitk_mix_finish_kernel(const float* __restrict__ slab, int par
 
 }  // namespace
 
+// GEMM-mix splits K when its wide tiles would leave most SMs idle; it then takes narrower
+// tiles (more units) and at least two parts.
+int mix_parts(int64_t T, int d) {
+  const int kbt = 2 * d / kBK;
+  if (splitk_parts(T, d, kMixBN, kbt) == 1) return 1;
+  const int s = splitk_parts(T, d, kMixSplitBN, kbt);
+  return s > 1 ? s : 2;
+}
+
 size_t tc_splitk_floats(int64_t T, int d, int d_v) {
   const size_t up = size_t(splitk_parts(T, d, kUpBN, d_v / kBK));
-  const size_t mix = size_t(splitk_parts(T, d, kMixBN, 2 * d / kBK));
+  const size_t mix = size_t(mix_parts(T, d));
   const size_t a = up > 1 ? up * size_t(T) * size_t(d) : 0;
   const size_t b = mix > 1 ? 2 * mix * size_t(T) * size_t(d) : 0;
   return a > b ? a : b;
@@ -605,9 +618,10 @@ cudaError_t launch_tc_mix(const __nv_bfloat16* U, const __nv_bfloat16* x,
                           float* rstd_out, float* slab, size_t slab_floats, DevStatus* st,
                           cudaStream_t stream) {
   if (T <= 0) return cudaSuccess;
+  const int parts = mix_parts(T, d);
   CUtensorMap mu, mx, mw;
   if (!make_map(&mu, U, T, d, kBM) || !make_map(&mx, x, T, d, kBM) ||
-      !make_map(&mw, W_mix, d, 2 * int64_t(d), kMixBN))
+      !make_map(&mw, W_mix, d, 2 * int64_t(d), parts > 1 ? kMixSplitBN : kMixBN))
     return cudaErrorInvalidValue;
   TcParams p{};
   p.M = int(T);
@@ -625,12 +639,12 @@ cudaError_t launch_tc_mix(const __nv_bfloat16* U, const __nv_bfloat16* x,
   p.mu_out = mu_out;
   p.rstd_out = rstd_out;
   p.st = st;
-  p.splits = splitk_parts(T, d, kMixBN, p.kb1 + p.kb2);
+  p.splits = parts;
   if (p.splits > 1 && (!slab || 2 * size_t(p.splits) * size_t(T) * size_t(d) > slab_floats))
-    p.splits = 1;
-  if (p.splits == 1) return launch_tc<kMixBN, 2, 6, false>(mu, mx, mw, p, stream);
+    return cudaErrorInvalidValue;  // the workspace is sized for the parts
+  if (p.splits == 1) return launch_tc<kMixBN, 2, 4, false>(mu, mx, mw, p, stream);
   p.slab = slab;
-  const cudaError_t e = launch_tc<kMixBN, 2, 6, true>(mu, mx, mw, p, stream);
+  const cudaError_t e = launch_tc<kMixSplitBN, 2, 6, true>(mu, mx, mw, p, stream);
   if (e != cudaSuccess) return e;
   const int64_t warps = T * ((d + 255) / 256);
   const cudaError_t e2 = launch_pdl(
