@@ -88,10 +88,10 @@ FP32_FMA_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
 # kernel, from one ncu capture of the current kernel code on that workload (cold cache);
 # an entry is removed when its kernel changes, and the roofline then reports null.
 NCU_TRAFFIC = {
-    ("prefill-bf16", "attend"): 206.088448e6 + 4.154624e6,       # attend_mma_kernel<16,8,2>
-    ("prefill-bf16", "attend_long"): 99.066880e6 + 3.440640e6,   # attend_tc_kernel
-    ("prefill-bf16", "mix"): 38.060544e6 + 0.069120e6,           # tc_gemm_kernel<128,2,6,0>
-    ("prefill-bf16", "up"): 6.864896e6 + 0.002816e6,             # tc_gemm_kernel<256,1,4,0>
+    ("prefill-bf16", "attend"): 206.086656e6 + 4.008448e6,       # attend_mma_kernel<16,8,2>
+    ("prefill-bf16", "attend_long"): 99.067136e6 + 3.023104e6,   # attend_tc_kernel
+    ("prefill-bf16", "mix"): 38.060800e6 + 0.069888e6,           # tc_gemm_kernel<256,2,4,0>
+    ("prefill-bf16", "up"): 6.864128e6 + 0.003584e6,             # tc_gemm_kernel<256,1,4,0>
 }
 
 
