@@ -9,9 +9,9 @@
 // Work: the routing pass cuts each segment of equal ids (every segment of a small batch;
 // the short segments of a large bf16 batch, whose long ones go to the tensor-core kernel)
 // into groups of at most 8 tokens and each group's n_t rows into chunks of `ch` rows (see
-// PlanOut). The chunks of all groups form one list that is split evenly over one
-// persistent CTA per SM, so a decode batch with a few dozen tokens still streams its rows
-// with every SM.
+// PlanOut). The chunks of all groups form one list that the plan cuts into one contiguous
+// range per persistent CTA (one per SM), of about equal cost, so a decode batch with a few
+// dozen tokens still streams its rows with every SM.
 //
 // Per CTA: thread 0 keeps a ring of up to 4 stages in flight, each filled by two bulk
 // copies (cp.async.bulk) of the chunk's contiguous K rows and V rows. Eight warps compute
@@ -19,8 +19,8 @@
 // an online (single-pass) softmax update: m' = max(m, max s), l' = l e^(m-m') + sum e^(s-m'),
 // acc' = acc e^(m-m') + sum_r e^(s_r-m') V_r, all in fp32. When a group ends inside the
 // CTA's range its tokens are finished there; otherwise the CTA writes its partial
-// (m, l, acc) and the last CTA to finish the group (an atomic counter, no waiting) merges
-// the partials in a fixed order, so results are deterministic.
+// (m, l, acc), and the CTA whose chunks complete the group's count (an atomic counter, no
+// waiting) merges the partials in CTA order, so results are deterministic.
 // Every wait on a copy is bounded: on a timeout the CTA records it, waits (bounded) for the
 // copies it issued and returns.
 #include "l3_attend_split.cuh"

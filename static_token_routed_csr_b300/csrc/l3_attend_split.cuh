@@ -1,7 +1,7 @@
 // Pieces shared by the two split-row gather-attend kernels (CUDA cores for fp32 layers,
-// warp-level tensor cores for bf16 layers): the walk over the plan's chunk list, the bulk
-// copies that fill a stage, and the merge of the partial (m, l, acc) of a group whose
-// chunks several CTAs processed ("L³: Large Lookup Layers", gist.science explainer,
+// warp-level tensor cores for bf16 layers): the bulk copy that fills a stage, the output
+// and partial slots, and the merge of the partial (m, l, acc) of a group whose chunks
+// several CTAs processed ("L³: Large Lookup Layers", gist.science explainer,
 // Technical Summary, "Core Architecture": a = V_tᵀ softmax(K_t x), here assembled from
 // row blocks by the usual rescaling m = max m_b, l = sum_b l_b e^(m_b - m),
 // acc = sum_b acc_b e^(m_b - m), a = acc / l).
@@ -27,32 +27,6 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
           "r"(tc::smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(tc::smem_u32(bar))
       : "memory");
-}
-
-// The CTA whose (non-empty) chunk range holds chunk c: the largest b with cta_start[b] <= c.
-__device__ __forceinline__ int cta_of(const int32_t* cta_start, int n_cta, int64_t c) {
-  int lo = 0, hi = n_cta - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (cta_start[mid] <= c)
-      lo = mid;
-    else
-      hi = mid - 1;
-  }
-  return lo;
-}
-
-// Largest group g in [0, n_groups) with groups[g].c0 <= c.
-__device__ __forceinline__ int find_group(const AttendGroup* groups, int n_groups, int64_t c) {
-  int lo = 0, hi = n_groups - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (groups[mid].c0 <= c)
-      lo = mid;
-    else
-      hi = mid - 1;
-  }
-  return lo;
 }
 
 __device__ __forceinline__ void write_a(const AttendArgs& a, int64_t i, int col, float v) {
