@@ -238,6 +238,18 @@ l3_status l3_get_error(void* ws, l3_stream_t stream);
 /* Static string naming a status. */
 const char* l3_status_string(l3_status status);
 
+/*
+ * Self-test of the bounded waits every kernel uses: enqueues one small kernel whose single
+ * thread waits on a shared-memory barrier that nothing completes, with a limit of
+ * limit_ns nanoseconds (1e3 .. 1e10). The wait gives up, records a timeout in the status
+ * words at the start of `ws`, and the kernel returns; l3_get_error(ws, stream) then
+ * reports L3_ERR_TIMEOUT and the device stays usable. ws_bytes must be at least 256.
+ * Returns L3_ERR_INVALID_ARG (null ws, ws_bytes < 256, limit out of range), L3_ERR_CUDA,
+ * or L3_OK once the kernel is enqueued.
+ */
+l3_status l3_selftest_wait_timeout(void* ws, size_t ws_bytes, int64_t limit_ns,
+                                   l3_stream_t stream);
+
 /* Kernels this library has launched in this process so far (host-side counter). */
 uint64_t l3_launch_count(void);
 

@@ -20,6 +20,7 @@ __all__ = [
     "STAGE_NAMES", "l3_alloc_offsets", "l3_workspace_size", "l3_saved_size",
     "l3_check_layer", "l3_route", "l3_route_noalloc", "l3_forward", "l3_forward_timed", "l3_forward_host",
     "l3_backward", "l3_get_error", "l3_status_string", "l3_launch_count", "l3_abi_version",
+    "l3_selftest_wait_timeout",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libl3.so")
@@ -68,6 +69,7 @@ _SIGNATURES = {
     "l3_status_string": (ctypes.c_char_p, [_I32]),
     "l3_launch_count": (ctypes.c_uint64, []),
     "l3_abi_version": (_I32, []),
+    "l3_selftest_wait_timeout": (_I32, [_P, _SZ, _I64, _P]),
 }
 
 _lib = None
@@ -220,6 +222,13 @@ def l3_status_string(status: int) -> str:
 
 def l3_launch_count() -> int:
     return int(lib().l3_launch_count())
+
+
+def l3_selftest_wait_timeout(ws, limit_ns: int, stream=None) -> None:
+    """Enqueue the bounded-wait self-test on ``ws`` (read the result with l3_get_error)."""
+    _check(lib().l3_selftest_wait_timeout(_ptr(ws), ws.numel() * ws.element_size(),
+                                          int(limit_ns), _stream(stream)),
+           "l3_selftest_wait_timeout")
 
 
 def l3_abi_version() -> int:

@@ -652,6 +652,16 @@ const char* l3_status_string(l3_status st) {
   return "L3_ERR_UNKNOWN";
 }
 
+l3_status l3_selftest_wait_timeout(void* ws, size_t ws_bytes, int64_t limit_ns,
+                                   l3_stream_t stream) {
+  if (!ws || ws_bytes < 256 || limit_ns < 1000 || limit_ns > 10000000000LL)
+    return L3_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  L3_CUDA(cudaMemsetAsync(ws, 0, sizeof(DevStatus), s));
+  L3_CUDA(launch_wait_selftest(static_cast<DevStatus*>(ws), uint64_t(limit_ns), s));
+  return L3_OK;
+}
+
 uint64_t l3_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 int32_t l3_abi_version(void) { return L3_ABI_VERSION; }

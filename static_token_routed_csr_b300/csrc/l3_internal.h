@@ -153,6 +153,10 @@ cudaError_t launch_ln_apply(const float* U, const float* mu, const float* rstd, 
 cudaError_t launch_cast(const float* src, void* dst, int dst_dtype, int64_t n,
                         cudaStream_t stream);
 
+// One thread waits, with the given limit, on an mbarrier phase nothing completes (the
+// timeout path of the kernels' bounded waits); l3_selftest.cu.
+cudaError_t launch_wait_selftest(DevStatus* st, uint64_t limit_ns, cudaStream_t stream);
+
 // ---- tensor-core GEMMs (l3_gemm_tc.cu), bf16 layers ------------------------------------------
 // Partial LayerNorm statistics per row: tc_up_stat_tiles(d) tiles of (sum, M2).
 int tc_up_stat_tiles(int d);

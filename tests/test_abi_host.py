@@ -129,3 +129,11 @@ def test_forward_argument_errors(lib):
 def test_launch_counter_is_monotone(lib):
     a = l3.l3_launch_count()
     assert l3.l3_launch_count() >= a >= 0
+
+
+def test_wait_selftest_argument_errors(lib):
+    # rejected on the host, before any device work
+    assert lib.l3_selftest_wait_timeout(None, 1 << 20, 10_000_000, None) == 1
+    assert lib.l3_selftest_wait_timeout(0x40, 255, 10_000_000, None) == 1
+    assert lib.l3_selftest_wait_timeout(0x40, 1 << 20, 999, None) == 1
+    assert lib.l3_selftest_wait_timeout(0x40, 1 << 20, 10_000_000_001, None) == 1

@@ -315,3 +315,16 @@ def test_single_row_tokens_return_value_row_exactly_bf16():
     a = c2.saved_views(sv)[0].cpu().numpy()
     V = W.table_rows_to_numpy(c2.V, c2.offs_np[ones])
     assert np.array_equal(a, V)
+
+
+def test_bounded_wait_runs_out_and_reports_timeout_without_a_fault():
+    # a wait that nothing completes gives up after its limit (20 ms), records the timeout,
+    # and the device stays usable: a forward afterwards is clean
+    ws = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda")
+    l3.l3_selftest_wait_timeout(ws, 20_000_000)
+    assert l3.l3_status_string(l3.l3_get_error(ws)) == "L3_ERR_TIMEOUT"
+    assert l3.l3_get_error(ws) == 0  # read-and-clear
+    c = Case(5)
+    y, _ = c.forward()
+    assert l3.l3_get_error(c.ws) == 0
+    assert_close(c.p, to_np(y), c.oracle_forward().y, "y after the timeout")
