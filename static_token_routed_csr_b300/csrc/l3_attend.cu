@@ -370,10 +370,10 @@ int attend_split_ctas(int d, int d_v, int dtype) {
 // Cost units of the plan's CTA split, in about 0.2 us of one CTA's time: a chunk, and the
 // extra work of a group (its x rows, its outputs, and an unpaired last chunk). A group
 // weighs relatively more where chunks are short (8 rows at the widest tables); the two
-// settings were measured on the prefill presets.
+// settings were measured on the prefill presets (16-row chunks: 1 .. 5 tried, 3 best).
 void attend_split_weights(int d, int d_v, int dtype, int* w_chunk, int* w_group) {
   *w_chunk = 4;
-  *w_group = attend_rows_per_chunk(d, d_v, dtype) >= 16 ? 5 : 7;
+  *w_group = attend_rows_per_chunk(d, d_v, dtype) >= 16 ? 3 : 7;
 }
 
 int attend_group_tokens(int) { return kPlanMT; }
