@@ -288,7 +288,8 @@ def run_reference(args, rank):
     offs_np = oracle.allocate(wl.freq, p.v, 1, p.k_max, p.power).offs
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     K, V = W.tables(wl, dev)
-    per_step = max(1, args.ref_tokens)
+    # a bounded sample per step: the whole run stays near 4096 oracle tokens (tens of s)
+    per_step = max(1, min(args.ref_tokens, 4096 // max(1, args.steps)))
     for w in range(args.warmup):
         time_oracle(wl, offs_np, K, V, [w % wl.T])
     total, toks = 0.0, 0
