@@ -137,3 +137,23 @@ def test_wait_selftest_argument_errors(lib):
     assert lib.l3_selftest_wait_timeout(0x40, 255, 10_000_000, None) == 1
     assert lib.l3_selftest_wait_timeout(0x40, 1 << 20, 999, None) == 1
     assert lib.l3_selftest_wait_timeout(0x40, 1 << 20, 10_000_000_001, None) == 1
+
+
+def test_stage_names_follow_the_header_enum():
+    src = open(HEADER).read()
+    stages = dict((name.lower(), int(v)) for name, v in
+                  re.findall(r"L3_STAGE_([A-Z_]+)\s*=\s*(\d+)", src))
+    n = int(re.search(r"L3_FWD_STAGES\s*=\s*(\d+)", src).group(1))
+    assert l3.L3_FWD_STAGES == n == len(l3.STAGE_NAMES)
+    assert [stages[s] for s in l3.STAGE_NAMES] == list(range(n))
+
+
+def test_workspace_grows_with_the_batch_and_covers_decode_scratch(lib):
+    # bf16 layer of the decode shape (d 2048, d_v 512): small batches need the split-K
+    # scratch of the GEMMs on top of the rest, larger ones need more of everything
+    L = _fake_layer(d=2048, d_v=512, k_max=512, vocab=1024, v=1024 * 256)
+    sizes = [lib.l3_workspace_size(ctypes.byref(L), T, 0) for T in (1, 64, 512, 8192, 65536)]
+    assert all(s > 0 for s in sizes)
+    assert sizes[-1] > sizes[-2] > sizes[0]
+    # at 64 tokens the split-K parts (fp32, a few per output element) dominate the growth
+    assert sizes[1] - sizes[0] > 64 * 2048 * 4
