@@ -1,13 +1,17 @@
 #!/usr/bin/env python
 """Benchmark of the L³ layer on B300: one JSON line on stdout (rank 0).
 
-Workload (default): the bf16 prefill batch — vocab 32768, v 262144 table rows, d 1024,
-d_v 256, T 8192 tokens (4 x 2048) with Zipf(1.1) ids, rows per id from the Zipf^0.7 rule
-capped at k = 512. A step is one l3_forward over the batch (route, gather-attend,
-GEMM-up + LayerNorm statistics, GEMM-mix), replayed as one CUDA graph captured from
-l3_forward; inputs are resident in HBM and L2 is flushed (a 256 MB write, then a 256 MB read) before every
-timed step, outside its events. `e2e` times the same
-forward through l3_forward_host from pinned host buffers, copies included.
+Workload (default): the large bf16 prefill batch — vocab 128256, v 4194304 table rows
+(a 17 GB key table and a 4 GB value table), d 2048, d_v 512, T 65536 tokens (16 x 4096)
+with Zipf(1.1) ids, rows per id from the Zipf^0.7 rule capped at k = 512. A step is one
+l3_forward over the batch (route, gather-attend, GEMM-up + LayerNorm statistics,
+GEMM-mix), replayed as one CUDA graph captured from l3_forward; inputs are resident in
+HBM and L2 is flushed (a 256 MB write, then a 256 MB read) before every timed step,
+outside its events. `e2e` times the same forward through l3_forward_host from pinned host
+buffers, copies included. Beside the headline the line carries, measured the same way,
+the decode batch (`decode`: vocab 128256, v 1048576, d 2048, d_v 512, T 64) and the
+prefill batch (`prefill`: vocab 32768, v 262144, d 1024, d_v 256, T 8192), and a forward
++ backward rate (`fwd_bwd`).
 
 Multi-GPU (torchrun): every rank runs an independent batch (its own token seed) on its
 own GPU with no collective on the data path; the timed region is bracketed by barriers,
@@ -142,17 +146,18 @@ class L2Flush:
 # ---- clocks --------------------------------------------------------------------------------------
 
 class ClockSampler:
-    """nvidia-smi samples (every 50 ms) kept for the window around the timed region."""
+    """nvidia-smi samples (every 50 ms) for the whole run; ``window(t0, t1)`` summarises
+    the samples taken while a timed region ran."""
 
     FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
         self.path = None
-        self.t0 = self.t1 = None
 
     def start(self):
         fd, self.path = tempfile.mkstemp(prefix="l3clk", suffix=".csv")
@@ -169,25 +174,10 @@ class ClockSampler:
         while time.time() < deadline and os.path.getsize(self.path) == 0:
             time.sleep(0.02)
 
-    def mark_start(self):
-        self.t0 = time.time()
-
-    def mark_end(self):
-        self.t1 = time.time()
-        time.sleep(0.15)
-
-    def stop(self) -> dict:
+    def _rows(self):
         import datetime
 
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
         rows = []
-        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
         with open(self.path) as f:
             for line in f:
                 parts = [s.strip() for s in line.split(",")]
@@ -198,17 +188,32 @@ class ClockSampler:
                     rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
                 except ValueError:
                     continue
-        os.unlink(self.path)
-        lo, hi = (self.t0 or 0) - 0.1, (self.t1 or 1e30) + 0.1
-        win = [r for r in rows if lo <= r[0] <= hi]
+        return rows
+
+    def window(self, t0: float, t1: float) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)  # the sample after the region's end
+        rows = self._rows()
+        win = [r for r in rows if t0 - 0.1 <= r[0] <= t1 + 0.1]
         if not win and rows:  # timed region shorter than the sampling interval: nearest sample
-            mid = 0.5 * ((self.t0 or 0) + (self.t1 or 0))
+            mid = 0.5 * (t0 + t1)
             win = [min(rows, key=lambda r: abs(r[0] - mid))]
-        reasons = sorted({nm for r in win for nm, val in zip(names, r[3])
+        reasons = sorted({nm for r in win for nm, val in zip(self.REASONS, r[3])
                           if val.lower().startswith("active")})
         return {"sm_mhz": statistics.median(r[1] for r in win) if win else None,
                 "sm_max_mhz": max(r[2] for r in win) if win else None, "reasons": reasons,
                 "samples": len(win)}
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        os.unlink(self.path)
 
 
 # ---- the CPU oracle as a baseline ------------------------------------------------------------------
@@ -313,30 +318,39 @@ def run_reference(args, rank):
     return 0
 
 
-def run_ours(args, rank, world, local_rank):
+class Layer:
+    """Device inputs of one preset (tables, weights, batch) and its forward workspace."""
+
+    def __init__(self, l3, cid, args, dev, shard=0, v=None, vocab=None, T=None):
+        import torch
+
+        self.wl = wl = W.make(cid, T=T, shard=shard, v=v, vocab=vocab)
+        self.p = p = wl.p
+        self.T = wl.T
+        self.offs_np = l3.l3_alloc_offsets(wl.freq, p.v, 1, p.k_max, p.power)
+        self.dt = dt = W.torch_dtype(p)
+        self.K, self.V = W.tables(wl, dev)
+        self.offs = torch.as_tensor(self.offs_np, device=dev)
+        self.W_up = torch.as_tensor(wl.W_up, device=dev).to(dt)
+        self.W_mix = torch.as_tensor(wl.W_mix, device=dev).to(dt)
+        self.ids = torch.as_tensor(wl.ids, device=dev)
+        self.x = torch.as_tensor(wl.x, device=dev).to(dt)
+        self.y = torch.empty((self.T, p.d), dtype=dt, device=dev)
+        self.L = l3.make_layer(self.offs, self.K, self.V, self.W_up, self.W_mix, p.k_max)
+        self.ws = torch.empty(l3.l3_workspace_size(self.L, self.T, l3.L3_PASS_FORWARD),
+                              dtype=torch.uint8, device=dev)
+        l3.l3_check_layer(self.L, self.ws)
+
+
+def graph_forward(l3, lay, args, flush, clk, world, window):
+    """Times ``args.steps`` replays of a CUDA graph of l3_forward (L2 flushed before each,
+    outside the events), then replays a second graph with events between the stages.
+
+    Returns (per-step ms list, per-stage mean ms list, launches per step, clock summary).
+    """
     import torch
     import torch.distributed as dist
 
-    import static_token_routed_csr_b300 as l3
-
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    p = W.PRESETS[args.config]
-    wl = W.make(args.config, shard=rank)
-    T = wl.T
-    offs_np = l3.l3_alloc_offsets(wl.freq, p.v, 1, p.k_max, p.power)
-    dt = W.torch_dtype(p)
-    K, V = W.tables(wl, dev)
-    offs = torch.as_tensor(offs_np, device=dev)
-    W_up = torch.as_tensor(wl.W_up, device=dev).to(dt)
-    W_mix = torch.as_tensor(wl.W_mix, device=dev).to(dt)
-    ids = torch.as_tensor(wl.ids, device=dev)
-    x = torch.as_tensor(wl.x, device=dev).to(dt)
-    y = torch.empty((T, p.d), dtype=dt, device=dev)
-    L = l3.make_layer(offs, K, V, W_up, W_mix, p.k_max)
-    ws = torch.empty(l3.l3_workspace_size(L, T, l3.L3_PASS_FORWARD), dtype=torch.uint8, device=dev)
-    l3.l3_check_layer(L, ws)
-    flush = L2Flush(dev)
     nst = l3.L3_FWD_STAGES
 
     def new_events():
@@ -349,11 +363,10 @@ def run_ours(args, rank, world, local_rank):
     warm = new_events()
     for _ in range(args.warmup):
         flush()
-        l3.l3_forward_timed(L, ids, x, y, ws, warm)
+        l3.l3_forward_timed(lay.L, lay.ids, lay.x, lay.y, lay.ws, warm)
     torch.cuda.synchronize()
-    if l3.l3_get_error(ws) != 0:
+    if l3.l3_get_error(lay.ws) != 0:
         raise RuntimeError("device-side error during warm-up")
-
     # The timed step is one replay of a CUDA graph that holds the whole forward, so host-side
     # enqueue gaps are not timed. The per-stage breakdown comes from a second graph with
     # event-record nodes between the stages, replayed after the timed steps: the events
@@ -370,13 +383,13 @@ def run_ours(args, rank, world, local_rank):
         return g
 
     n_cap0 = l3.l3_launch_count()
-    graph = capture(lambda: l3.l3_forward(L, ids, x, y, ws))
+    graph = capture(lambda: l3.l3_forward(lay.L, lay.ids, lay.x, lay.y, lay.ws))
     launches_per_step = l3.l3_launch_count() - n_cap0
-    graph_st = capture(lambda: l3.l3_forward_timed(L, ids, x, y, ws, stage_ev))
+    graph_st = capture(lambda: l3.l3_forward_timed(lay.L, lay.ids, lay.x, lay.y, lay.ws, stage_ev))
     for g in (graph, graph_st):
         g.replay()
     torch.cuda.synchronize()
-    if l3.l3_get_error(ws) != 0:
+    if l3.l3_get_error(lay.ws) != 0:
         raise RuntimeError("device-side error in the captured forward")
     step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps)]
@@ -386,67 +399,157 @@ def run_ours(args, rank, world, local_rank):
             dist.barrier()
         torch.cuda.synchronize()
 
-    clk = ClockSampler(local_rank)
-    clk.start()
     barrier()
-    clk.mark_start()
+    t0 = time.time()
     for k in range(args.steps):
         flush()
         step_ev[k][0].record()
         graph.replay()
         step_ev[k][1].record()
     barrier()
-    clk.mark_end()
+    t1 = time.time()
     stage_samples = []
     for k in range(args.steps):
         flush()
         graph_st.replay()
         torch.cuda.synchronize()
         stage_samples.append([stage_ev[s].elapsed_time(stage_ev[s + 1]) for s in range(nst)])
-    launches = launches_per_step * args.steps
-    clocks = clk.stop()
     step_ms = [a.elapsed_time(b) for a, b in step_ev]
     stage_ms = [statistics.mean(smp[s] for smp in stage_samples) for s in range(nst)]
+    if l3.l3_get_error(lay.ws) != 0:
+        raise RuntimeError("device-side error in the timed steps")
+    return step_ms, stage_ms, launches_per_step, clk.window(t0, t1) if window else None
+
+
+def attend_summary(lay, stage_ms, names, peaks):
+    acct = workload_bytes(lay.p, lay.wl.ids, lay.offs_np)
+    att_ms = stage_ms[names.index("attend")]
+    long_ms = stage_ms[names.index("attend_long")]
+    attend_s = (att_ms + long_ms) / 1e3
+    return acct, {
+        "unique_gbs": acct["attend_bytes"] / attend_s / 1e9,
+        "logical_gbs": acct["logical_bytes"] / attend_s / 1e9,
+        "frac_of_8tbs": acct["attend_bytes"] / attend_s / 8e12,
+        "frac_of_measured": acct["attend_bytes"] / attend_s / 1e9 / peaks["hbm_gbs"],
+        "unique_rows": acct["unique_rows"], "distinct_ids": acct["distinct_ids"],
+        "long_threshold": acct["long_threshold"], "long_ids": acct["long_ids"],
+        "short_gbs": acct["attend_short_bytes"] / (att_ms / 1e3) / 1e9,
+        "short_frac_of_measured": acct["attend_short_bytes"] / (att_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+        "long_gbs": (acct["attend_long_bytes"] / (long_ms / 1e3) / 1e9 if long_ms > 0 else None)}
+
+
+def gemm_summary(acct, stage_ms, names, peaks):
+    out = {}
+    for st, key in (("up", "up_flops"), ("mix", "mix_flops")):
+        ms = stage_ms[names.index(st)]
+        tf = acct[key] / (ms / 1e3) / 1e12
+        out[st] = {"tflops": tf, "frac_of_measured": tf / peaks["bf16_tflops"]}
+    return out
+
+
+def sub_workload(l3, cid, args, dev, flush, clk, peaks) -> dict:
+    """A second workload measured beside the headline (same protocol, own clock window)."""
+    import torch
+
+    lay = Layer(l3, cid, args, dev)
+    step_ms, stage_ms, launches, clocks = graph_forward(l3, lay, args, flush, clk, 1, True)
+    names = l3.STAGE_NAMES
+    ms = statistics.mean(step_ms)
+    acct, att = attend_summary(lay, stage_ms, names, peaks)
+    p = lay.p
+    esz = 2 if p.dtype == "bf16" else 4
+    weights = (p.d * p.d_v + 2 * p.d * p.d) * esz
+    step_bytes = acct["attend_bytes"] + lay.T * p.d * esz + weights  # + U/x re-reads not counted
+    out = {"workload": config_block(p, lay.T)["workload"],
+           "value": lay.T / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
+           "stage_ms": dict(zip(names, stage_ms)), "attend_hbm": att,
+           "gemm": gemm_summary(acct, stage_ms, names, peaks),
+           "step_unique_bytes": step_bytes,
+           "step_frac_of_measured_hbm": step_bytes / (ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+           "gpu_launches_per_step": launches, "clocks": clocks}
+    del lay
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import static_token_routed_csr_b300 as l3
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    lay = Layer(l3, args.config, args, dev, shard=rank, v=args.rows, vocab=args.vocab,
+                T=args.tokens)
+    p, T = lay.p, lay.T
+    flush = L2Flush(dev)
+    clk = ClockSampler(local_rank)
+    clk.start()
+    step_ms, stage_ms, launches_per_step, clocks = graph_forward(l3, lay, args, flush, clk,
+                                                                 world, True)
+    launches = launches_per_step * args.steps
     total_ms = max_over_ranks(sum(step_ms), dev)
     value = job_rate(world, T, args.steps, total_ms)
+    names = l3.STAGE_NAMES
+    peaks = load_peaks()
 
     if args.fwd_only:
+        clk.stop()
         if rank == 0:
-            print(json.dumps({"metric": METRIC, "value": value,
-                              "unit": "tokens/s", "stage_ms": dict(zip(l3.STAGE_NAMES, stage_ms)),
+            print(json.dumps({"metric": METRIC, "value": value, "unit": "tokens/s",
+                              "config": config_block(p, T),
+                              "stage_ms": dict(zip(names, stage_ms)),
                               "note": "forward only (profiling run)"}), flush=True)
         return 0
     # end to end through the host-buffer entry point
-    ws_h = torch.empty(l3.l3_workspace_size(L, T, l3.L3_PASS_FORWARD_HOST), dtype=torch.uint8,
+    import torch.distributed as dist
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    ws_h = torch.empty(l3.l3_workspace_size(lay.L, T, l3.L3_PASS_FORWARD_HOST), dtype=torch.uint8,
                        device=dev)
-    ids_h = ids.cpu().pin_memory()
-    x_h = x.cpu().pin_memory()
-    y_h = torch.empty((T, p.d), dtype=dt).pin_memory()
+    ids_h = lay.ids.cpu().pin_memory()
+    x_h = lay.x.cpu().pin_memory()
+    y_h = torch.empty((T, p.d), dtype=lay.dt).pin_memory()
     for _ in range(max(1, args.warmup)):
-        l3.l3_forward_host(L, ids_h, x_h, y_h, ws_h)
+        l3.l3_forward_host(lay.L, ids_h, x_h, y_h, ws_h)
     torch.cuda.synchronize()
+    e2e_steps = min(args.steps, args.e2e_steps)
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
+              for _ in range(e2e_steps)]
     barrier()
-    for k in range(args.steps):
+    for k in range(e2e_steps):
         flush()
         e2e_ev[k][0].record()
-        l3.l3_forward_host(L, ids_h, x_h, y_h, ws_h)
+        l3.l3_forward_host(lay.L, ids_h, x_h, y_h, ws_h)
         e2e_ev[k][1].record()
     barrier()
     e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e_ev), dev)
-    if not torch.equal(y_h.to(dev), y):
+    if not torch.equal(y_h.to(dev), lay.y):
         raise RuntimeError("host-buffer forward disagrees with the device forward")
+    del ws_h
     esz = 2 if p.dtype == "bf16" else 4
 
-    # fwd+bwd on the small fwd+bwd preset (reported beside the headline)
-    fb = fwd_bwd_rate(l3, dev, args)
+    acct, att = attend_summary(lay, stage_ms, names, peaks)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(lay.wl, lay.offs_np, lay.K, lay.V)
+    del lay
+    torch.cuda.empty_cache()
 
+    # beside the headline: forward + backward, the decode batch and the prefill batch
+    fb = fwd_bwd_rate(l3, dev, args)
+    subs = {}
+    if not args.no_sub:
+        for key, cid in (("decode", 3), ("prefill", 2)):
+            if cid != args.config:
+                subs[key] = sub_workload(l3, cid, args, dev, flush, clk, peaks)
+    clk.stop()
     if rank != 0:
         return 0
-    acct = workload_bytes(p, wl.ids, offs_np)
-    peaks = load_peaks()
-    names = l3.STAGE_NAMES
     dom = int(np.argmax(stage_ms))
     dom_s = stage_ms[dom] / 1e3
     hbm_bytes = {"route": acct["route_bytes"], "attend": acct["attend_short_bytes"],
@@ -469,10 +572,10 @@ def run_ours(args, rank, world, local_rank):
             roof = {"kernel": "gemm-" + names[dom] + " (fp32 CUDA cores)", "bound": "alu",
                     "achieved": achieved, "peak": FP32_FMA_TFLOPS, "unit": "TFLOP/s",
                     "frac": achieved / FP32_FMA_TFLOPS, "traffic": None}
-    roof["traffic"] = NCU_TRAFFIC.get((p.name, names[dom]))
+    roof["traffic"] = NCU_TRAFFIC.get((p.name, names[dom])) if args.rows is None and \
+        args.tokens is None and args.vocab is None else None
     roof["peak_source"] = peaks["source"] if roof["bound"] != "alu" else (
         "derived: 148 SMs x 128 fp32 lanes x 2 FLOP x 2.032 GHz")
-    attend_s = (stage_ms[names.index("attend")] + stage_ms[names.index("attend_long")]) / 1e3
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
@@ -480,24 +583,19 @@ def run_ours(args, rank, world, local_rank):
         "data": "synthetic (seeded Zipf ids, N(0,1) x, N(0,0.02^2) tables, N(0,1/fan_in) weights)",
         "config": config_block(p, T),
         "stage_ms": dict(zip(names, stage_ms)),
-        "attend_hbm": {"unique_gbs": acct["attend_bytes"] / attend_s / 1e9,
-                       "logical_gbs": acct["logical_bytes"] / attend_s / 1e9,
-                       "frac_of_8tbs": acct["attend_bytes"] / attend_s / 8e12,
-                       "frac_of_measured": acct["attend_bytes"] / attend_s / 1e9 / peaks["hbm_gbs"],
-                       "unique_rows": acct["unique_rows"], "distinct_ids": acct["distinct_ids"],
-                       "long_threshold": acct["long_threshold"], "long_ids": acct["long_ids"],
-                       "short_gbs": acct["attend_short_bytes"] / (stage_ms[names.index("attend")] / 1e3) / 1e9,
-                       "long_gbs": (acct["attend_long_bytes"] / (stage_ms[names.index("attend_long")] / 1e3) / 1e9
-                                    if stage_ms[names.index("attend_long")] > 0 else None)},
+        "attend_hbm": att,
+        "gemm": gemm_summary(acct, stage_ms, names, peaks) if p.dtype == "bf16" else None,
         "roofline": roof,
-        "e2e": {"value": job_rate(world, T, args.steps, e2e_ms), "unit": "tokens/s",
+        "e2e": {"value": job_rate(world, T, e2e_steps, e2e_ms), "unit": "tokens/s",
+                "steps": e2e_steps,
                 "h2d_bytes_per_step": T * 4 + T * p.d * esz, "d2h_bytes_per_step": T * p.d * esz},
         "fwd_bwd": fb,
         "gpu_launches": launches,
         "clocks": clocks,
     }
-    if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wl, offs_np, K, V)
+    line.update(subs)
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
     print(json.dumps(line), flush=True)
     return 0
 
@@ -549,10 +647,18 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=500)  # ~0.2 s timed: clock samples fall inside
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--config", type=int, default=2, choices=sorted(W.PRESETS))
+    ap.add_argument("--config", type=int, default=4, choices=sorted(W.PRESETS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fwd-only", action="store_true",
-                    help="skip the e2e and fwd+bwd legs (for profiler captures)")
+                    help="skip the e2e, fwd+bwd and side-workload legs (for profiler captures)")
+    ap.add_argument("--no-sub", action="store_true",
+                    help="skip the decode and prefill workloads measured beside the headline")
+    ap.add_argument("--e2e-steps", type=int, default=50,
+                    help="timed steps of the host-buffer (end-to-end) leg")
+    ap.add_argument("--rows", type=int, default=None,
+                    help="profiling: table rows v of a smaller table with the preset's shapes")
+    ap.add_argument("--vocab", type=int, default=None, help="profiling: vocabulary size")
+    ap.add_argument("--tokens", type=int, default=None, help="profiling: tokens T per batch")
     ap.add_argument("--ref-tokens", type=int, default=128,
                     help="tokens per reference-arm step")
     args = ap.parse_args(argv)

@@ -163,7 +163,9 @@ l3_status l3_route(const l3_layer* layer, const int32_t* ids, int64_t T, int32_t
  *          outside [0, vocab) (the other outputs are then unspecified)
  * Only layer->vocab is read. T may be 0; T > 65536 returns L3_ERR_WORKSPACE. The first
  * call on a device looks up the array's device address with that device current, so
- * make that first call before any stream capture. Every call shares the one array and
+ * make that first call before any stream capture. That address is kept for the life of
+ * the process: after a cudaDeviceReset of a device, this entry point must not be called
+ * on it again (the array may then live elsewhere). Every call shares the one array and
  * clears its status words on entry; calls whose GPU work overlaps (on streams with no
  * ordering between them) race on it.
  */

@@ -114,15 +114,18 @@ class Workload:
 
 
 def make(cid: int, T: Optional[int] = None, shard: int = 0, with_dy: Optional[bool] = None,
-         vocab: Optional[int] = None) -> Workload:
+         vocab: Optional[int] = None, v: Optional[int] = None) -> Workload:
     """Token-side inputs and weights of preset ``cid`` (tables are drawn by ``tables``).
 
     ``T`` overrides the token count (parity cases at reduced size); ``shard`` selects an
-    independent batch (one per rank); ``vocab`` is only for tests of tiny variants.
+    independent batch (one per rank); ``vocab`` and ``v`` shrink the vocabulary and the
+    table (tests of tiny variants, profiler captures of a preset's shapes on smaller tables).
     """
     p = PRESETS[cid]
     if vocab is not None:
         p = dataclasses.replace(p, vocab=vocab)
+    if v is not None:
+        p = dataclasses.replace(p, v=v)
     T = p.T if T is None else int(T)
     c = cid + 100 * shard
     ids = sample_ids(p.vocab, T, np.random.default_rng([c, 1]))

@@ -4,6 +4,8 @@
 #include <climits>
 #include <cmath>
 #include <cstring>
+#include <mutex>
+#include <vector>
 
 #include "l3_internal.h"
 
@@ -343,6 +345,42 @@ l3_status forward_impl(const l3_layer* L, const int32_t* ids, int64_t T, const v
 }  // namespace
 
 void count_launch(int n) { g_launches.fetch_add(uint64_t(n), std::memory_order_relaxed); }
+
+namespace {
+struct SmemAttr {
+  const void* kernel;
+  int dev;
+  int bytes;
+};
+std::mutex g_attr_mu;
+std::vector<SmemAttr> g_attrs;
+constexpr int kMaxDevices = 64;
+int g_sms[kMaxDevices] = {};
+}  // namespace
+
+cudaError_t ensure_smem_attr(const void* kernel, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(g_attr_mu);
+  for (const SmemAttr& a : g_attrs)
+    if (a.kernel == kernel && a.dev == dev && a.bytes >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  g_attrs.push_back(SmemAttr{kernel, dev, bytes});
+  return cudaSuccess;
+}
+
+int device_sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+  int n = __atomic_load_n(&g_sms[dev], __ATOMIC_RELAXED);
+  if (n > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    n = 148;
+  __atomic_store_n(&g_sms[dev], n, __ATOMIC_RELAXED);
+  return n;
+}
 
 cudaError_t launch_check_offsets(const int32_t* offs, int64_t vocab, int64_t v, int k_max,
                                  DevStatus* st, cudaStream_t stream) {

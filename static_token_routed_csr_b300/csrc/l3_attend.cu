@@ -335,8 +335,7 @@ template <typename TE>
 cudaError_t launch_split(const AttendArgs& a, cudaStream_t stream) {
   const SplitShape sh = split_shape(a.d, a.d_v, a.dtype);
   if (sh.stages < 2 || sh.ch != a.ch) return cudaErrorInvalidValue;
-  static cudaError_t attr = cudaFuncSetAttribute(
-      attend_split_kernel<TE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+  const cudaError_t attr = ensure_smem_attr(attend_split_kernel<TE>, kSmemLimit);
   if (attr != cudaSuccess) return attr;
   if (a.n_cta < 1 || a.n_cta > kMaxCtas) return cudaErrorInvalidValue;
   attend_split_kernel<TE><<<a.n_cta, kThreads, sh.smem, stream>>>(a, sh);
@@ -347,16 +346,7 @@ cudaError_t launch_split(const AttendArgs& a, cudaStream_t stream) {
 }  // namespace
 
 namespace split {
-int sm_count() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
-}
+int sm_count() { return device_sm_count(); }
 }  // namespace split
 
 cudaError_t launch_attend_mma(const AttendArgs& a, cudaStream_t stream);

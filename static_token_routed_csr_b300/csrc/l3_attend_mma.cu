@@ -617,8 +617,7 @@ cudaError_t launch_ch(const AttendArgs& a, const MmaShape& sh, cudaStream_t stre
   CUtensorMap mk, mv;
   if (!make_row_block_map(&mk, a.K, a.v, a.d, CH) || !make_row_block_map(&mv, a.V, a.v, a.d_v, CH))
     return cudaErrorInvalidValue;
-  static cudaError_t attr = cudaFuncSetAttribute(
-      attend_mma_kernel<CH, KSW, MTW>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+  const cudaError_t attr = ensure_smem_attr(attend_mma_kernel<CH, KSW, MTW>, kSmemLimit);
   if (attr != cudaSuccess) return attr;
   if (a.n_cta < 1 || a.n_cta > kMaxCtas) return cudaErrorInvalidValue;
   const cudaError_t e = launch_pdl(attend_mma_kernel<CH, KSW, MTW>, dim3(a.n_cta),

@@ -528,16 +528,7 @@ bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, in
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int sm_count() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
-}
+int sm_count() { return device_sm_count(); }
 
 }  // namespace
 
@@ -576,12 +567,7 @@ cudaError_t launch_attend_tc(const AttendTcArgs& a, cudaStream_t stream) {
   p.a_f32 = a.a_f32;
   p.ml = a.ml;
   p.st = a.st;
-  static std::once_flag once;
-  static cudaError_t attr = cudaSuccess;
-  std::call_once(once, [] {
-    attr = cudaFuncSetAttribute(attend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kSmemBytes);
-  });
+  const cudaError_t attr = ensure_smem_attr(attend_tc_kernel, kSmemBytes);
   if (attr != cudaSuccess) return attr;
   e = launch_pdl(attend_tc_kernel, dim3(sm_count()), dim3(kThreads), size_t(kSmemBytes), stream,
                  mk, mx, mv, p);

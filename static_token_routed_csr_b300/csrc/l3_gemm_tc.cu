@@ -402,27 +402,14 @@ bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, in
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int num_sms() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
-}
+int num_sms() { return device_sm_count(); }
 
 template <int BN, int NACC, int STAGES, bool SPLIT>
 cudaError_t launch_tc(const CUtensorMap& a1, const CUtensorMap& a2, const CUtensorMap& b,
                       const TcParams& p, cudaStream_t stream) {
   constexpr int kSmem = STAGES * (kBM + BN) * kBK * 2 + 1024 + 256;
   auto kern = tc_gemm_kernel<BN, NACC, STAGES, SPLIT>;
-  static std::once_flag once;
-  static cudaError_t attr = cudaSuccess;
-  std::call_once(once, [&] {
-    attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-  });
+  const cudaError_t attr = ensure_smem_attr(kern, kSmem);
   if (attr != cudaSuccess) return attr;
   const int units = ((p.M + kBM - 1) / kBM) * ((p.N + BN - 1) / BN) * (SPLIT ? p.splits : 1);
   // a side job (row sums) is spread over every SM even when there are fewer tiles

@@ -10,6 +10,16 @@ namespace l3 {
 
 void count_launch(int n = 1);
 
+// Raises `kernel`'s dynamic shared-memory limit to `bytes` for the current device. The
+// attribute belongs to the device's context, so it is set once per (kernel, device) pair.
+cudaError_t ensure_smem_attr(const void* kernel, int bytes);
+template <typename K>
+inline cudaError_t ensure_smem_attr(K* kernel, int bytes) {
+  return ensure_smem_attr(reinterpret_cast<const void*>(kernel), bytes);
+}
+// Streaming multiprocessors of the current device (looked up once per device).
+int device_sm_count();
+
 // ---- routing (l3_route.cu) ---------------------------------------------------------------
 struct RouteOut {
   int32_t* perm;       // [T]

@@ -525,11 +525,9 @@ cudaError_t launch_route(const int32_t* ids, int64_t T, int64_t vocab, void* scr
   int idbits = 1;
   while (idbits < 31 && (int64_t(1) << idbits) < vocab) ++idbits;
   if (idbits + kIdxBits <= 32) {
-    static cudaError_t a1 = cudaFuncSetAttribute(
-        route_radix_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kRadixSmallSmem));
-    static cudaError_t a2 = cudaFuncSetAttribute(
-        route_radix_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sizeof(RadixSmem)));
+    const cudaError_t a1 = ensure_smem_attr(route_radix_small_kernel, int(kRadixSmallSmem));
     if (a1 != cudaSuccess) return a1;
+    const cudaError_t a2 = ensure_smem_attr(route_radix_chunk_kernel, int(sizeof(RadixSmem)));
     if (a2 != cudaSuccess) return a2;
     const int passes = (idbits + 7) / 8;
     if (T <= kRadixN) {

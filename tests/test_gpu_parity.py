@@ -18,12 +18,13 @@ if not torch.cuda.is_available():  # pragma: no cover - CPU runs deselect this m
 
 import l3_workloads as W  # noqa: E402
 import static_token_routed_csr_b300 as l3  # noqa: E402
-from gpu_case import Case, assert_close, assert_fp32_close, to_np  # noqa: E402
+from gpu_case import (BF16_U, GRAD_FP32_RTOL, Case, assert_close, assert_fp32_close,  # noqa: E402
+                      RouteOnly, assert_rounded_weight_bound, to_np)
 
 
 def _route(case):
     T = case.T
-    dev = case.x.device
+    dev = case.ids.device
     perm = torch.full((max(T, 1),), -7, dtype=torch.int32, device=dev)
     seg_start = torch.full((T + 1,), -7, dtype=torch.int32, device=dev)
     seg_id = torch.full((max(T, 1),), -7, dtype=torch.int32, device=dev)
@@ -42,6 +43,18 @@ def test_route_bit_exact(cid, T):
     c = Case(cid, T=T)
     perm, seg_start, seg_id, S = _route(c)
     ref = oracle.route(c.wl.ids)
+    assert S == len(ref.seg_id)
+    assert np.array_equal(perm, ref.perm)
+    assert np.array_equal(seg_start, ref.seg_start)
+    assert np.array_equal(seg_id, ref.seg_id)
+    assert l3.l3_get_error(c.ws) == 0
+
+
+@pytest.mark.parametrize("T", [3000, 40000])  # one CTA sort; sorted runs of 4096 and 4 merge passes
+def test_route_wide_vocab_bit_exact(T):
+    c = RouteOnly(T)
+    perm, seg_start, seg_id, S = _route(c)
+    ref = oracle.route(c.ids_np)
     assert S == len(ref.seg_id)
     assert np.array_equal(perm, ref.perm)
     assert np.array_equal(seg_start, ref.seg_start)
@@ -127,8 +140,9 @@ def test_forward_small_all_tokens(cid, T):
 
 
 def test_forward_ragged_tile_shapes_all_tokens():
-    # d = 320: odd column-tile counts in both GEMMs (spare tiles in the 2 x 2 cluster mode),
-    # 1100 tokens: odd row-tile count, long segments on tensor cores, short ones split
+    # d = 320: odd column-tile counts in both GEMMs (5 tiles of 64, a 256-wide tile and a
+    # ragged one); 1100 tokens: odd row-tile count, long segments on tensor cores, short
+    # ones split
     c = Case(6)
     y, _ = c.forward()
     fw = c.oracle_forward()
@@ -232,6 +246,9 @@ def test_backward_parity(cid, T):
     ref = oracle.backward(c.offs_np, K, V, c.wl.W_up, c.wl.W_mix, c.wl.ids, c.wl.x, c.wl.dy)
     for name in ("dx", "dK", "dV", "dW_up", "dW_mix"):
         assert_close(c.p, to_np(g[name]), getattr(ref, name), name)
+        # every step of the backward is fp32: an fp32-level normwise bound as well
+        assert_fp32_close(to_np(g[name]), getattr(ref, name), name + " (fp32 level)",
+                          rtol=GRAD_FP32_RTOL if c.p.dtype == "bf16" else None)
 
 
 def test_backward_deterministic_and_untouched_rows_zero():
@@ -254,18 +271,23 @@ def test_forward_bf16_saved_state_and_layernorm_statistics(T):
     torch.cuda.synchronize()
     fw = c.oracle_forward()
     a, ml, mu, rstd = c.saved_views(sv)
-    if T < 1024:
-        # fp32 arithmetic on the bf16 inputs
-        assert_fp32_close(to_np(a), fw.a, "a (fp32 copy)")
-        np.testing.assert_allclose(to_np(ml[:, 1]), fw.l, rtol=1e-5)
-    else:
-        # tensor cores take the softmax weights as bf16: relative error ~2^-9
-        err = np.abs(to_np(a) - fw.a).max() / np.abs(fw.a).max()
-        assert err < 1e-2, err
-        np.testing.assert_allclose(to_np(ml[:, 1]), fw.l, rtol=1e-2)
-    np.testing.assert_allclose(to_np(ml[:, 0]), fw.m, rtol=0, atol=1e-3 * np.abs(fw.m).max() + 1e-4)
-    np.testing.assert_allclose(to_np(rstd), fw.rstd, rtol=1e-2)
-    np.testing.assert_allclose(to_np(mu), fw.mu, rtol=0, atol=2e-2 * np.abs(fw.u).max())
+    a, ml = to_np(a), to_np(ml)
+    long = c.long_segment_tokens()
+    assert (T < 1024) == (not long.any())
+    # split-row tokens: fp32 arithmetic on the bf16 inputs (weights as bf16 hi + lo)
+    assert_fp32_close(a[~long], fw.a[~long], "a (fp32 copy), split-row tokens")
+    np.testing.assert_allclose(ml[~long, 1], fw.l[~long], rtol=1e-5)
+    if long.any():
+        # tensor-core tokens: the derived bound of bf16-rounded weights
+        toks = np.nonzero(long)[0]
+        assert_rounded_weight_bound(a[toks], ml[toks, 1], c.oracle_weights(toks), "a, tensor-core tokens")
+    np.testing.assert_allclose(ml[:, 0], fw.m, rtol=0, atol=1e-3 * np.abs(fw.m).max() + 1e-4)
+    # A and U enter the GEMMs rounded to bf16 (reading "bf16 storage"). Rounding u_n to
+    # u_n (1 + d_n), |d_n| <= u, moves the mean by at most u max|u| and the variance by a
+    # relative 2u (rstd by u); the rounding of a only adds errors uncorrelated with u_n,
+    # smaller by about 1/sqrt(d). Bound: 2u for both.
+    np.testing.assert_allclose(to_np(rstd), fw.rstd, rtol=2 * BF16_U)
+    np.testing.assert_allclose(to_np(mu), fw.mu, rtol=0, atol=2 * BF16_U * np.abs(fw.u).max())
     assert_close(c.p, to_np(y), fw.y, "y")
     assert l3.l3_get_error(c.ws) == 0
 
@@ -281,8 +303,12 @@ def test_tensor_core_attend_one_long_segment_and_mixed_ranges():
     toks = np.unique(np.concatenate([np.nonzero(ids == 0)[0][::37], np.nonzero(ids != 0)[0][::5]]))
     fw = c.oracle_forward(tokens=toks)
     assert_close(c.p, to_np(y)[toks], fw.y, "y")
-    a = to_np(c.saved_views(sv)[0])[toks]
-    assert np.abs(a - fw.a).max() / np.abs(fw.a).max() < 1e-2
+    a, ml, _, _ = c.saved_views(sv)
+    long = c.long_segment_tokens()[toks]
+    assert long.any() and (~long).any()
+    assert_rounded_weight_bound(to_np(a)[toks[long]], to_np(ml)[toks[long], 1],
+                                c.oracle_weights(toks[long]), "a, id 0")
+    assert_fp32_close(to_np(a)[toks[~long]], fw.a[~long], "a, short ids")
     assert l3.l3_get_error(c.ws) == 0
 
 

@@ -4,9 +4,10 @@ Such callers (a plugin whose host program owns all device allocations, a latency
 loop that must not enter an allocator) cannot hand the library a workspace. This entry
 point keeps its scratch in a fixed array the library declares in device memory. The test
 calls it through the C ABI twice in a row, on different batches, and checks both results
-against l3_route (bit for bit: the outputs are integers), then checks the size limit and
-the bad-id report. This file is collected last so that a run stopping at the first
-failure has run every other test already.
+against l3_route and against the oracle's stable sort (bit for bit: the outputs are
+integers), then covers the largest batch the fixed array holds (65536 tokens, on both sort
+paths), an empty batch, the size limit and the bad-id report. This file is collected last
+so that a run stopping at the first failure has run every other test already.
 """
 import ctypes
 
@@ -19,8 +20,9 @@ pytestmark = pytest.mark.gpu
 if not torch.cuda.is_available():  # pragma: no cover
     pytest.skip("needs a CUDA device", allow_module_level=True)
 
+import oracle  # noqa: E402
 import static_token_routed_csr_b300 as l3  # noqa: E402
-from gpu_case import Case  # noqa: E402
+from gpu_case import Case, RouteOnly  # noqa: E402
 
 
 def _outs(T, dev="cuda"):
@@ -56,6 +58,17 @@ def _same(a, b):
     assert np.array_equal(ia[:S], ib[:S])
 
 
+def _matches_oracle(got, ids_np):
+    perm, start, sid, n = (t.cpu().numpy() for t in got)
+    ref = oracle.route(ids_np)
+    S = int(n[0])
+    assert S == len(ref.seg_id)
+    T = len(ids_np)
+    assert np.array_equal(perm[:T], ref.perm)
+    assert np.array_equal(start[:S + 1], ref.seg_start)
+    assert np.array_equal(sid[:S], ref.seg_id)
+
+
 def test_no_alloc_route_matches_workspace_route_twice():
     first = Case(2, T=12289)   # several sort runs and merge passes
     second = Case(1)           # small batch: one CTA sort, leftovers of the first call remain
@@ -64,6 +77,29 @@ def test_no_alloc_route_matches_workspace_route_twice():
         got = _no_alloc(case)
         torch.cuda.synchronize()
         _same(got, ref)
+        _matches_oracle(got, case.wl.ids)
+
+
+@pytest.mark.parametrize("vocab,T", [(128256, 65536),    # 32-bit keys: 8 runs, 3 merge passes
+                                     (1 << 20, 65536),   # 64-bit keys: 16 runs, 4 merge passes
+                                     (1 << 20, 3000)])   # 64-bit keys, one CTA
+def test_no_alloc_route_full_array_and_wide_ids(vocab, T):
+    case = RouteOnly(T, seed=vocab % 97, vocab=vocab)
+    got = _no_alloc(case)
+    torch.cuda.synchronize()
+    _matches_oracle(got, case.ids_np)
+    _same(got, _with_workspace(case))
+
+
+def test_no_alloc_route_empty_batch():
+    case = Case(1)
+    n = torch.full((1,), -7, dtype=torch.int32, device="cuda")
+    start = torch.full((1,), -7, dtype=torch.int32, device="cuda")
+    rc = l3.lib().l3_route_noalloc(ctypes.byref(case.layer), None, 0, None, start.data_ptr(), None,
+                                   n.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert rc == 0, l3.l3_status_string(rc)
+    torch.cuda.synchronize()
+    assert int(n.item()) == 0 and int(start.item()) == 0
 
 
 def test_no_alloc_limits_and_bad_ids():
