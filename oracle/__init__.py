@@ -2,10 +2,10 @@
 
 Importable only by tests/, __graft_entry__.smoke() and bench.py's CPU legs.
 """
-from .l3_oracle import (Allocation, Backward, Forward, Route, allocate, attend,
-                        attend_dense_masked, backward, forward, forward_token,
-                        layer_norm, route, token_rows)
+from .l3_oracle import (Allocation, Backward, Forward, Route, allocate, allocate_from_counts,
+                        attend, attend_dense_masked, backward, count_ids, forward,
+                        forward_token, layer_norm, route, token_rows)
 
-__all__ = ["Allocation", "Backward", "Forward", "Route", "allocate", "attend",
-           "attend_dense_masked", "backward", "forward", "forward_token", "layer_norm",
-           "route", "token_rows"]
+__all__ = ["Allocation", "Backward", "Forward", "Route", "allocate", "allocate_from_counts",
+           "attend", "attend_dense_masked", "backward", "count_ids", "forward",
+           "forward_token", "layer_norm", "route", "token_rows"]

@@ -110,6 +110,29 @@ def allocate(freq, v: int, n_min: int, n_max: int, power: float) -> Allocation:
 
 
 # --------------------------------------------------------------------------------------
+# Frequencies from a token stream ([gist] "Information-Theoretic Embedding Allocation":
+# the allocation follows how often each token occurs; a stream of token ids stands in
+# for the training corpus, whose corpus-driven Algorithm 1 is not on the pages).
+# --------------------------------------------------------------------------------------
+
+def count_ids(ids, vocab: int) -> np.ndarray:
+    """Occurrences of each id 0..vocab-1 in the stream (int64). Ids outside [0, vocab)
+    are an error."""
+    ids = np.asarray(ids, dtype=np.int64)
+    if ids.size and (ids.min() < 0 or ids.max() >= vocab):
+        raise ValueError("token id outside [0, vocab)")
+    return np.bincount(ids, minlength=vocab).astype(np.int64)
+
+
+def allocate_from_counts(counts, v: int, n_min: int, n_max: int, power: float,
+                         smoothing: float) -> Allocation:
+    """The frequency allocation with freq_t = count_t + smoothing (add-smoothing keeps an
+    id that never occurred at a positive frequency; the clamp gives it n_min rows)."""
+    freq = np.asarray(counts, dtype=np.int64).astype(np.float64) + float(smoothing)
+    return allocate(freq, v, n_min, n_max, power)
+
+
+# --------------------------------------------------------------------------------------
 # Routing ([gist] "Core Architecture": static routing, t alone selects rows;
 # "Systems-Friendly Design": sorting the batch by token id).
 # --------------------------------------------------------------------------------------
