@@ -120,6 +120,30 @@ enum {
 l3_status l3_alloc_offsets(const double* freq, int64_t vocab, int64_t v, int32_t n_min,
                            int32_t n_max, double power, int32_t* offs_out);
 
+/*
+ * Token frequencies of a stream of token ids, the statistic the allocation follows
+ * (explainer, "Information-Theoretic Embedding Allocation": frequent tokens get more
+ * rows). A stream of ids stands in for the training corpus; the corpus-driven Algorithm 1
+ * itself is not on the pages.
+ *   ids     [n] int32 token ids (device), 0 <= n < 2^31
+ *   counts  [vocab] int64 out (device): counts[t] = occurrences of id t (overwritten)
+ *   ws      >= 256 bytes of device memory for the status words
+ * Ids outside [0, vocab) are not counted; l3_get_error(ws, stream) then reports
+ * L3_ERR_TOKEN_RANGE. The counts are exact (integer atomics) and independent of order.
+ */
+l3_status l3_count_ids(const int32_t* ids, int64_t n, int64_t vocab, int64_t* counts, void* ws,
+                       size_t ws_bytes, l3_stream_t stream);
+
+/*
+ * l3_alloc_offsets with freq[t] = counts_host[t] + smoothing (host only, synchronous).
+ * Add-smoothing gives ids that never occurred a positive frequency (they end up with the
+ * fewest rows). counts_host: [vocab] int64 >= 0 (from l3_count_ids); smoothing >= 0, and
+ * with smoothing = 0 every count must be positive. Errors as l3_alloc_offsets.
+ */
+l3_status l3_alloc_offsets_counts(const int64_t* counts_host, int64_t vocab, int64_t v,
+                                  int32_t n_min, int32_t n_max, double power, double smoothing,
+                                  int32_t* offs_out);
+
 /* Bytes of workspace a call needs (pass: L3_PASS_*), 0 if the layer is invalid. */
 size_t l3_workspace_size(const l3_layer* layer, int64_t T, int32_t pass);
 

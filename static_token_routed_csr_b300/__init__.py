@@ -20,7 +20,7 @@ __all__ = [
     "STAGE_NAMES", "l3_alloc_offsets", "l3_workspace_size", "l3_saved_size",
     "l3_check_layer", "l3_route", "l3_route_noalloc", "l3_forward", "l3_forward_timed", "l3_forward_host",
     "l3_backward", "l3_get_error", "l3_status_string", "l3_launch_count", "l3_abi_version",
-    "l3_selftest_wait_timeout",
+    "l3_selftest_wait_timeout", "l3_count_ids", "l3_alloc_offsets_counts",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libl3.so")
@@ -70,6 +70,9 @@ _SIGNATURES = {
     "l3_launch_count": (ctypes.c_uint64, []),
     "l3_abi_version": (_I32, []),
     "l3_selftest_wait_timeout": (_I32, [_P, _SZ, _I64, _P]),
+    "l3_count_ids": (_I32, [_P, _I64, _I64, _P, _P, _SZ, _P]),
+    "l3_alloc_offsets_counts": (_I32, [_P, _I64, _I64, _I32, _I32, ctypes.c_double,
+                                       ctypes.c_double, _P]),
 }
 
 _lib = None
@@ -147,6 +150,23 @@ def l3_alloc_offsets(freq, v: int, n_min: int, n_max: int, power: float) -> np.n
     out = np.zeros(f.shape[0] + 1, dtype=np.int32)
     _check(lib().l3_alloc_offsets(_ptr(f), f.shape[0], int(v), int(n_min), int(n_max),
                                   float(power), _ptr(out)), "l3_alloc_offsets")
+    return out
+
+
+def l3_count_ids(ids, vocab: int, counts, ws, stream=None) -> None:
+    """counts [vocab] int64 (device) = occurrences of each id in ``ids`` (device int32)."""
+    _check(lib().l3_count_ids(_ptr(ids), ids.numel(), int(vocab), _ptr(counts), _ptr(ws),
+                              ws.numel() * ws.element_size(), _stream(stream)), "l3_count_ids")
+
+
+def l3_alloc_offsets_counts(counts, v: int, n_min: int, n_max: int, power: float,
+                            smoothing: float) -> np.ndarray:
+    """Host-only allocation from token counts (freq = counts + smoothing); offs [vocab+1]."""
+    c = np.ascontiguousarray(counts, dtype=np.int64)
+    out = np.zeros(c.shape[0] + 1, dtype=np.int32)
+    _check(lib().l3_alloc_offsets_counts(_ptr(c), c.shape[0], int(v), int(n_min), int(n_max),
+                                         float(power), float(smoothing), _ptr(out)),
+           "l3_alloc_offsets_counts")
     return out
 
 

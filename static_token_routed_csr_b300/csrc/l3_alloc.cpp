@@ -130,3 +130,16 @@ extern "C" l3_status l3_alloc_offsets(const double* freq, int64_t vocab, int64_t
   }
   return run == v ? L3_OK : L3_ERR_INFEASIBLE;
 }
+
+extern "C" l3_status l3_alloc_offsets_counts(const int64_t* counts, int64_t vocab, int64_t v,
+                                             int32_t n_min, int32_t n_max, double power,
+                                             double smoothing, int32_t* offs_out) {
+  if (!counts || vocab < 1 || !(smoothing >= 0.0) || !std::isfinite(smoothing))
+    return L3_ERR_INVALID_ARG;
+  std::vector<double> freq(static_cast<size_t>(vocab));
+  for (int64_t t = 0; t < vocab; ++t) {
+    if (counts[t] < 0) return L3_ERR_INVALID_ARG;
+    freq[size_t(t)] = double(counts[t]) + smoothing;  // l3_alloc_offsets rejects a zero
+  }
+  return l3_alloc_offsets(freq.data(), vocab, v, n_min, n_max, power, offs_out);
+}

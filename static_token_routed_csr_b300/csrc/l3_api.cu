@@ -662,6 +662,18 @@ l3_status l3_backward(const l3_layer* L, const int32_t* ids, int64_t T, const vo
   return L3_OK;
 }
 
+l3_status l3_count_ids(const int32_t* ids, int64_t n, int64_t vocab, int64_t* counts, void* ws,
+                       size_t ws_bytes, l3_stream_t stream) {
+  if (n < 0 || n >= (int64_t(1) << 31) || vocab < 1 || vocab >= (int64_t(1) << 31) || !counts ||
+      !ws || (n > 0 && !ids))
+    return L3_ERR_INVALID_ARG;
+  if (ws_bytes < sizeof(DevStatus)) return L3_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  L3_CUDA(cudaMemsetAsync(ws, 0, sizeof(DevStatus), s));
+  L3_CUDA(launch_count_ids(ids, n, vocab, counts, static_cast<DevStatus*>(ws), s));
+  return L3_OK;
+}
+
 l3_status l3_get_error(void* ws, l3_stream_t stream) {
   if (!ws) return L3_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

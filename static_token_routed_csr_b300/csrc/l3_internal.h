@@ -225,6 +225,12 @@ struct SegReduceArgs {
 };
 cudaError_t launch_seg_reduce(const SegReduceArgs& a, cudaStream_t stream);
 
+// ---- token-stream counts (l3_count.cu) ---------------------------------------------------
+// counts[t] (int64, zeroed here) = occurrences of id t in ids[0..n); ids outside [0, vocab)
+// are not counted and set st->token_range.
+cudaError_t launch_count_ids(const int32_t* ids, int64_t n, int64_t vocab, int64_t* counts,
+                             DevStatus* st, cudaStream_t stream);
+
 // ---- layer check (l3_api.cu) ---------------------------------------------------------------
 cudaError_t launch_check_offsets(const int32_t* offs, int64_t vocab, int64_t v, int k_max,
                                  DevStatus* st, cudaStream_t stream);

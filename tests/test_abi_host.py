@@ -157,3 +157,39 @@ def test_workspace_grows_with_the_batch_and_covers_decode_scratch(lib):
     assert sizes[-1] > sizes[-2] > sizes[0]
     # at 64 tokens the split-K parts (fp32, a few per output element) dominate the growth
     assert sizes[1] - sizes[0] > 64 * 2048 * 4
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_alloc_offsets_from_counts_bit_exact_vs_oracle(seed):
+    rng = np.random.default_rng([seed, 21])
+    vocab = int(rng.integers(50, 3000))
+    ids = W.sample_ids(vocab, int(rng.integers(0, 50000)), rng)
+    counts = oracle.count_ids(ids, vocab)
+    v = int(vocab * rng.integers(2, 30))
+    smoothing = [1.0, 0.5, 1e-3, 2.0][seed]
+    got = l3.l3_alloc_offsets_counts(counts, v, 1, 64, 0.7, smoothing)
+    want = oracle.allocate_from_counts(counts, v, 1, 64, 0.7, smoothing).offs
+    assert np.array_equal(got.astype(np.int64), want)
+
+
+def test_alloc_offsets_from_counts_errors():
+    counts = np.array([3, 0, 5], dtype=np.int64)
+    with pytest.raises(l3.L3Error) as e:
+        l3.l3_alloc_offsets_counts(counts, 6, 1, 4, 1.0, 0.0)  # an unseen id, no smoothing
+    assert e.value.status == 1
+    with pytest.raises(l3.L3Error):
+        l3.l3_alloc_offsets_counts(np.array([3, -1], dtype=np.int64), 4, 1, 4, 1.0, 1.0)
+    with pytest.raises(l3.L3Error):
+        l3.l3_alloc_offsets_counts(counts, 6, 1, 4, 1.0, float("nan"))
+    with pytest.raises(l3.L3Error) as e:
+        l3.l3_alloc_offsets_counts(counts, 100, 1, 4, 1.0, 1.0)  # 100 > 3 * 4 rows
+    assert e.value.status == 2
+
+
+def test_count_ids_argument_errors(lib):
+    ws = np.zeros(256, np.uint8)
+    counts = np.zeros(4, np.int64)
+    assert lib.l3_count_ids(None, 5, 4, counts.ctypes.data, ws.ctypes.data, 256, None) == 1
+    assert lib.l3_count_ids(None, 0, 0, counts.ctypes.data, ws.ctypes.data, 256, None) == 1
+    assert lib.l3_count_ids(None, 0, 4, None, ws.ctypes.data, 256, None) == 1
+    assert lib.l3_count_ids(None, 0, 4, counts.ctypes.data, ws.ctypes.data, 8, None) == 4
