@@ -268,16 +268,41 @@ class Backward(NamedTuple):
     dW_mix: np.ndarray  # [d, 2d]
 
 
-def backward(offs, K, V, W_up, W_mix, ids, x, dy, eps: float = 1e-5) -> Backward:
-    """Gradients of sum(dy * y) for the layer formula, in fp64.
+def backward_token(offs, K, V, W_up, W_mix, t: int, x, g, eps: float):
+    """The chain rule of the layer formula for one token (id t, input x, upstream dy = g).
 
-    Per token (rows R of id t, forward values s, p, a, u, h, mu, rstd):
-      dW_mix += dy cᵀ with c = [h; x];  dc = W_mixᵀ dy;  dh = dc[:d];  dx = dc[d:]
+    Forward values s, p, a, u, h, mu, rstd of the token, then:
+      dW_mix term: g cᵀ with c = [h; x];  dc = W_mixᵀ g;  dh = dc[:d];  dx = dc[d:]
       du = rstd (dh - mean(dh) - h mean(dh h))          (LayerNorm, no affine)
-      dW_up += du aᵀ;  da = W_upᵀ du
+      dW_up term: du aᵀ;  da = W_upᵀ du
       dp_j = V_j . da;  ds_j = p_j (dp_j - sum_k p_k dp_k)   (softmax)
-      dx += K_Rᵀ ds;  dK[R] += ds xᵀ;  dV[R] += p daᵀ
+      dx += K_Rᵀ ds;  dK[R] term: ds xᵀ;  dV[R] term: p daᵀ
+    Returns (dx, dK_rows, dV_rows, dW_up term, dW_mix term) for the rows R of id t.
     """
+    W_up, W_mix = _f64(W_up), _f64(W_mix)
+    d = W_up.shape[0]
+    rows = token_rows(offs, t)
+    Kt = _f64(K[rows.start:rows.stop])
+    Vt = _f64(V[rows.start:rows.stop])
+    xi = _f64(x)
+    g = _f64(g)
+    a, _, p, _, _ = attend(Kt, Vt, xi)
+    u = W_up @ a
+    h, _, rstd = layer_norm(u, eps)
+    c = np.concatenate([h, xi])
+    dc = W_mix.T @ g
+    dh = dc[:d]
+    du = rstd * (dh - np.mean(dh) - h * np.mean(dh * h))
+    da = W_up.T @ du
+    dp = Vt @ da
+    ds = p * (dp - np.dot(p, dp))
+    dx = dc[d:] + Kt.T @ ds
+    return dx, np.outer(ds, xi), np.outer(p, da), np.outer(du, a), np.outer(g, c)
+
+
+def backward(offs, K, V, W_up, W_mix, ids, x, dy, eps: float = 1e-5) -> Backward:
+    """Gradients of sum(dy * y) for the layer formula, in fp64, dense dK and dV
+    (``backward_token`` per token, summed)."""
     W_up, W_mix = _f64(W_up), _f64(W_mix)
     ids = np.asarray(ids)
     d, d_v = W_up.shape
@@ -290,23 +315,52 @@ def backward(offs, K, V, W_up, W_mix, ids, x, dy, eps: float = 1e-5) -> Backward
     for i in range(len(ids)):
         t = int(ids[i])
         rows = token_rows(offs, t)
-        Kt = _f64(K[rows.start:rows.stop])
-        Vt = _f64(V[rows.start:rows.stop])
-        xi = _f64(x[i])
-        g = _f64(dy[i])
-        a, _, p, _, _ = attend(Kt, Vt, xi)
-        u = W_up @ a
-        h, _, rstd = layer_norm(u, eps)
-        c = np.concatenate([h, xi])
-        dW_mix += np.outer(g, c)
-        dc = W_mix.T @ g
-        dh = dc[:d]
-        du = rstd * (dh - np.mean(dh) - h * np.mean(dh * h))
-        dW_up += np.outer(du, a)
-        da = W_up.T @ du
-        dp = Vt @ da
-        ds = p * (dp - np.dot(p, dp))
-        dx[i] = dc[d:] + Kt.T @ ds
-        dK[rows.start:rows.stop] += np.outer(ds, xi)
-        dV[rows.start:rows.stop] += np.outer(p, da)
+        dx[i], gK, gV, gu, gm = backward_token(offs, K, V, W_up, W_mix, t, x[i], dy[i], eps)
+        dK[rows.start:rows.stop] += gK
+        dV[rows.start:rows.stop] += gV
+        dW_up += gu
+        dW_mix += gm
     return Backward(dx, dK, dV, dW_up, dW_mix)
+
+
+class SparseBackward(NamedTuple):
+    dx: np.ndarray      # [len(tokens), d] for the requested tokens
+    rows: dict          # id t -> (dK rows [n_t, d], dV rows [n_t, d_v]), summed over t's tokens
+    dW_up: object       # [d, d_v], or None when not requested
+    dW_mix: object      # [d, 2d], or None
+
+
+def backward_rows(offs, K, V, W_up, W_mix, ids, x, dy, eps: float = 1e-5, tokens=None,
+                  row_ids=None, weights: bool = True) -> SparseBackward:
+    """The same gradients with dK and dV kept only for the rows the batch touches.
+
+    ``tokens``: the tokens whose dx is returned (default all). ``row_ids``: the ids whose
+    row gradients are returned (default every id in the batch); each sums over all of
+    that id's tokens in the batch. ``weights``: also sum dW_up and dW_mix over all tokens.
+    Only the tokens these outputs need are visited.
+    """
+    ids = np.asarray(ids)
+    W_up, W_mix = _f64(W_up), _f64(W_mix)
+    d, d_v = W_up.shape
+    tok = list(range(len(ids))) if tokens is None else [int(i) for i in tokens]
+    want = set(int(t) for t in (np.unique(ids) if row_ids is None else row_ids))
+    visit = range(len(ids)) if weights else sorted(set(tok) | {i for i in range(len(ids))
+                                                                  if int(ids[i]) in want})
+    pos = {i: j for j, i in enumerate(tok)}
+    dx = np.zeros((len(tok), d))
+    rows = {t: (np.zeros((len(token_rows(offs, t)), d)), np.zeros((len(token_rows(offs, t)), d_v)))
+            for t in want}
+    dW_up = np.zeros((d, d_v)) if weights else None
+    dW_mix = np.zeros((d, 2 * d)) if weights else None
+    for i in visit:
+        t = int(ids[i])
+        gx, gK, gV, gu, gm = backward_token(offs, K, V, W_up, W_mix, t, x[i], dy[i], eps)
+        if i in pos:
+            dx[pos[i]] = gx
+        if t in rows:
+            rows[t][0][:] += gK
+            rows[t][1][:] += gV
+        if weights:
+            dW_up += gu
+            dW_mix += gm
+    return SparseBackward(dx, rows, dW_up, dW_mix)

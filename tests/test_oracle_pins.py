@@ -230,3 +230,33 @@ def test_gradient_identities():
     np.testing.assert_allclose(g.dK[r.start:r.stop].sum(axis=0), 0.0, atol=1e-14)
     assert not g.dK[:r.start].any() and not g.dK[r.stop:].any()
     assert not g.dV[:r.start].any() and not g.dV[r.stop:].any()
+
+
+def test_row_gradients_keep_only_touched_rows_and_match_the_dense_form():
+    # the sparse form stores the same sums: the touched ids' rows of dense dK/dV, every
+    # other row of the dense form zero, dx and dW unchanged; subsets of tokens and ids
+    # select rows of the same results
+    rng = np.random.default_rng(12)
+    offs, K, V, W_up, W_mix, ids, x = _rand_layer(rng, vocab=7, d=5, d_v=4, T=11)
+    dy = rng.standard_normal((11, 5))
+    dense = oracle.backward(offs, K, V, W_up, W_mix, ids, x, dy)
+    sp = oracle.backward_rows(offs, K, V, W_up, W_mix, ids, x, dy)
+    assert sorted(sp.rows) == sorted(set(ids.tolist()))
+    touched = np.zeros(int(offs[-1]), bool)
+    for t, (gK, gV) in sp.rows.items():
+        r = oracle.token_rows(offs, t)
+        touched[r.start:r.stop] = True
+        np.testing.assert_allclose(gK, dense.dK[r.start:r.stop], rtol=0, atol=1e-13)
+        np.testing.assert_allclose(gV, dense.dV[r.start:r.stop], rtol=0, atol=1e-13)
+    assert not dense.dK[~touched].any() and not dense.dV[~touched].any()
+    np.testing.assert_allclose(sp.dx, dense.dx, atol=1e-13)
+    np.testing.assert_allclose(sp.dW_up, dense.dW_up, atol=1e-13)
+    np.testing.assert_allclose(sp.dW_mix, dense.dW_mix, atol=1e-13)
+    some = [8, 2]
+    t0 = int(ids[5])
+    sub = oracle.backward_rows(offs, K, V, W_up, W_mix, ids, x, dy, tokens=some, row_ids=[t0],
+                               weights=False)
+    assert sub.dW_up is None and list(sub.rows) == [t0]
+    np.testing.assert_allclose(sub.dx, dense.dx[some], atol=1e-13)
+    r = oracle.token_rows(offs, t0)
+    np.testing.assert_allclose(sub.rows[t0][0], dense.dK[r.start:r.stop], atol=1e-13)
