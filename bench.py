@@ -534,6 +534,9 @@ def run_ours(args, rank, world, local_rank):
     esz = 2 if p.dtype == "bf16" else 4
 
     acct, att = attend_summary(lay, stage_ms, names, peaks)
+    fb_rows = None
+    if p.dtype == "bf16" and not args.no_bwd:
+        fb_rows = fwd_bwd_rows_rate(l3, lay, args, flush, acct, world)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(lay.wl, lay.offs_np, lay.K, lay.V)
@@ -547,6 +550,7 @@ def run_ours(args, rank, world, local_rank):
         for key, cid in (("decode", 3), ("prefill", 2)):
             if cid != args.config:
                 subs[key] = sub_workload(l3, cid, args, dev, flush, clk, peaks)
+        subs["offload"] = offload_leg(l3, 3, args, dev, flush, peaks)
     clk.stop()
     if rank != 0:
         return 0
@@ -589,7 +593,8 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": job_rate(world, T, e2e_steps, e2e_ms), "unit": "tokens/s",
                 "steps": e2e_steps,
                 "h2d_bytes_per_step": T * 4 + T * p.d * esz, "d2h_bytes_per_step": T * p.d * esz},
-        "fwd_bwd": fb,
+        "fwd_bwd": fb_rows if fb_rows is not None else fb,
+        "fwd_bwd_small": fb,
         "gpu_launches": launches,
         "clocks": clocks,
     }
@@ -598,6 +603,168 @@ def run_ours(args, rank, world, local_rank):
         line["cpu_baseline"] = cpu
     print(json.dumps(line), flush=True)
     return 0
+
+
+def fwd_bwd_rows_rate(l3, lay, args, flush, acct, world) -> dict:
+    """Forward (keeping the saved state) + row-gradient backward over the headline batch,
+    one CUDA graph per step, L2 flushed before each step (outside the events)."""
+    import torch
+
+    p, T, dev = lay.p, lay.T, lay.x.device
+    g = torch.Generator(device=dev)
+    g.manual_seed(7000 + p.cid)
+    dy = torch.randn((T, p.d), generator=g, device=dev).to(torch.bfloat16)
+    rows = acct["unique_rows"]
+    sv = torch.empty(l3.l3_saved_size(lay.L, T), dtype=torch.uint8, device=dev)
+    wsb = torch.empty(l3.l3_workspace_size(lay.L, T, l3.L3_PASS_BACKWARD_ROWS), dtype=torch.uint8,
+                      device=dev)
+    dx = torch.empty((T, p.d), device=dev)
+    row_index = torch.empty(rows, dtype=torch.int32, device=dev)
+    dK = torch.empty((rows, p.d), device=dev)
+    dV = torch.empty((rows, p.d_v), device=dev)
+    n_rows = torch.zeros(1, dtype=torch.int32, device=dev)
+    dWu = torch.empty((p.d, p.d_v), device=dev)
+    dWm = torch.empty((p.d, 2 * p.d), device=dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+
+    def step(timed):
+        if timed:
+            ev[0].record()
+        l3.l3_forward(lay.L, lay.ids, lay.x, lay.y, lay.ws, saved=sv)
+        if timed:
+            ev[1].record()
+        l3.l3_backward_rows(lay.L, lay.ids, lay.x, dy, sv, dx, row_index, dK, dV, n_rows, dWu, dWm,
+                            wsb)
+        if timed:
+            ev[2].record()
+
+    for _ in range(args.warmup):
+        flush()
+        step(False)
+    torch.cuda.synchronize()
+    if l3.l3_get_error(wsb) != 0 or int(n_rows.item()) != rows:
+        raise RuntimeError("row-gradient backward reported an error")
+    cap = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(graph, stream=cap, capture_error_mode="thread_local"):
+        step(False)
+    torch.cuda.synchronize()
+    steps = max(3, min(args.steps, args.bwd_steps))
+    tot = 0.0
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(steps)]
+    for k in range(steps):
+        flush()
+        pairs[k][0].record()
+        graph.replay()
+        pairs[k][1].record()
+    torch.cuda.synchronize()
+    tot = sum(a.elapsed_time(b) for a, b in pairs)
+    total_ms = max_over_ranks(tot, dev)
+    # the split between forward and backward, from one eager step with events
+    flush()
+    step(True)
+    torch.cuda.synchronize()
+    return {"workload": config_block(p, T)["workload"] + ", dy ~ N(0,1) bf16",
+            "value": job_rate(world, T, steps, total_ms), "unit": "tokens/s",
+            "ms_per_step": total_ms / steps, "steps": steps,
+            "fwd_ms": ev[0].elapsed_time(ev[1]), "bwd_ms": ev[1].elapsed_time(ev[2]),
+            "touched_rows": rows,
+            "row_grad_bytes": rows * (p.d + p.d_v) * 4,
+            "l2": "flushed before every timed step (outside the timed events)"}
+
+
+def offload_leg(l3, cid, args, dev, flush, peaks) -> dict:
+    """Tables in pinned host memory: per step the batch's rows are staged into device memory
+    (l3_stage_rows) and the forward runs over the staged layer. Reported serially (stage, then
+    forward) and pipelined (the next batch's rows staged on a second stream while the current
+    forward runs, double-buffered staging), the way a model would prefetch during earlier
+    layers."""
+    import torch
+
+    lay = Layer(l3, cid, args, dev)
+    p, T = lay.p, lay.T
+    K_h, V_h = lay.K.cpu().pin_memory(), lay.V.cpu().pin_memory()
+    del lay.K, lay.V
+    torch.cuda.empty_cache()
+    L_h = l3.make_layer(lay.offs, K_h, V_h, lay.W_up, lay.W_mix, p.k_max)
+    acct = workload_bytes(p, lay.wl.ids, lay.offs_np)
+    U = acct["unique_rows"]
+    cap = U + T
+    bufs = []
+    for _ in range(2):
+        K_s = torch.empty((cap, p.d), dtype=lay.dt, device=dev)
+        V_s = torch.empty((cap, p.d_v), dtype=lay.dt, device=dev)
+        offs_s = torch.empty(T + 1, dtype=torch.int32, device=dev)
+        ids_s = torch.empty(T, dtype=torch.int32, device=dev)
+        n_rows = torch.zeros(1, dtype=torch.int32, device=dev)
+        ws_s = torch.empty(l3.l3_workspace_size(L_h, T, l3.L3_PASS_STAGE), dtype=torch.uint8,
+                           device=dev)
+        y = torch.empty((T, p.d), dtype=lay.dt, device=dev)
+        bufs.append(dict(K=K_s, V=V_s, offs=offs_s, ids=ids_s, n=n_rows, ws=ws_s, y=y))
+    s_main = torch.cuda.current_stream()
+    s_copy = torch.cuda.Stream()
+
+    def stage(b, stream):
+        with torch.cuda.stream(stream):
+            b["L"] = l3.l3_stage_rows(L_h, lay.ids, b["K"], b["V"], b["offs"], b["ids"], b["n"],
+                                      b["ws"], stream=stream)
+
+    def fwd(b):
+        wsf = b.setdefault("wsf", torch.empty(l3.l3_workspace_size(b["L"], T, l3.L3_PASS_FORWARD),
+                                              dtype=torch.uint8, device=dev))
+        l3.l3_forward(b["L"], b["ids"], lay.x, b["y"], wsf)
+
+    for k in range(max(2, args.warmup)):
+        stage(bufs[k % 2], s_main)
+        fwd(bufs[k % 2])
+    torch.cuda.synchronize()
+    if l3.l3_get_error(bufs[0]["ws"]) != 0 or int(bufs[0]["n"].item()) != U:
+        raise RuntimeError("staging reported an error")
+    steps = max(3, min(args.steps, 50))
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    st_ms, fw_ms = [], []
+    for _ in range(steps):
+        flush()
+        ev[0].record()
+        stage(bufs[0], s_main)
+        ev[1].record()
+        fwd(bufs[0])
+        ev[2].record()
+        torch.cuda.synchronize()
+        st_ms.append(ev[0].elapsed_time(ev[1]))
+        fw_ms.append(ev[1].elapsed_time(ev[2]))
+    # pipelined: stage batch k + 1 on the copy stream while batch k's forward runs
+    done = [torch.cuda.Event() for _ in range(2)]
+    staged = [torch.cuda.Event() for _ in range(2)]
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    stage(bufs[0], s_copy)
+    staged[0].record(s_copy)
+    torch.cuda.synchronize()
+    a.record()
+    for k in range(steps):
+        cur, nxt = bufs[k % 2], bufs[(k + 1) % 2]
+        s_copy.wait_event(done[(k + 1) % 2]) if k > 0 else None
+        stage(nxt, s_copy)
+        staged[(k + 1) % 2].record(s_copy)
+        s_main.wait_event(staged[k % 2])
+        fwd(cur)
+        done[k % 2].record(s_main)
+    b.record()
+    torch.cuda.synchronize()
+    pipe_ms = a.elapsed_time(b) / steps
+    staged_bytes = U * (p.d + p.d_v) * (2 if p.dtype == "bf16" else 4)
+    st = statistics.median(st_ms)
+    out = {"workload": config_block(p, T)["workload"] + ", tables in pinned host memory",
+           "stage_ms": st, "forward_ms": statistics.median(fw_ms),
+           "serial_ms_per_step": st + statistics.median(fw_ms),
+           "pipelined_ms_per_step": pipe_ms, "value": T / (pipe_ms / 1e3), "unit": "tokens/s",
+           "staged_bytes": staged_bytes, "host_link_gbs": staged_bytes / (st / 1e3) / 1e9,
+           "l2": "serial steps flushed before each step; pipelined steps back to back"}
+    del K_h, V_h, bufs, lay
+    torch.cuda.empty_cache()
+    return out
 
 
 def fwd_bwd_rate(l3, dev, args) -> dict:
@@ -655,6 +822,9 @@ def main(argv=None):
                     help="skip the decode and prefill workloads measured beside the headline")
     ap.add_argument("--e2e-steps", type=int, default=50,
                     help="timed steps of the host-buffer (end-to-end) leg")
+    ap.add_argument("--bwd-steps", type=int, default=20,
+                    help="timed steps of the forward + row-gradient backward leg")
+    ap.add_argument("--no-bwd", action="store_true", help="skip the forward + backward leg")
     ap.add_argument("--rows", type=int, default=None,
                     help="profiling: table rows v of a smaller table with the preset's shapes")
     ap.add_argument("--vocab", type=int, default=None, help="profiling: vocabulary size")

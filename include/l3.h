@@ -50,7 +50,8 @@ typedef enum l3_status {
   L3_ERR_INVALID_ARG = 1, /* null pointer, bad size or shape                          */
   L3_ERR_INFEASIBLE = 2,  /* allocation: vocab*n_min <= v <= vocab*n_max does not hold */
   L3_ERR_UNSUPPORTED = 3, /* shape outside what the kernels handle (see l3_layer)       */
-  L3_ERR_WORKSPACE = 4,   /* workspace smaller than l3_workspace_size                   */
+  L3_ERR_WORKSPACE = 4,   /* workspace smaller than l3_workspace_size, or (device-found)
+                             a row output smaller than the rows a batch touches           */
   L3_ERR_TOKEN_RANGE = 5, /* a token id was outside [0, vocab)          (device-found)  */
   L3_ERR_CUDA = 6,        /* a CUDA runtime call failed                                 */
   L3_ERR_LAYER = 7,       /* offsets not 0 = offs[0] < ... < offs[vocab] = v, or a range
@@ -91,7 +92,13 @@ typedef struct l3_layer {
 } l3_layer;
 
 /* Passes for l3_workspace_size. */
-enum { L3_PASS_FORWARD = 0, L3_PASS_BACKWARD = 1, L3_PASS_FORWARD_HOST = 2 };
+enum {
+  L3_PASS_FORWARD = 0,
+  L3_PASS_BACKWARD = 1,
+  L3_PASS_FORWARD_HOST = 2,
+  L3_PASS_BACKWARD_ROWS = 3,
+  L3_PASS_STAGE = 4
+};
 
 /* Stages of l3_forward, for l3_forward_timed. */
 enum {
@@ -254,10 +261,75 @@ l3_status l3_backward(const l3_layer* layer, const int32_t* ids, int64_t T, cons
                       l3_stream_t stream);
 
 /*
+ * Backward pass at batch scale for bf16 layers, with the table gradients of the rows the
+ * batch touches only (a dense dK/dV of a large table would be mostly zeros): the gradients
+ * of sum(dy * y) for the layer formula (explainer, "Core Architecture"), given the `saved`
+ * state of an l3_forward call on the same layer, ids and x. Batch sorting (explainer,
+ * "Systems-Friendly Design") makes each id's tokens one segment; each touched row's
+ * gradient is the sum over its id's segment, in batch order.
+ *   dy         [T, d]          bf16
+ *   dx         [T, d]          fp32 out
+ *   row_index  [max_rows]      int32 out: the touched table rows, ascending (the ranges
+ *                              offs[t] .. offs[t+1]-1 of the batch's distinct ids)
+ *   dK_rows    [max_rows, d]   fp32 out: row r holds dK of table row row_index[r]
+ *   dV_rows    [max_rows, d_v] fp32 out
+ *   n_rows     [1]             int32 out: touched rows (entries past it are unspecified)
+ *   max_rows   capacity of the row outputs; min(v, T * k_max) always suffices. If the batch
+ *              touches more rows, the rows past max_rows are not written and l3_get_error
+ *              reports L3_ERR_WORKSPACE.
+ *   dW_up      [d, d_v]        fp32 out;  dW_mix [d, 2d] fp32 out
+ * Arithmetic: every product accumulates in fp32 on tensor cores. u = W_up a is recomputed
+ * in fp32 (a split into bf16 hi + lo) with its LayerNorm statistics; du and da enter the
+ * products that lead to the softmax gradients as bf16 hi + lo, and the weights p and their
+ * gradients ds are fp32, entering the row-gradient products as bf16 hi + lo; h, x and dy
+ * enter the weight gradients as bf16. Every output is overwritten and the result is
+ * bitwise repeatable.
+ * The plain products with the weight matrices and the weight gradients run on cuBLASLt
+ * (its scratch inside `ws`); everything else runs in this library's kernels.
+ * ws: >= l3_workspace_size(layer, T, L3_PASS_BACKWARD_ROWS) bytes. fp32 layers:
+ * L3_ERR_UNSUPPORTED (l3_backward covers them).
+ */
+l3_status l3_backward_rows(const l3_layer* layer, const int32_t* ids, int64_t T, const void* x,
+                           const void* dy, const void* saved, float* dx, int32_t* row_index,
+                           float* dK_rows, float* dV_rows, int32_t* n_rows, int64_t max_rows,
+                           float* dW_up, float* dW_mix, void* ws, size_t ws_bytes,
+                           l3_stream_t stream);
+
+/*
+ * Staging of a batch's rows for tables kept in host memory (explainer, "Systems-Friendly
+ * Design": the tables may live in CPU memory; static routing tells from the token ids alone
+ * which rows a batch needs, so they can be fetched ahead, e.g. while earlier layers run).
+ * Copies the rows of the batch's distinct ids into compact device tables and describes them
+ * as a staged layer over which l3_forward gives the same outputs as over the full tables:
+ *   layer       the full layer; K and V may be pinned host memory the device can address
+ *               (cudaHostAlloc / cudaMallocHost, or cudaHostRegister'ed), or device memory;
+ *               offs, W_up, W_mix are device memory
+ *   ids         [T] int32 token ids of the batch (device), T >= 1
+ *   K_stage     [max_rows, d], V_stage [max_rows, d_v] (device, layer dtype) out: the
+ *               distinct ids' rows, in increasing id order
+ *   max_rows    capacity, T <= max_rows <= T * k_max; the batch's touched rows plus T always
+ *               suffice (the rows past the staged ones are given zeros, up to 128 of them).
+ *               If the batch touches more rows, l3_get_error reports L3_ERR_WORKSPACE and
+ *               the staged tables are incomplete.
+ *   offs_stage  [T + 1] int32 out (device): staged offsets (staged id s = the s-th distinct
+ *               id); ids_stage [T] int32 out (device): each token's staged id
+ *   n_rows      [1] int32 out (device): rows staged
+ *   staged      out (host struct): the staged layer: vocab T, v max_rows, offs offs_stage,
+ *               K K_stage, V V_stage, the rest as `layer`; only ids_stage's ids are valid
+ *               in it (the unused staged ids have one-row ranges past the staged rows)
+ * ws: >= l3_workspace_size(layer, T, L3_PASS_STAGE) bytes. Asynchronous on `stream`.
+ * Errors: L3_ERR_INVALID_ARG (also pageable host tables), L3_ERR_WORKSPACE, L3_ERR_CUDA.
+ */
+l3_status l3_stage_rows(const l3_layer* layer, const int32_t* ids, int64_t T, void* K_stage,
+                        void* V_stage, int64_t max_rows, int32_t* offs_stage, int32_t* ids_stage,
+                        int32_t* n_rows, l3_layer* staged, void* ws, size_t ws_bytes,
+                        l3_stream_t stream);
+
+/*
  * Synchronise `stream`, then read and clear the status words that the kernels of the
  * most recent call on `ws` wrote there. Returns L3_OK, L3_ERR_TOKEN_RANGE, L3_ERR_LAYER,
- * L3_ERR_TIMEOUT or L3_ERR_CUDA (the first that applies, in that order of priority
- * after L3_ERR_CUDA).
+ * L3_ERR_TIMEOUT, L3_ERR_WORKSPACE or L3_ERR_CUDA (the first that applies, in that order
+ * of priority after L3_ERR_CUDA).
  */
 l3_status l3_get_error(void* ws, l3_stream_t stream);
 

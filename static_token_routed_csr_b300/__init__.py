@@ -16,7 +16,8 @@ import numpy as np
 
 __all__ = [
     "L3Error", "L3Layer", "lib", "make_layer", "L3_F32", "L3_BF16",
-    "L3_PASS_FORWARD", "L3_PASS_BACKWARD", "L3_PASS_FORWARD_HOST", "L3_FWD_STAGES",
+    "L3_PASS_FORWARD", "L3_PASS_BACKWARD", "L3_PASS_FORWARD_HOST", "L3_PASS_BACKWARD_ROWS",
+    "L3_FWD_STAGES", "l3_backward_rows", "l3_stage_rows", "L3_PASS_STAGE",
     "STAGE_NAMES", "l3_alloc_offsets", "l3_workspace_size", "l3_saved_size",
     "l3_check_layer", "l3_route", "l3_route_noalloc", "l3_forward", "l3_forward_timed", "l3_forward_host",
     "l3_backward", "l3_get_error", "l3_status_string", "l3_launch_count", "l3_abi_version",
@@ -26,7 +27,8 @@ __all__ = [
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libl3.so")
 
 L3_F32, L3_BF16 = 0, 1
-L3_PASS_FORWARD, L3_PASS_BACKWARD, L3_PASS_FORWARD_HOST = 0, 1, 2
+L3_PASS_FORWARD, L3_PASS_BACKWARD, L3_PASS_FORWARD_HOST, L3_PASS_BACKWARD_ROWS = 0, 1, 2, 3
+L3_PASS_STAGE = 4
 L3_FWD_STAGES = 5
 STAGE_NAMES = ("route", "attend", "attend_long", "up", "mix")
 STATUS = {0: "L3_OK", 1: "L3_ERR_INVALID_ARG", 2: "L3_ERR_INFEASIBLE", 3: "L3_ERR_UNSUPPORTED",
@@ -65,6 +67,9 @@ _SIGNATURES = {
     "l3_forward_timed": (_I32, [_LP, _P, _I64, _P, _P, _I32, _P, _P, _SZ, _P, _P]),
     "l3_forward_host": (_I32, [_LP, _P, _I64, _P, _P, _I32, _P, _SZ, _P]),
     "l3_backward": (_I32, [_LP, _P, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "l3_backward_rows": (_I32, [_LP, _P, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _P, _P, _P,
+                                _SZ, _P]),
+    "l3_stage_rows": (_I32, [_LP, _P, _I64, _P, _P, _I64, _P, _P, _P, _LP, _P, _SZ, _P]),
     "l3_get_error": (_I32, [_P, _P]),
     "l3_status_string": (ctypes.c_char_p, [_I32]),
     "l3_launch_count": (ctypes.c_uint64, []),
@@ -229,6 +234,29 @@ def l3_backward(layer: L3Layer, ids, x, dy, saved, dx, dK, dV, dW_up, dW_mix, ws
                              _ptr(saved), _ptr(dx), _ptr(dK), _ptr(dV), _ptr(dW_up),
                              _ptr(dW_mix), _ptr(ws), ws.numel() * ws.element_size(),
                              _stream(stream)), "l3_backward")
+
+
+def l3_backward_rows(layer: L3Layer, ids, x, dy, saved, dx, row_index, dK_rows, dV_rows, n_rows,
+                     dW_up, dW_mix, ws, stream=None) -> None:
+    """Row-gradient backward (bf16 layers); the row outputs' capacity is row_index.numel()."""
+    _check(lib().l3_backward_rows(ctypes.byref(layer), _ptr(ids), ids.numel(), _ptr(x), _ptr(dy),
+                                  _ptr(saved), _ptr(dx), _ptr(row_index), _ptr(dK_rows),
+                                  _ptr(dV_rows), _ptr(n_rows), row_index.numel(), _ptr(dW_up),
+                                  _ptr(dW_mix), _ptr(ws), ws.numel() * ws.element_size(),
+                                  _stream(stream)), "l3_backward_rows")
+
+
+def l3_stage_rows(layer: L3Layer, ids, K_stage, V_stage, offs_stage, ids_stage, n_rows, ws,
+                  stream=None) -> L3Layer:
+    """Stage the batch's rows of host-resident tables into K_stage / V_stage (device); returns
+    the staged layer (its capacity is K_stage.shape[0])."""
+    staged = L3Layer()
+    _check(lib().l3_stage_rows(ctypes.byref(layer), _ptr(ids), ids.numel(), _ptr(K_stage),
+                               _ptr(V_stage), K_stage.shape[0], _ptr(offs_stage), _ptr(ids_stage),
+                               _ptr(n_rows), ctypes.byref(staged), _ptr(ws),
+                               ws.numel() * ws.element_size(), _stream(stream)), "l3_stage_rows")
+    staged._keep = (getattr(layer, "_keep", None), K_stage, V_stage, offs_stage)
+    return staged
 
 
 def l3_get_error(ws, stream=None) -> int:

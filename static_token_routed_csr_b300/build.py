@@ -3,7 +3,7 @@
 Usage: ``python -m static_token_routed_csr_b300.build [--force] [--debug]``. Every ``.cu``
 under ``csrc/`` is compiled by nvcc for ``sm_103a`` only, every ``.cpp`` by g++ (with
 ``-ffp-contract=off`` so host arithmetic is not fused), and the objects are linked into
-one shared library against the CUDA runtime. Objects are rebuilt when a source or header
+one shared library against the CUDA runtime and cuBLASLt (the backward's plain GEMMs). Objects are rebuilt when a source or header
 is newer than them.
 """
 from __future__ import annotations
@@ -81,7 +81,7 @@ def build(force: bool = False, debug: bool = False, verbose: bool = False) -> st
             logs = list(ex.map(_run, jobs))
     if jobs or not os.path.exists(LIB) or force:
         libdir = os.path.join(cuda, "lib64")
-        _run([nvcc, *ARCH, "-shared", "-o", LIB, *objs, "-L", libdir, "-lcudart",
+        _run([nvcc, *ARCH, "-shared", "-o", LIB, *objs, "-L", libdir, "-lcudart", "-lcublasLt",
               "-Xlinker", "-rpath", "-Xlinker", libdir])
     if verbose:
         for lg in logs:

@@ -60,6 +60,8 @@ struct FwdWs {
   int32_t* counters;
   int32_t* cta_start;  // the plan's split of the chunk list over the split-row kernel's CTAs
   int32_t* cta_group;
+  CtaHead* cta_head;
+  AttendCut* cuts;
   int n_cta;
   AttendItem* items;
   float* a_f32;
@@ -99,6 +101,8 @@ FwdWs carve_fwd(Carve& c, const l3_layer* L, int64_t T) {
   w.n_cta = attend_split_ctas(int(d), int(dv), L->dtype);
   w.cta_start = c.take<int32_t>(size_t(kPlanMaxCtas) + 1);
   w.cta_group = c.take<int32_t>(size_t(kPlanMaxCtas));
+  w.cta_head = c.take<CtaHead>(size_t(kPlanMaxCtas));
+  w.cuts = c.take<AttendCut>(size_t(kPlanMaxCtas));
   w.tc_th = attend_tc_threshold(T, int(d), int(dv), L->dtype);
   if (w.tc_th > 0) {
     w.max_items = int(T / w.tc_th + 1);
@@ -162,6 +166,51 @@ BwdWs carve_bwd(Carve& c, const l3_layer* L, int64_t T) {
   return w;
 }
 
+struct BwdRowsWs {
+  DevStatus* st;
+  void* route_scratch;
+  int32_t *seg_start, *n_seg;
+  AttendGroup* groups;
+  int32_t* hdr;
+  int32_t* counters;
+  __nv_bfloat16 *a_hi, *a_lo, *h16, *du_hi, *du_lo, *x_sorted, *da_sorted, *da16, *da16_lo;
+  float *U32, *rstd, *dh, *da, *delta, *p_buf, *ds_buf;
+  int32_t *seg_row0, *seg_unit0;
+  void* lt_ws;
+};
+
+BwdRowsWs carve_bwd_rows(Carve& c, const l3_layer* L, int64_t T) {
+  BwdRowsWs w{};
+  const size_t t = size_t(T), d = size_t(L->d), dv = size_t(L->d_v), km = size_t(L->k_max);
+  w.st = c.take<DevStatus>(1);
+  w.route_scratch = c.raw(route_scratch_bytes(T));
+  w.seg_start = c.take<int32_t>(t + 1);
+  w.n_seg = c.take<int32_t>(1);
+  w.groups = c.take<AttendGroup>(t + 1);
+  w.hdr = c.take<int32_t>(kPlanHdrWords);
+  w.counters = c.take<int32_t>(t + 1);
+  w.a_hi = c.take<__nv_bfloat16>(t * dv);
+  w.a_lo = c.take<__nv_bfloat16>(t * dv);
+  w.h16 = c.take<__nv_bfloat16>(t * d);
+  w.du_hi = c.take<__nv_bfloat16>(t * d);
+  w.du_lo = c.take<__nv_bfloat16>(t * d);
+  w.x_sorted = c.take<__nv_bfloat16>(t * d);
+  w.da_sorted = c.take<__nv_bfloat16>(t * dv);
+  w.da16 = c.take<__nv_bfloat16>(t * dv);
+  w.da16_lo = c.take<__nv_bfloat16>(t * dv);
+  w.U32 = c.take<float>(t * d);
+  w.rstd = c.take<float>(t);
+  w.dh = c.take<float>(t * d);
+  w.da = c.take<float>(t * dv);
+  w.delta = c.take<float>(t);
+  w.p_buf = c.take<float>(t * km);
+  w.ds_buf = c.take<float>(t * km);
+  w.seg_row0 = c.take<int32_t>(t + 1);
+  w.seg_unit0 = c.take<int32_t>(t + 1);
+  w.lt_ws = c.raw(kLtWorkspace);
+  return w;
+}
+
 #define L3_CUDA(call)                      \
   do {                                     \
     if ((call) != cudaSuccess) {           \
@@ -222,7 +271,7 @@ l3_status forward_impl(const l3_layer* L, const int32_t* ids, int64_t T, const v
   const int ch = attend_rows_per_chunk(d, dv, L->dtype);
   PlanOut plan{w.groups, w.plan_hdr, w.counters, w.items, L->offs, L->v, L->k_max, ch,
                attend_group_tokens(L->dtype), w.tc_th > 0 ? w.tc_th : INT32_MAX,
-               w.cta_start, w.cta_group, w.n_cta, 0, 0};
+               w.cta_start, w.cta_group, w.cta_head, w.n_cta, 0, 0};
   attend_split_weights(d, dv, L->dtype, &plan.w_chunk, &plan.w_group);
   L3_CUDA(launch_route(ids, T, L->vocab, w.route_scratch,
                        RouteOut{w.perm, w.seg_start, w.seg_id, w.n_seg}, w.st, s, &keys, &plan));
@@ -251,6 +300,8 @@ l3_status forward_impl(const l3_layer* L, const int32_t* ids, int64_t T, const v
     aa.part = w.part;
     aa.cta_start = w.cta_start;
     aa.cta_group = w.cta_group;
+    aa.cta_head = w.cta_head;
+    aa.cuts = w.cuts;
     aa.n_cta = w.n_cta;
     aa.st = w.st;
     L3_CUDA(launch_attend_fwd(aa, s));
@@ -409,6 +460,13 @@ size_t l3_workspace_size(const l3_layer* L, int64_t T, int32_t pass) {
     }
   } else if (pass == L3_PASS_BACKWARD) {
     carve_bwd(c, L, T);
+  } else if (pass == L3_PASS_BACKWARD_ROWS) {
+    carve_bwd_rows(c, L, T);
+  } else if (pass == L3_PASS_STAGE) {
+    c.take<DevStatus>(1);
+    c.raw(route_scratch_bytes(T));
+    for (int k = 0; k < 3; ++k) c.take<int32_t>(size_t(T) + 1);
+    c.take<int32_t>(1);
   } else {
     return 0;
   }
@@ -674,6 +732,213 @@ l3_status l3_count_ids(const int32_t* ids, int64_t n, int64_t vocab, int64_t* co
   return L3_OK;
 }
 
+l3_status l3_backward_rows(const l3_layer* L, const int32_t* ids, int64_t T, const void* x,
+                           const void* dy, const void* saved, float* dx, int32_t* row_index,
+                           float* dK_rows, float* dV_rows, int32_t* n_rows, int64_t max_rows,
+                           float* dW_up, float* dW_mix, void* ws, size_t ws_bytes,
+                           l3_stream_t stream) {
+  l3_status e = check_layer_args(L);
+  if (e != L3_OK) return e;
+  if (L->dtype != L3_BF16) return L3_ERR_UNSUPPORTED;
+  if (T < 0 || T >= (int64_t(1) << 31) || max_rows < 0) return L3_ERR_INVALID_ARG;
+  if (!dW_up || !dW_mix || !n_rows || !ws) return L3_ERR_INVALID_ARG;
+  if (T > 0 && (!ids || !x || !dy || !saved || !dx || !row_index || !dK_rows || !dV_rows))
+    return L3_ERR_INVALID_ARG;
+  if (ws_bytes < l3_workspace_size(L, T, L3_PASS_BACKWARD_ROWS)) return L3_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int d = int(L->d), dv = int(L->d_v);
+  Carve c(ws);
+  BwdRowsWs w = carve_bwd_rows(c, L, T);
+  L3_CUDA(cudaMemsetAsync(w.st, 0, sizeof(DevStatus), s));
+  if (T == 0) {
+    L3_CUDA(cudaMemsetAsync(dW_up, 0, size_t(d) * size_t(dv) * 4, s));
+    L3_CUDA(cudaMemsetAsync(dW_mix, 0, size_t(d) * size_t(2 * d) * 4, s));
+    L3_CUDA(cudaMemsetAsync(n_rows, 0, 4, s));
+    return L3_OK;
+  }
+  Carve cs(const_cast<void*>(saved));
+  const Saved sv = carve_saved(cs, L, T);
+  const int ch = attend_bwd_rows_per_chunk(d, dv);
+  // batch sorting and the token groups (every segment in groups of at most 8 tokens)
+  PlanOut plan{w.groups, w.hdr, w.counters, nullptr, L->offs, L->v, L->k_max, ch, kPlanMT,
+               INT32_MAX, nullptr, nullptr, nullptr, 0, 1, 0};
+  const uint64_t* keys = nullptr;
+  L3_CUDA(launch_route(ids, T, L->vocab, w.route_scratch,
+                       RouteOut{nullptr, w.seg_start, nullptr, w.n_seg}, w.st, s, &keys, &plan));
+  const int Ti = int(T);
+  auto gemm = [&](int m, int n, int k, bool ta, bool tb, const void* A, int64_t lda, const void* B,
+                  int64_t ldb, void* C, int64_t ldc, bool c16, bool acc) {
+    return lt_gemm(LtGemm{m, n, k, ta, tb, A, lda, B, ldb, C, ldc, c16, acc}, w.lt_ws,
+                   kLtWorkspace, s);
+  };
+  BwdSmallArgs sa{};
+  sa.T = T;
+  sa.d = d;
+  sa.d_v = dv;
+  sa.eps = L->ln_eps;
+  // u = W_up a in fp32 from a as bf16 hi + lo, and h = LayerNorm(u) (fp32 and bf16)
+  sa.stage = 3;
+  sa.a = sv.a;
+  sa.a_hi = w.a_hi;
+  sa.a_lo = w.a_lo;
+  L3_CUDA(launch_bwd_small(sa, s));
+  L3_CUDA(gemm(d, Ti, dv, true, false, L->W_up, dv, w.a_hi, dv, w.U32, d, false, false));
+  L3_CUDA(gemm(d, Ti, dv, true, false, L->W_up, dv, w.a_lo, dv, w.U32, d, false, true));
+  sa.stage = 0;
+  sa.U32 = w.U32;
+  sa.h16 = w.h16;
+  sa.rstd_out = w.rstd;
+  L3_CUDA(launch_bwd_small(sa, s));
+  // dW_mix = dyᵀ [h x]
+  L3_CUDA(gemm(d, d, Ti, false, true, w.h16, d, dy, d, dW_mix, 2 * d, false, false));
+  L3_CUDA(gemm(d, d, Ti, false, true, x, d, dy, d, dW_mix + d, 2 * d, false, false));
+  // dh = dy W_mix[:, :d] and the direct term dx = dy W_mix[:, d:]
+  L3_CUDA(gemm(d, Ti, d, false, false, L->W_mix, 2 * d, dy, d, w.dh, d, false, false));
+  L3_CUDA(gemm(d, Ti, d, false, false, static_cast<const __nv_bfloat16*>(L->W_mix) + d, 2 * d, dy,
+               d, dx, d, false, false));
+  // du = LayerNorm backward (bf16 hi + lo); dW_up = duᵀ a; da = du W_up from both parts
+  sa.stage = 1;
+  sa.dh = w.dh;
+  sa.du = w.du_hi;
+  sa.du_lo = w.du_lo;
+  L3_CUDA(launch_bwd_small(sa, s));
+  L3_CUDA(gemm(dv, d, Ti, false, true, w.a_hi, dv, w.du_hi, d, dW_up, dv, false, false));
+  L3_CUDA(gemm(dv, Ti, d, false, false, L->W_up, dv, w.du_hi, d, w.da, dv, false, false));
+  L3_CUDA(gemm(dv, Ti, d, false, false, L->W_up, dv, w.du_lo, d, w.da, dv, false, true));
+  // x and da in sorted order, da as bf16 hi + lo, delta = a . da
+  sa.stage = 2;
+  sa.keys = keys;
+  sa.x = static_cast<const __nv_bfloat16*>(x);
+  sa.da = w.da;
+  sa.x_sorted = w.x_sorted;
+  sa.da_sorted = w.da_sorted;
+  sa.da16 = w.da16;
+  sa.da16_lo = w.da16_lo;
+  sa.delta = w.delta;
+  L3_CUDA(launch_bwd_small(sa, s));
+  // Phase A: p, ds per token and row; dx += sum_j ds_j K_j
+  AttendBwdRowsArgs ab{};
+  ab.sorted_keys = keys;
+  ab.T = T;
+  ab.groups = w.groups;
+  ab.hdr = w.hdr;
+  ab.K = L->K;
+  ab.V = L->V;
+  ab.v = L->v;
+  ab.d = d;
+  ab.d_v = dv;
+  ab.ch = ch;
+  ab.k_max = L->k_max;
+  ab.x = static_cast<const __nv_bfloat16*>(x);
+  ab.da16 = w.da16;
+  ab.da16_lo = w.da16_lo;
+  ab.ml = sv.ml;
+  ab.delta = w.delta;
+  ab.dx = dx;
+  ab.p_buf = w.p_buf;
+  ab.ds_buf = w.ds_buf;
+  ab.n_cta = device_sm_count();
+  ab.st = w.st;
+  L3_CUDA(launch_attend_bwd_rows(ab, s));
+  // Phase B: the touched rows' dK and dV, in segment order
+  L3_CUDA(launch_row_plan(keys, w.seg_start, w.n_seg, L->offs, d, dv, w.seg_row0, w.seg_unit0,
+                          n_rows, max_rows, w.st, s));
+  SegRowsArgs sr{};
+  sr.sorted_keys = keys;
+  sr.seg_start = w.seg_start;
+  sr.n_seg = w.n_seg;
+  sr.offs = L->offs;
+  sr.seg_row0 = w.seg_row0;
+  sr.seg_unit0 = w.seg_unit0;
+  sr.x_sorted = w.x_sorted;
+  sr.da_sorted = w.da_sorted;
+  sr.p_buf = w.p_buf;
+  sr.ds_buf = w.ds_buf;
+  sr.k_max = L->k_max;
+  sr.d = d;
+  sr.d_v = dv;
+  sr.row_index = row_index;
+  sr.dK_rows = dK_rows;
+  sr.dV_rows = dV_rows;
+  sr.max_rows = max_rows;
+  sr.st = w.st;
+  L3_CUDA(launch_seg_rows(sr, s));
+  return L3_OK;
+}
+
+l3_status l3_stage_rows(const l3_layer* L, const int32_t* ids, int64_t T, void* K_stage,
+                        void* V_stage, int64_t max_rows, int32_t* offs_stage, int32_t* ids_stage,
+                        int32_t* n_rows, l3_layer* staged, void* ws, size_t ws_bytes,
+                        l3_stream_t stream) {
+  l3_status e = check_layer_args(L);
+  if (e != L3_OK) return e;
+  if (T < 1 || T >= (int64_t(1) << 31) || !ids || !K_stage || !V_stage || !offs_stage ||
+      !ids_stage || !n_rows || !staged || !ws)
+    return L3_ERR_INVALID_ARG;
+  // the staged layer has vocabulary T and max_rows rows
+  if (max_rows < T || max_rows > T * int64_t(L->k_max) || max_rows >= (int64_t(1) << 31))
+    return L3_ERR_INVALID_ARG;
+  if (ws_bytes < l3_workspace_size(L, T, L3_PASS_STAGE)) return L3_ERR_WORKSPACE;
+  // the tables may be pinned host memory (read through its device-mapped address) or
+  // device memory
+  const void* src[2] = {L->K, L->V};
+  const void* dev_src[2] = {nullptr, nullptr};
+  for (int k = 0; k < 2; ++k) {
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, src[k]) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return L3_ERR_INVALID_ARG;
+    }
+    if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged)
+      dev_src[k] = src[k];
+    else if (at.type == cudaMemoryTypeHost && at.devicePointer)
+      dev_src[k] = at.devicePointer;
+    else
+      return L3_ERR_INVALID_ARG;  // pageable host memory: the device cannot read it
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  Carve c(ws);
+  DevStatus* st = c.take<DevStatus>(1);
+  void* route_scratch = c.raw(route_scratch_bytes(T));
+  int32_t* seg_start = c.take<int32_t>(size_t(T) + 1);
+  int32_t* n_seg = c.take<int32_t>(1);
+  int32_t* seg_row0 = c.take<int32_t>(size_t(T) + 1);
+  int32_t* seg_unit0 = c.take<int32_t>(size_t(T) + 1);
+  L3_CUDA(cudaMemsetAsync(st, 0, sizeof(DevStatus), s));
+  const uint64_t* keys = nullptr;
+  L3_CUDA(launch_route(ids, T, L->vocab, route_scratch, RouteOut{nullptr, seg_start, nullptr, n_seg},
+                       st, s, &keys));
+  L3_CUDA(launch_row_plan(keys, seg_start, n_seg, L->offs, int(L->d), int(L->d_v), seg_row0,
+                          seg_unit0, n_rows, max_rows, st, s));
+  const size_t es = L->dtype == L3_BF16 ? 2 : 4;
+  StageArgs sa{};
+  sa.sorted_keys = keys;
+  sa.seg_start = seg_start;
+  sa.n_seg = n_seg;
+  sa.offs = L->offs;
+  sa.seg_row0 = seg_row0;
+  sa.n_rows = n_rows;
+  sa.K_host = dev_src[0];
+  sa.V_host = dev_src[1];
+  sa.k_row_bytes = L->d * int64_t(es);
+  sa.v_row_bytes = L->d_v * int64_t(es);
+  sa.K_st = K_stage;
+  sa.V_st = V_stage;
+  sa.max_rows = max_rows;
+  sa.offs_st = offs_stage;
+  sa.ids_st = ids_stage;
+  sa.T = T;
+  sa.st = st;
+  L3_CUDA(launch_stage_rows(sa, s));
+  *staged = *L;
+  staged->vocab = T;
+  staged->v = max_rows;
+  staged->offs = offs_stage;
+  staged->K = K_stage;
+  staged->V = V_stage;
+  return L3_OK;
+}
+
 l3_status l3_get_error(void* ws, l3_stream_t stream) {
   if (!ws) return L3_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -684,6 +949,7 @@ l3_status l3_get_error(void* ws, l3_stream_t stream) {
   if (h.token_range) return L3_ERR_TOKEN_RANGE;
   if (h.layer_bad) return L3_ERR_LAYER;
   if (h.timeout) return L3_ERR_TIMEOUT;
+  if (h.capacity) return L3_ERR_WORKSPACE;
   return L3_OK;
 }
 

@@ -40,12 +40,14 @@
 #include <mutex>
 
 #include "l3_attend_split.cuh"
+#include "l3_mma.cuh"
 
 namespace l3 {
 
 namespace {
 
 using namespace split;
+using namespace wmma;
 
 constexpr int kWarps = kThreads / 32;       // consumer warps (scores, softmax, values)
 constexpr int kCtaThreads = kThreads + 32;  // + one producer warp (TMA copies)
@@ -98,73 +100,6 @@ MmaShape mma_shape(int d, int d_v) {
   return s;
 }
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                        uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];"
-               : "=r"(r0), "=r"(r1)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                          uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x2_t(uint32_t addr, uint32_t& r0, uint32_t& r1) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];"
-               : "=r"(r0), "=r"(r1)
-               : "r"(addr));
-}
-
-// D (16x8 fp32) += A (16x16 bf16, row) B (16x8 bf16, col)
-__device__ __forceinline__ void mma16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                      uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-      "{%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-// D (16x8 fp32) += A (16x8 bf16, row) B (8x8 bf16, col)
-__device__ __forceinline__ void mma8(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5}, {%6}, "
-      "{%0, %1, %2, %3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(b0));
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  return uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
-         (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
-}
-// hi = bf16(v), lo = bf16(v - hi), packed in pairs (lower k in the low half).
-__device__ __forceinline__ void split_pair(float v0, float v1, uint32_t& hi, uint32_t& lo) {
-  const float h0 = __bfloat162float(__float2bfloat16_rn(v0));
-  const float h1 = __bfloat162float(__float2bfloat16_rn(v1));
-  hi = pack_bf16(h0, h1);
-  lo = pack_bf16(v0 - h0, v1 - h1);
-}
-
-// Byte offset of (row, column) in a block of `rows` rows laid out as [col / 64][row][64]
-// with the 128-byte swizzle (16-byte piece index XOR row % 8); the block is 1024-aligned.
-__device__ __forceinline__ uint32_t sw128(int rows, int row, int col) {
-  return uint32_t((col >> 6) * rows * 128 + row * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4));
-}
-
-__device__ __forceinline__ void tma_load_3d(const CUtensorMap* map, uint64_t* bar, uint32_t dst,
-                                            int32_t x, int32_t y, int32_t z) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(tc::smem_u32(bar)), "r"(x), "r"(y), "r"(z)
-      : "memory");
-}
 
 // Barrier of the kThreads consumer threads (named barrier 1; the producer warp is not in it).
 __device__ __forceinline__ void cbar() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
@@ -220,15 +155,37 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
   if (warp == kWarps) {
     // The plan's group list is read 32 groups at a time (lane l holds group w0 + l) and the
     // current group's fields are taken from the window by shuffles.
+    const uint32_t tx = uint32_t(CH) * 2u * uint32_t(d + dv);
+    // The range's first group comes from the plan's head for this CTA (one 64-byte read):
+    // the copies of its first chunks go out at once; the group list is read meanwhile.
+    const int hv = lane < 16 ? reinterpret_cast<const int32_t*>(&a.cta_head[b])[lane] : 0;
+    int pg = __shfl_sync(0xffffffffu, hv, 0);
+    int g_q0 = __shfl_sync(0xffffffffu, hv, 1), g_mt = __shfl_sync(0xffffffffu, hv, 2);
+    int g_n = __shfl_sync(0xffffffffu, hv, 3), g_row0 = __shfl_sync(0xffffffffu, hv, 4);
+    int g_c0 = __shfl_sync(0xffffffffu, hv, 5);
+    int64_t p_next = __shfl_sync(0xffffffffu, hv, 6);
+    const int r_first = __shfl_sync(0xffffffffu, hv, 7);
+    int ptok = __shfl_sync(0xffffffffu, hv, 8 + (lane & 7));  // lane j < 8: token j
+    int early = int(p_next - cb);
+    early = early < S ? early : S;
+    early = early < nk ? early : nk;
+    if (lane == 0) {
+      for (int e = 0; e < early; ++e) {
+        const uint32_t st = ring_s + uint32_t(e * sh.stage_bytes);
+        tc::mbar_arrive_expect_tx(&ms->full[e], tx);
+        tma_load_3d(&mapK, &ms->full[e], st, 0, r_first + e * CH, 0);
+        tma_load_3d(&mapV, &ms->full[e], st + uint32_t(sh.k_bytes), 0, r_first + e * CH, 0);
+      }
+    }
+    // The plan's group list is read 32 groups at a time (lane l holds group w0 + l) and the
+    // fields of later groups are taken from the window by shuffles.
     const int n_groups = a.hdr[kPlanGroups];
-    int w0 = a.cta_group[b];
+    int w0 = pg;
     AttendGroup wg{};
     auto load_window = [&]() {
       if (w0 + lane <= n_groups) wg = groups[w0 + lane];
     };
-    load_window();
-    int pg = w0, g_q0 = 0, g_mt = 0, g_n = 0, g_row0 = 0, g_c0 = 0, ptok = 0;
-    int64_t p_next = 0;
+    load_window();  // first used when the producer moves past the first group
     auto take = [&]() {  // fields of group pg; pg and pg + 1 lie in the window
       const int src = pg - w0;
       g_q0 = __shfl_sync(0xffffffffu, wg.q0, src);
@@ -243,8 +200,6 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
         if (lane == j) ptok = v;
       }
     };
-    take();
-    const uint32_t tx = uint32_t(CH) * 2u * uint32_t(d + dv);
     auto prefetch_x = [&]() {
       for (int j = 0; j < g_mt; ++j) {
         const char* row = reinterpret_cast<const char*>(
@@ -289,11 +244,13 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
       __syncwarp();
       if (lane == 0) {
         tc::mbar_arrive(&ms->meta_full[s]);
-        const int r0 = g_row0 + int(c - g_c0) * CH;
-        const uint32_t st = ring_s + uint32_t(s * sh.stage_bytes);
-        tc::mbar_arrive_expect_tx(&ms->full[s], tx);
-        tma_load_3d(&mapK, &ms->full[s], st, 0, r0, 0);
-        tma_load_3d(&mapV, &ms->full[s], st + uint32_t(sh.k_bytes), 0, r0, 0);
+        if (issued >= early) {  // (the first `early` chunks' copies are in flight)
+          const int r0 = g_row0 + int(c - g_c0) * CH;
+          const uint32_t st = ring_s + uint32_t(s * sh.stage_bytes);
+          tc::mbar_arrive_expect_tx(&ms->full[s], tx);
+          tma_load_3d(&mapK, &ms->full[s], st, 0, r0, 0);
+          tma_load_3d(&mapV, &ms->full[s], st + uint32_t(sh.k_bytes), 0, r0, 0);
+        }
       }
       if (fresh) prefetch_x();
     }
@@ -321,6 +278,7 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
   int64_t i0 = 0, i1 = 0, itid = 0;
   bool ok = true;
 
+  bool cut_set = false;  // (thread 0) this CTA left a group to the combine kernel
   auto finish = [&](int par) {
     const int64_t c0 = gc0, c1 = c_next;
     const bool whole = c0 >= cb && c1 <= ce;
@@ -367,7 +325,11 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
       pe[0] = ms->m_run[par][tid];
       pe[1] = ms->l_run[par][tid];
     }
-    arrive_and_merge(a, cg, c0, c1, cb, ce, q0, mt, &ms->merge, tid, kThreads, [] { cbar(); });
+    // a group that starts here and runs past the range is merged by the combine kernel
+    if (tid == 0 && c0 >= cb && c1 > ce) {
+      a.cuts[b] = AttendCut{cg, q0, mt, second ? 1 : 0, c0, c1};
+      cut_set = true;
+    }
   };
 
   // A consumer step takes one chunk, or two consecutive chunks of the same group (stages k
@@ -581,9 +543,71 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
   }
 
   if (ok && cg >= 0) finish(u & 1);
+  if (tid == 0 && !cut_set) a.cuts[b] = AttendCut{-1, 0, 0, 0, 0, 0};
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+// Merges the partials of the groups the split-row kernel's CTAs cut: CTA b takes the group
+// that starts in split-row CTA b's range and runs past it, if there is one. Its holders are
+// b and the CTAs after it whose (non-empty) ranges start before the group's end; the
+// partials are merged in CTA order, as the in-kernel merge does, so results are identical.
+constexpr int kCombineThreads = 256;
+__global__ void __launch_bounds__(kCombineThreads) attend_combine_kernel(const AttendArgs a) {
+  __shared__ MergeSmem sm;
+  grid_dep_wait();  // the split-row kernel's partials are complete
+  grid_dep_release();
+  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
+  const int32_t* cs = a.cta_start;
+  if (cs[b] >= cs[b + 1]) return;
+  const AttendCut cut = a.cuts[b];
+  if (cut.g < 0) return;
+  if (tid < 32) {
+    int nh = 1;
+    for (int base = b + 1;; base += 32) {
+      const int bb = base + lane;
+      const bool inside = bb < a.n_cta;
+      const bool ne = inside && cs[bb] < cs[bb + 1];
+      const bool holds = ne && cs[bb] < cut.c1;
+      const unsigned m_hold = __ballot_sync(0xffffffffu, holds);
+      const unsigned m_stop = __ballot_sync(0xffffffffu, !inside || (ne && cs[bb] >= cut.c1));
+      // holders come before the first non-empty range past the group
+      const unsigned take = m_stop ? m_hold & ((1u << (__ffs(m_stop) - 1)) - 1u) : m_hold;
+      if ((take >> lane) & 1u) {
+        const int k = nh + __popc(take & ((1u << lane) - 1u));
+        if (k < kMergeCap) sm.hold[k] = bb;
+      }
+      nh += __popc(take);
+      if (m_stop) break;
+    }
+    if (lane == 0) {
+      sm.hold[0] = b;
+      sm.nh = nh < kMergeCap ? nh : kMergeCap;
+      sm.first_second = cut.second;
+    }
+  }
+  merge_held(a, cut.q0, cut.mt, &sm, tid, kCombineThreads, [] { __syncthreads(); });
+}
+
+template <int CH, int KSW, int MTW>
+cudaError_t launch_ch(const AttendArgs& a, const MmaShape& sh, cudaStream_t stream) {
+  CUtensorMap mk, mv;
+  if (!make_row_block_map(&mk, a.K, a.v, a.d, CH) || !make_row_block_map(&mv, a.V, a.v, a.d_v, CH))
+    return cudaErrorInvalidValue;
+  const cudaError_t attr = ensure_smem_attr(attend_mma_kernel<CH, KSW, MTW>, kSmemLimit);
+  if (attr != cudaSuccess) return attr;
+  if (a.n_cta < 1 || a.n_cta > kMaxCtas) return cudaErrorInvalidValue;
+  cudaError_t e = launch_pdl(attend_mma_kernel<CH, KSW, MTW>, dim3(a.n_cta), dim3(kCtaThreads),
+                             size_t(sh.smem), stream, mk, mv, a, sh);
+  count_launch();
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(attend_combine_kernel, dim3(a.n_cta), dim3(kCombineThreads), 0, stream, a);
+  count_launch();
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+}  // namespace
+
+namespace wmma {
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
@@ -612,21 +636,7 @@ bool make_row_block_map(CUtensorMap* map, const void* base, int64_t rows, int64_
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int CH, int KSW, int MTW>
-cudaError_t launch_ch(const AttendArgs& a, const MmaShape& sh, cudaStream_t stream) {
-  CUtensorMap mk, mv;
-  if (!make_row_block_map(&mk, a.K, a.v, a.d, CH) || !make_row_block_map(&mv, a.V, a.v, a.d_v, CH))
-    return cudaErrorInvalidValue;
-  const cudaError_t attr = ensure_smem_attr(attend_mma_kernel<CH, KSW, MTW>, kSmemLimit);
-  if (attr != cudaSuccess) return attr;
-  if (a.n_cta < 1 || a.n_cta > kMaxCtas) return cudaErrorInvalidValue;
-  const cudaError_t e = launch_pdl(attend_mma_kernel<CH, KSW, MTW>, dim3(a.n_cta),
-                                   dim3(kCtaThreads), size_t(sh.smem), stream, mk, mv, a, sh);
-  count_launch();
-  return e != cudaSuccess ? e : cudaGetLastError();
-}
-
-}  // namespace
+}  // namespace wmma
 
 int attend_mma_rows_per_chunk(int d, int d_v) { return mma_shape(d, d_v).ch; }
 

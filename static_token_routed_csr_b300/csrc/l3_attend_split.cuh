@@ -50,8 +50,13 @@ struct MergeSmem {
   float w[kMT][kMergeW];  // a holder's m, then its weight
   float l[kMT][kMergeW];
   float M[kMT], inv_l[kMT];
+  int64_t tok[kMT];       // batch index of each of the group's tokens
   int nh, first_second, last;
 };
+
+template <typename Bar>
+__device__ __noinline__ void merge_held(const AttendArgs& a, int q0, int mt, MergeSmem* sm,
+                                        int tid, int nthr, Bar bar);
 
 // After this CTA (chunks [cb, ce)) wrote its partial for group g (chunks [c0, c1)): count
 // the group's chunks done and, in the CTA that completes the count, merge all partials in
@@ -107,6 +112,15 @@ __device__ __noinline__ void arrive_and_merge(const AttendArgs& a, int g, int64_
       sm->first_second = c0 > cs[b0] ? 1 : 0;  // the group is CTA b0's second slot
     }
   }
+  merge_held(a, q0, mt, sm, tid, nthr, bar);
+}
+
+// Merge the partials of a group (tokens q0 .. q0 + mt - 1 in sorted order) held by the CTAs
+// sm->hold[0 .. sm->nh) in CTA order (holder 0 keeps it in its second slot if
+// sm->first_second), and write the group's outputs. Same caller rules as arrive_and_merge.
+template <typename Bar>
+__device__ __noinline__ void merge_held(const AttendArgs& a, int q0, int mt, MergeSmem* sm,
+                                        int tid, int nthr, Bar bar) {
   bar();
   const int nh = sm->nh;
   const bool fs = sm->first_second != 0;
@@ -135,29 +149,48 @@ __device__ __noinline__ void arrive_and_merge(const AttendArgs& a, int g, int64_
     for (int h = 0; h < nw; ++h) sm->w[j][h] = expf(sm->w[j][h] - M) * inv;
     sm->M[j] = M;
     sm->inv_l[j] = inv;
+    const int64_t i = int64_t(uint32_t(a.sorted_keys[q0 + j]));
+    sm->tok[j] = i;
     if (a.ml) {
-      const int64_t i = int64_t(uint32_t(a.sorted_keys[q0 + j]));
       a.ml[2 * i] = M;
       a.ml[2 * i + 1] = L;
     }
   }
   bar();
-  // a = sum_h w_h acc_h, two columns per thread and token
+  // a = sum_h w_h acc_h. Thread tid takes the column pair cp = tid % half of the tokens
+  // tid / half, + nthr / half, ... (d_v <= 512, so half <= nthr). The code is kept compact:
+  // a merge runs at most once per group, often with the instruction cache cold, and four
+  // holders' loads are in flight per step.
   const int half = a.d_v / 2;
-  for (int idx = tid; idx < mt * half; idx += nthr) {
-    const int j = idx / half, col = 2 * (idx - j * half);
+  const int jstep = nthr / half;
+  const int cp = tid % half;
+#pragma unroll 1
+  for (int j = tid / half; j < mt; j += jstep) {
     float s0 = 0.f, s1 = 0.f;
-#pragma unroll 4
-    for (int h = 0; h < nh; ++h) {
+    int h = 0;
+#pragma unroll 1
+    for (; h + 4 <= nw; h += 4) {
+      float2 v[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        v[e] = __ldcg(reinterpret_cast<const float2*>(entry(h + e, j) + 2 + 2 * cp));
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float wt = sm->w[j][h + e];
+        s0 = fmaf(v[e].x, wt, s0);
+        s1 = fmaf(v[e].y, wt, s1);
+      }
+    }
+#pragma unroll 1
+    for (; h < nh; ++h) {
       const float* pp = entry(h, j);
       const float wt = h < kMergeW ? sm->w[j][h] : expf(__ldcg(pp) - sm->M[j]) * sm->inv_l[j];
-      const float2 v = __ldcg(reinterpret_cast<const float2*>(pp + 2 + col));
+      const float2 v = __ldcg(reinterpret_cast<const float2*>(pp + 2 + 2 * cp));
       s0 = fmaf(v.x, wt, s0);
       s1 = fmaf(v.y, wt, s1);
     }
-    const int64_t i = int64_t(uint32_t(a.sorted_keys[q0 + j]));
-    write_a(a, i, col, s0);
-    write_a(a, i, col + 1, s1);
+    write_a(a, sm->tok[j], 2 * cp, s0);
+    write_a(a, sm->tok[j], 2 * cp + 1, s1);
   }
 }
 

@@ -15,7 +15,7 @@ struct DevStatus {
   int32_t token_range;  // a token id outside [0, vocab)
   int32_t layer_bad;    // offsets table violates its contract
   int32_t timeout;      // a bounded wait gave up (bit pattern says where)
-  int32_t pad;
+  int32_t capacity;     // an output held fewer rows than the batch touches
 };
 
 constexpr size_t kAlign = 256;

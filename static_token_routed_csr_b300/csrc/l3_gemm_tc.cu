@@ -87,13 +87,23 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return lo | (hi << 16);
 }
 
+// Shared staging of the swapped GEMM-up epilogue: 128 rows (features) x up to 64 columns
+// (tokens), row stride 65 floats (conflict-free both ways).
+constexpr int kSwapLd = 65;
+constexpr int kSwapStageBytes = kBM * kSwapLd * 4;
+
 // NACC * BN TMEM columns per accumulator set; two sets (the epilogue of one tile overlaps
 // the next tile's MMAs) when they fit in the 512 columns, else one.
-template <int BN, int NACC, int STAGES, bool SPLIT>
+// SWAP (batches of at most 64 tokens): the weight matrix is the 128-row operand A (rows =
+// output features, K contiguous, from mapA1 at every k-block) and the tokens are the N = 64
+// columns, from mapB for k-blocks below kb1 and mapB2 above; the epilogue writes the
+// transposed outputs.
+template <int BN, int NACC, int STAGES, bool SPLIT, bool SWAP = false>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA1,
                    const __grid_constant__ CUtensorMap mapA2,
-                   const __grid_constant__ CUtensorMap mapB, const TcParams p) {
+                   const __grid_constant__ CUtensorMap mapB,
+                   const __grid_constant__ CUtensorMap mapB2, const TcParams p) {
   static_assert(NACC * BN <= int(kTmemCols), "TMEM budget");
   constexpr uint32_t NBUF = 2 * NACC * BN <= int(kTmemCols) ? 2 : 1;
   constexpr int A_BYTES = kBM * kBK * 2;
@@ -153,6 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::tma_prefetch_desc(&mapA1);
       tc::tma_prefetch_desc(&mapA2);
       tc::tma_prefetch_desc(&mapB);
+      if (SWAP) tc::tma_prefetch_desc(&mapB2);
       uint32_t it = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
@@ -166,11 +177,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc::mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
           unsigned char* a_dst = smem + s * STAGE_BYTES;
-          if (kb < p.kb1)
+          if (SWAP) {
             tc::tma_load_2d(&mapA1, &full[s], a_dst, kb * kBK, m_blk * kBM);
-          else
-            tc::tma_load_2d(&mapA2, &full[s], a_dst, (kb - p.kb1) * kBK, m_blk * kBM);
-          tc::tma_load_2d(&mapB, &full[s], a_dst + A_BYTES, kb * kBK, n_blk * BN);
+            if (kb < p.kb1)
+              tc::tma_load_2d(&mapB, &full[s], a_dst + A_BYTES, kb * kBK, n_blk * BN);
+            else
+              tc::tma_load_2d(&mapB2, &full[s], a_dst + A_BYTES, (kb - p.kb1) * kBK, n_blk * BN);
+          } else {
+            if (kb < p.kb1)
+              tc::tma_load_2d(&mapA1, &full[s], a_dst, kb * kBK, m_blk * kBM);
+            else
+              tc::tma_load_2d(&mapA2, &full[s], a_dst, (kb - p.kb1) * kBK, m_blk * kBM);
+            tc::tma_load_2d(&mapB, &full[s], a_dst + A_BYTES, kb * kBK, n_blk * BN);
+          }
           ++it;
         }
       }
@@ -247,7 +266,64 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n0 = n_blk * BN;
       const int ncols = p.N - n0 < BN ? p.N - n0 : BN;
       const uint32_t acc0 = lane_base + uint32_t(int(b) * NACC * BN);
-      if (SPLIT) {
+      if (SWAP && SPLIT) {
+        // split-K part, transposed problem: row m is an output feature, columns are tokens;
+        // raw accumulators to slab[(part NACC + acc) M + m][N] (columns past N not stored)
+        const int part = u / tiles;
+#pragma unroll
+        for (int acc = 0; acc < NACC; ++acc) {
+          const bool has = NACC == 1 || (acc == 0 ? k_lo < p.kb1 : k_hi > p.kb1);
+          float* dst = p.slab + ((int64_t(part) * NACC + acc) * p.M + m) * p.N + n0;
+          for (int c = 0; c < BN / 32; ++c) {
+            if (c * 32 >= ncols) break;
+            float v[32];
+            if (has) {
+              tc::tmem_ld32(acc0 + uint32_t(acc * BN + c * 32), v);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = 0.f;
+            }
+            if (row_ok)
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (c * 32 + j < ncols) dst[c * 32 + j] = v[j];
+          }
+        }
+      } else if (SWAP) {
+        // GEMM-up, transposed: row m is feature m, columns the tokens. U[token][m] = bf16,
+        // then per token the (sum, squared deviations) of this tile's 128 rounded features,
+        // through a shared staging tile (threads e < ncols take token e).
+        float* su = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES + 256);
+        const int e = q * 32 + lane;  // epilogue thread id = row of the tile
+        for (int c = 0; c < BN / 32; ++c) {
+          if (c * 32 >= ncols) break;
+          float v[32];
+          tc::tmem_ld32(acc0 + uint32_t(c * 32), v);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float r = round_bf16(v[j]);
+            su[e * kSwapLd + c * 32 + j] = row_ok ? r : 0.f;
+            if (row_ok && c * 32 + j < ncols)
+              p.U[int64_t(n0 + c * 32 + j) * p.M + m] = __float2bfloat16_rn(r);
+          }
+        }
+        asm volatile("bar.sync 2, 128;" ::: "memory");
+        if (e < ncols) {
+          const int rows = p.M - m_blk * kBM < kBM ? p.M - m_blk * kBM : kBM;
+          float sum = 0.f;
+          for (int f = 0; f < rows; ++f) sum += su[f * kSwapLd + e];
+          const float mean = sum / float(rows);
+          float m2 = 0.f;
+          for (int f = 0; f < rows; ++f) {
+            const float dd = su[f * kSwapLd + e] - mean;
+            m2 = fmaf(dd, dd, m2);
+          }
+          float* st = p.stats + (int64_t(m_blk) * p.N + n0 + e) * 2;
+          st[0] = sum;
+          st[1] = m2;
+        }
+        asm volatile("bar.sync 2, 128;" ::: "memory");
+      } else if (SPLIT) {
         // split-K part: raw accumulators (zeros for an accumulator this K range missed)
         const int part = u / tiles;
 #pragma unroll
@@ -404,18 +480,19 @@ bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, in
 
 int num_sms() { return device_sm_count(); }
 
-template <int BN, int NACC, int STAGES, bool SPLIT>
+template <int BN, int NACC, int STAGES, bool SPLIT, bool SWAP = false>
 cudaError_t launch_tc(const CUtensorMap& a1, const CUtensorMap& a2, const CUtensorMap& b,
-                      const TcParams& p, cudaStream_t stream) {
-  constexpr int kSmem = STAGES * (kBM + BN) * kBK * 2 + 1024 + 256;
-  auto kern = tc_gemm_kernel<BN, NACC, STAGES, SPLIT>;
+                      const CUtensorMap& b2, const TcParams& p, cudaStream_t stream) {
+  constexpr int kSmem =
+      STAGES * (kBM + BN) * kBK * 2 + 1024 + 256 + (SWAP && !SPLIT ? kSwapStageBytes : 0);
+  auto kern = tc_gemm_kernel<BN, NACC, STAGES, SPLIT, SWAP>;
   const cudaError_t attr = ensure_smem_attr(kern, kSmem);
   if (attr != cudaSuccess) return attr;
   const int units = ((p.M + kBM - 1) / kBM) * ((p.N + BN - 1) / BN) * (SPLIT ? p.splits : 1);
   // a side job (row sums) is spread over every SM even when there are fewer tiles
   const int grid = units < num_sms() && !p.cs_W ? units : num_sms();
   const cudaError_t e = launch_pdl(kern, dim3(grid), dim3(kThreads), size_t(kSmem), stream, a1,
-                                   a2, b, p);
+                                   a2, b, b2, p);
   count_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -453,6 +530,7 @@ __global__ void splitk_up_finish_kernel(const float* __restrict__ slab, int part
 #pragma unroll
   for (int j = 0; j < 8; ++j) v[j] = 0.f;
   if (on)
+#pragma unroll 4
     for (int s = 0; s < parts; ++s) {
       const float4* src = reinterpret_cast<const float4*>(slab + (int64_t(s) * M + m) * N + c0);
       const float4 a = __ldcg(src), b = __ldcg(src + 1);
@@ -496,9 +574,11 @@ __global__ void splitk_mix_finish_kernel(const float* __restrict__ slab, int par
   if (w >= int64_t(M) * n_chunks) return;
   const int m = int(w / n_chunks), chunk = int(w % n_chunks);
   float tot = 0.f;
+#pragma unroll 4
   for (int j = 0; j < stat_tiles; ++j) tot += stats_in[(int64_t(j) * M + m) * 2];
   const float mean = tot / float(N);
   float m2 = 0.f;
+#pragma unroll 4
   for (int j = 0; j < stat_tiles; ++j) {
     const float* st = stats_in + (int64_t(j) * M + m) * 2;
     const int cnt = N - j * stat_bn < stat_bn ? N - j * stat_bn : stat_bn;
@@ -515,6 +595,7 @@ __global__ void splitk_mix_finish_kernel(const float* __restrict__ slab, int par
   float v0[8], v1[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) v0[j] = v1[j] = 0.f;
+#pragma unroll 4
   for (int s = 0; s < parts; ++s) {
     const float4* a = reinterpret_cast<const float4*>(slab + ((int64_t(s) * 2) * M + m) * N + c0);
     const float4* b = reinterpret_cast<const float4*>(slab + ((int64_t(s) * 2 + 1) * M + m) * N + c0);
@@ -538,7 +619,92 @@ __global__ void splitk_mix_finish_kernel(const float* __restrict__ slab, int par
   }
 }
 
+// Split-K finish of the transposed GEMM-mix (batches of at most 64 tokens): slab holds
+// [part][acc][feature][token]; y[token][feature] = rstd (sum acc0 - mu colsum) + sum acc1
+// with the token's mu / rstd merged from the transposed GEMM-up's per-128-feature
+// statistics. A CTA takes 32 features of every token: threads read along the tokens, and a
+// shared tile turns the result so that y is written along its rows.
+constexpr int kSwapTok = 64;
+__global__ void __launch_bounds__(256) splitk_mix_swap_finish_kernel(
+    const float* __restrict__ slab, int parts, int M, int N, const float* __restrict__ stats_in,
+    int stat_tiles, int stat_bn, const float* __restrict__ colsum, float eps, void* Y,
+    int y_dtype, float* mu_out, float* rstd_out) {
+  grid_dep_wait();
+  grid_dep_release();
+  __shared__ float s_mean[kSwapTok], s_rstd[kSwapTok];
+  __shared__ float sy[kSwapTok][33];
+  const int tid = threadIdx.x;
+  const int f0 = blockIdx.x * 32;
+  if (tid < N) {
+    float tot = 0.f;
+#pragma unroll 4
+    for (int j = 0; j < stat_tiles; ++j) tot += stats_in[(int64_t(j) * N + tid) * 2];
+    const float mean = tot / float(M);
+    float m2 = 0.f;
+#pragma unroll 4
+    for (int j = 0; j < stat_tiles; ++j) {
+      const float* st = stats_in + (int64_t(j) * N + tid) * 2;
+      const int cnt = M - j * stat_bn < stat_bn ? M - j * stat_bn : stat_bn;
+      const float dm = st[0] / float(cnt) - mean;
+      m2 += st[1] + float(cnt) * dm * dm;
+    }
+    const float rstd = 1.f / sqrtf(m2 / float(M) + eps);
+    s_mean[tid] = mean;
+    s_rstd[tid] = rstd;
+    if (blockIdx.x == 0 && mu_out) {
+      mu_out[tid] = mean;
+      rstd_out[tid] = rstd;
+    }
+  }
+  __syncthreads();
+  const int fl = tid >> 3, nb = (tid & 7) * 8, f = f0 + fl;
+  if (f < M) {
+    float v0[8], v1[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v0[j] = v1[j] = 0.f;
+#pragma unroll 4
+    for (int s = 0; s < parts; ++s) {
+      const float* a = slab + ((int64_t(s) * 2) * M + f) * N;
+      const float* b = slab + ((int64_t(s) * 2 + 1) * M + f) * N;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (nb + j < N) {
+          v0[j] += __ldcg(a + nb + j);
+          v1[j] += __ldcg(b + nb + j);
+        }
+    }
+    const float c = __ldg(colsum + f);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (nb + j < N) sy[nb + j][fl] = fmaf(s_rstd[nb + j], v0[j] - s_mean[nb + j] * c, v1[j]);
+  }
+  __syncthreads();
+  for (int idx = tid; idx < N * 32; idx += 256) {
+    const int n = idx >> 5, fc = idx & 31;
+    if (f0 + fc >= M) continue;
+    const int64_t o = int64_t(n) * M + f0 + fc;
+    if (y_dtype == L3_BF16)
+      static_cast<__nv_bfloat16*>(Y)[o] = __float2bfloat16_rn(sy[n][fc]);
+    else
+      static_cast<float*>(Y)[o] = sy[n][fc];
+  }
+}
+
 }  // namespace
+
+// Batches of at most this many tokens take the transposed GEMMs (weights as the 128-row
+// MMA operand, the tokens as its N = 64 columns): GEMM-up needs no split, GEMM-mix splits
+// K over enough parts to fill the SMs.
+constexpr int64_t kSwapMaxT = kSwapTok;
+constexpr int kSwapBN = kSwapTok;
+int swap_mix_parts(int d) {
+  const int tiles = (d + kBM - 1) / kBM;
+  int s = num_sms() / tiles;
+  const int kbt = 2 * d / kBK;
+  if (s > kbt) s = kbt;
+  if (s > 16) s = 16;
+  return s < 1 ? 1 : s;
+}
 
 // GEMM-mix splits K when its wide tiles would leave most SMs idle; it then takes narrower
 // tiles (more units) and at least two parts.
@@ -550,6 +716,7 @@ int mix_parts(int64_t T, int d) {
 }
 
 size_t tc_splitk_floats(int64_t T, int d, int d_v) {
+  if (T <= kSwapMaxT) return size_t(swap_mix_parts(d)) * 2 * size_t(T) * size_t(d);
   const size_t up = size_t(splitk_parts(T, d, kUpBN, d_v / kBK));
   const size_t mix = size_t(mix_parts(T, d));
   const size_t a = up > 1 ? up * size_t(T) * size_t(d) : 0;
@@ -557,13 +724,41 @@ size_t tc_splitk_floats(int64_t T, int d, int d_v) {
   return a > b ? a : b;
 }
 
-int tc_up_stat_tiles(int d) { return (d + kUpBN - 1) / kUpBN; }
+// Statistics tiles of GEMM-up: 256-column tiles, or 128-feature tiles in the transposed form
+// (the buffer is sized for the larger count).
+int tc_up_stat_tiles(int d) { return (d + kBM - 1) / kBM; }
 
 cudaError_t launch_tc_up(const __nv_bfloat16* A, const __nv_bfloat16* W_up, int64_t T, int d,
                          int d_v, __nv_bfloat16* U, float* stats, float* slab,
                          size_t slab_floats, const __nv_bfloat16* W_mix, float* colsum,
                          DevStatus* st, cudaStream_t stream) {
   if (T <= 0) return cudaSuccess;
+  if (T <= kSwapMaxT) {
+    // transposed: D[features x tokens] = W_up A^T, U[token][feature] and per-token
+    // statistics of each 128-feature tile
+    CUtensorMap mw, ma;
+    if (!make_map(&mw, W_up, d, d_v, kBM) || !make_map(&ma, A, T, d_v, kSwapBN))
+      return cudaErrorInvalidValue;
+    TcParams p{};
+    p.M = d;
+    p.N = int(T);
+    p.kb1 = d_v / kBK;
+    p.kb2 = 0;
+    p.mode = 0;
+    p.U = U;
+    p.stats = stats;
+    p.st = st;
+    p.splits = 1;
+    if (colsum) {
+      if ((reinterpret_cast<uintptr_t>(W_mix) & 15) != 0) return cudaErrorInvalidValue;
+      p.cs_W = W_mix;
+      p.cs_rows = d;
+      p.cs_ld = 2 * d;
+      p.cs_cols = d;
+      p.cs_out = colsum;
+    }
+    return launch_tc<kSwapBN, 1, 6, false, true>(mw, mw, ma, ma, p, stream);
+  }
   CUtensorMap ma, mb;
   if (!make_map(&ma, A, T, d_v, kBM) || !make_map(&mb, W_up, d, d_v, kUpBN))
     return cudaErrorInvalidValue;
@@ -588,9 +783,9 @@ cudaError_t launch_tc_up(const __nv_bfloat16* A, const __nv_bfloat16* W_up, int6
   p.splits = splitk_parts(T, d, kUpBN, p.kb1);
   if (p.splits > 1 && (!slab || size_t(p.splits) * size_t(T) * size_t(d) > slab_floats))
     p.splits = 1;  // no room for the parts: one K range per tile
-  if (p.splits == 1) return launch_tc<kUpBN, 1, 4, false>(ma, ma, mb, p, stream);
+  if (p.splits == 1) return launch_tc<kUpBN, 1, 4, false>(ma, ma, mb, mb, p, stream);
   p.slab = slab;
-  const cudaError_t e = launch_tc<kUpBN, 1, 4, true>(ma, ma, mb, p, stream);
+  const cudaError_t e = launch_tc<kUpBN, 1, 4, true>(ma, ma, mb, mb, p, stream);
   if (e != cudaSuccess) return e;
   const int64_t warps = T * ((d + kUpBN - 1) / kUpBN);
   const cudaError_t e2 = launch_pdl(splitk_up_finish_kernel, dim3(unsigned((warps + 7) / 8)),
@@ -605,6 +800,32 @@ cudaError_t launch_tc_mix(const __nv_bfloat16* U, const __nv_bfloat16* x,
                           float* rstd_out, float* slab, size_t slab_floats, DevStatus* st,
                           cudaStream_t stream) {
   if (T <= 0) return cudaSuccess;
+  if (T <= kSwapMaxT) {
+    // transposed: D[features x tokens] = W_mix [U x]^T over K = 2d in parts, then the finish
+    const int parts = swap_mix_parts(d);
+    if (!slab || 2 * size_t(parts) * size_t(T) * size_t(d) > slab_floats)
+      return cudaErrorInvalidValue;
+    CUtensorMap mw, mu, mx;
+    if (!make_map(&mw, W_mix, d, 2 * int64_t(d), kBM) || !make_map(&mu, U, T, d, kSwapBN) ||
+        !make_map(&mx, x, T, d, kSwapBN))
+      return cudaErrorInvalidValue;
+    TcParams p{};
+    p.M = d;
+    p.N = int(T);
+    p.kb1 = d / kBK;
+    p.kb2 = d / kBK;
+    p.mode = 1;
+    p.st = st;
+    p.splits = parts;
+    p.slab = slab;
+    cudaError_t e = launch_tc<kSwapBN, 2, 6, true, true>(mw, mw, mu, mx, p, stream);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(splitk_mix_swap_finish_kernel, dim3(unsigned((d + 31) / 32)), dim3(256), 0,
+                   stream, slab, parts, d, int(T), stats, tc_up_stat_tiles(d), int(kBM), colsum,
+                   eps, y, y_dtype, mu_out, rstd_out);
+    count_launch();
+    return e != cudaSuccess ? e : cudaGetLastError();
+  }
   const int parts = mix_parts(T, d);
   CUtensorMap mu, mx, mw;
   if (!make_map(&mu, U, T, d, kBM) || !make_map(&mx, x, T, d, kBM) ||
@@ -617,7 +838,7 @@ cudaError_t launch_tc_mix(const __nv_bfloat16* U, const __nv_bfloat16* x,
   p.kb2 = d / kBK;
   p.mode = 1;
   p.stats_in = stats;
-  p.stat_tiles = tc_up_stat_tiles(d);
+  p.stat_tiles = (d + kUpBN - 1) / kUpBN;
   p.stat_bn = kUpBN;
   p.colsum = colsum;
   p.eps = eps;
@@ -629,9 +850,9 @@ cudaError_t launch_tc_mix(const __nv_bfloat16* U, const __nv_bfloat16* x,
   p.splits = parts;
   if (p.splits > 1 && (!slab || 2 * size_t(p.splits) * size_t(T) * size_t(d) > slab_floats))
     return cudaErrorInvalidValue;  // the workspace is sized for the parts
-  if (p.splits == 1) return launch_tc<kMixBN, 2, 4, false>(mu, mx, mw, p, stream);
+  if (p.splits == 1) return launch_tc<kMixBN, 2, 4, false>(mu, mx, mw, mw, p, stream);
   p.slab = slab;
-  const cudaError_t e = launch_tc<kMixSplitBN, 2, 6, true>(mu, mx, mw, p, stream);
+  const cudaError_t e = launch_tc<kMixSplitBN, 2, 6, true>(mu, mx, mw, mw, p, stream);
   if (e != cudaSuccess) return e;
   const int64_t warps = T * ((d + 255) / 256);
   const cudaError_t e2 = launch_pdl(

@@ -45,6 +45,21 @@ struct alignas(16) AttendGroup {
   int32_t pad;
   int32_t tok[kPlanMT];  // batch index of each token (0 past mt)
 };
+// The group that holds the first chunk of a CTA's range in the split-row kernel, copied
+// out by the plan so that the kernel can issue its first copies after a single read.
+struct alignas(16) CtaHead {
+  int32_t g;    // group index
+  int32_t q0, mt, n, row0, c0;
+  int32_t c1;   // the group's end chunk (the next group's c0)
+  int32_t row;  // table row of the range's first chunk
+  int32_t tok[kPlanMT];
+};
+// A group cut by the end of a split-row CTA's range that starts in that range: written by the
+// CTA (g < 0: none) for the combine kernel, which merges the group's partials.
+struct alignas(16) AttendCut {
+  int32_t g, q0, mt, second;  // second: the group is the CTA's second partial slot
+  int64_t c0, c1;             // the group's chunks
+};
 struct AttendItem {
   int32_t q0;  // first sorted position
   int32_t nt;  // tokens (1..kTcNT)
@@ -70,6 +85,7 @@ struct PlanOut {
   // be empty; cta_group[b] is the group holding chunk cta_start[b].
   int32_t* cta_start;  // [n_cta + 1]
   int32_t* cta_group;  // [n_cta]
+  CtaHead* cta_head;   // [n_cta]: the group holding chunk cta_start[b]
   int n_cta;
   int w_chunk, w_group;
 };
@@ -97,6 +113,8 @@ struct AttendArgs {
   float* part;           // attend_part_floats(T, d_v) floats: partial (m, l, acc) per slot
   const int32_t* cta_start;  // the plan's split of the chunk list (PlanOut)
   const int32_t* cta_group;
+  const CtaHead* cta_head;
+  AttendCut* cuts;           // [n_cta] (bf16 kernel): groups left to the combine kernel
   int n_cta;                 // grid of the split-row kernel
   DevStatus* st;
 };
@@ -225,11 +243,126 @@ struct SegReduceArgs {
 };
 cudaError_t launch_seg_reduce(const SegReduceArgs& a, cudaStream_t stream);
 
+// ---- plain GEMMs of the backward on cuBLASLt (l3_blas.cu) ---------------------------------
+// Column-major C[m x n] (ldc; fp32, or bf16 with c_bf16) = op(A)[m x k] op(B)[k x n]
+// (+ C when accumulate), A and B bf16 (op = transpose when trans_*), fp32 accumulation.
+struct LtGemm {
+  int m, n, k;
+  bool trans_a, trans_b;
+  const void* A;
+  int64_t lda;
+  const void* B;
+  int64_t ldb;
+  void* C;
+  int64_t ldc;
+  bool c_bf16;
+  bool accumulate;
+};
+constexpr size_t kLtWorkspace = size_t(32) << 20;  // cuBLASLt scratch carved from the workspace
+cudaError_t lt_gemm(const LtGemm& g, void* ws, size_t ws_bytes, cudaStream_t stream);
+
 // ---- token-stream counts (l3_count.cu) ---------------------------------------------------
 // counts[t] (int64, zeroed here) = occurrences of id t in ids[0..n); ids outside [0, vocab)
 // are not counted and set st->token_range.
 cudaError_t launch_count_ids(const int32_t* ids, int64_t n, int64_t vocab, int64_t* counts,
                              DevStatus* st, cudaStream_t stream);
+
+// ---- backward at batch scale with row gradients (l3_backward_rows.cu) --------------------
+struct AttendBwdRowsArgs {
+  const uint64_t* sorted_keys;
+  int64_t T;
+  const AttendGroup* groups;  // the routing plan's groups (every segment, ch-row chunks)
+  const int32_t* hdr;
+  const void* K;
+  const void* V;
+  int64_t v;
+  int d, d_v, ch, k_max;
+  const __nv_bfloat16* x;     // [T, d] batch order
+  const __nv_bfloat16* da16;     // [T, d_v] batch order, bf16(da)
+  const __nv_bfloat16* da16_lo;  // [T, d_v] bf16(da - bf16(da))
+  const float* ml;            // [T, 2] the forward's (max score, denominator)
+  const float* delta;         // [T] a_i . da_i
+  float* dx;                  // [T, d]: holds the direct term; the attention term is added
+  float* p_buf;               // [T, k_max] by sorted position and row within the id
+  float* ds_buf;              // [T, k_max]
+  int n_cta;
+  DevStatus* st;
+};
+// Rows per chunk of the backward's plan for a layer shape.
+int attend_bwd_rows_per_chunk(int d, int d_v);
+cudaError_t launch_attend_bwd_rows(const AttendBwdRowsArgs& a, cudaStream_t stream);
+struct SegRowsArgs {
+  const uint64_t* sorted_keys;
+  const int32_t* seg_start;
+  const int32_t* n_seg;
+  const int32_t* offs;
+  const int32_t* seg_row0;   // [S] first output row of each segment
+  const int32_t* seg_unit0;  // [S + 1] first work unit of each segment
+  const __nv_bfloat16* x_sorted;   // [T, d]
+  const __nv_bfloat16* da_sorted;  // [T, d_v]
+  const float* p_buf;
+  const float* ds_buf;
+  int k_max, d, d_v;
+  int32_t* row_index;  // [max_rows]
+  float* dK_rows;      // [max_rows, d]
+  float* dV_rows;      // [max_rows, d_v]
+  int64_t max_rows;
+  DevStatus* st;
+};
+int seg_rows_col_blocks(int d, int d_v);
+cudaError_t launch_seg_rows(const SegRowsArgs& a, cudaStream_t stream);
+cudaError_t launch_row_plan(const uint64_t* keys, const int32_t* seg_start, const int32_t* n_seg,
+                            const int32_t* offs, int d, int d_v, int32_t* seg_row0,
+                            int32_t* seg_unit0, int32_t* n_rows, int64_t max_rows,
+                            DevStatus* st, cudaStream_t stream);
+// Row kernels of the backward: stage 0: LayerNorm of the fp32 U (h over U, h16, rstd);
+// stage 1: du = LayerNorm backward of dh as bf16 hi + lo; stage 2: x and da in sorted
+// order, da as bf16 hi + lo, delta = a . da; stage 3: a as bf16 hi + lo.
+struct BwdSmallArgs {
+  int stage;
+  int64_t T;
+  int d, d_v;
+  float eps;
+  float* U32;
+  __nv_bfloat16* h16;
+  float* rstd_out;
+  const float* dh;
+  __nv_bfloat16* du;
+  __nv_bfloat16* du_lo;
+  const uint64_t* keys;
+  const __nv_bfloat16* x;
+  const float* a;
+  const float* da;
+  __nv_bfloat16* x_sorted;
+  __nv_bfloat16* da_sorted;
+  __nv_bfloat16* da16;
+  __nv_bfloat16* da16_lo;
+  float* delta;
+  __nv_bfloat16* a_hi;
+  __nv_bfloat16* a_lo;
+};
+cudaError_t launch_bwd_small(const BwdSmallArgs& a, cudaStream_t stream);
+
+// ---- staging of a batch's rows from host-resident tables (l3_stage.cu) ---------------------
+struct StageArgs {
+  const uint64_t* sorted_keys;
+  const int32_t* seg_start;
+  const int32_t* n_seg;
+  const int32_t* offs;      // the full layer's offsets (device)
+  const int32_t* seg_row0;  // [S] staged row of each segment's first row
+  const int32_t* n_rows;    // [1] staged rows U
+  const void* K_host;       // device-accessible address of the (pinned, mapped) host tables
+  const void* V_host;
+  int64_t k_row_bytes, v_row_bytes;
+  void* K_st;               // [max_rows, d] staged tables (device)
+  void* V_st;
+  int64_t max_rows;
+  int32_t* offs_st;         // [T + 1]
+  int32_t* ids_st;          // [T]
+  int64_t T;
+  DevStatus* st;
+};
+cudaError_t launch_stage_rows(const StageArgs& a, cudaStream_t stream);
 
 // ---- layer check (l3_api.cu) ---------------------------------------------------------------
 cudaError_t launch_check_offsets(const int32_t* offs, int64_t vocab, int64_t v, int k_max,

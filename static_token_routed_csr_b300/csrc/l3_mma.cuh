@@ -1,0 +1,90 @@
+// Warp-level tensor-core helpers shared by the split-row gather-attend and the backward
+// kernels: matrix loads from shared memory, mma.sync on bf16, bf16 hi + lo splitting of fp32
+// values, the 128-byte swizzled layout the 3-D TMA views of the tables produce, and those
+// tensor maps.
+#pragma once
+
+#include <cudaTypedefs.h>
+
+#include "l3_internal.h"
+#include "l3_tc.cuh"
+
+namespace l3 {
+namespace wmma {
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];"
+               : "=r"(r0), "=r"(r1)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2_t(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];"
+               : "=r"(r0), "=r"(r1)
+               : "r"(addr));
+}
+
+// D (16x8 fp32) += A (16x16 bf16, row) B (16x8 bf16, col)
+__device__ __forceinline__ void mma16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                      uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// D (16x8 fp32) += A (16x8 bf16, row) B (8x8 bf16, col)
+__device__ __forceinline__ void mma8(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5}, {%6}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(b0));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  return uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
+         (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+}
+// hi = bf16(v), lo = bf16(v - hi), packed in pairs (lower k in the low half).
+__device__ __forceinline__ void split_pair(float v0, float v1, uint32_t& hi, uint32_t& lo) {
+  const float h0 = __bfloat162float(__float2bfloat16_rn(v0));
+  const float h1 = __bfloat162float(__float2bfloat16_rn(v1));
+  hi = pack_bf16(h0, h1);
+  lo = pack_bf16(v0 - h0, v1 - h1);
+}
+
+// Byte offset of (row, column) in a block of `rows` rows laid out as [col / 64][row][64]
+// with the 128-byte swizzle (16-byte piece index XOR row % 8); the block is 1024-aligned.
+__device__ __forceinline__ uint32_t sw128(int rows, int row, int col) {
+  return uint32_t((col >> 6) * rows * 128 + row * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4));
+}
+
+__device__ __forceinline__ void tma_load_3d(const CUtensorMap* map, uint64_t* bar, uint32_t dst,
+                                            int32_t x, int32_t y, int32_t z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(tc::smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+
+// bf16 table [rows, cols] viewed as [cols / 64][rows][64]; box: all column blocks of
+// `box_rows` rows, 128-byte swizzle (defined in l3_attend_mma.cu).
+bool make_row_block_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols,
+                        int box_rows);
+
+}  // namespace wmma
+}  // namespace l3

@@ -3,9 +3,10 @@
 // layer's attention mask block-diagonal).
 //
 // Keys are (id << 32) | batch position. They are unique, so any correct sort of the keys
-// is the stable sort of the ids. With ids below 2^19, blocks of 8192 tokens are sorted by
-// one CTA each with a stable radix sort on the ids; otherwise blocks of 4096 keys are
-// sorted by a shared-memory bitonic network. Blocks are then merged pairwise (each key
+// is the stable sort of the ids. Batches of at most 256 tokens are ranked in one pass by one
+// CTA. Larger ones: with ids below 2^19, blocks of 8192 tokens are sorted by one CTA each
+// with a stable radix sort on the ids; otherwise blocks of 4096 keys are sorted by a
+// shared-memory bitonic network. Blocks are then merged pairwise (each key
 // finds its rank in the other run by binary search).
 // A last pass marks segment starts and numbers the segments, and (for the forward) lays out
 // the work plan of the split-row gather-attend.
@@ -122,6 +123,28 @@ __device__ int4 block_exclusive_scan4(int4 v, int4* warp_tot, int4* total) {
   return r;
 }
 
+// CTA b's head: group gh, which holds chunk c (the first of b's range); an empty head
+// when there is no such group (gh >= NG: the range is empty).
+__device__ void write_head(const PlanOut& pl, int64_t b, int gh, int64_t c, int NG) {
+  CtaHead h{};
+  if (gh >= NG) {
+    pl.cta_head[b] = h;
+    return;
+  }
+  const AttendGroup& gr = pl.groups[gh];
+  h.g = gh;
+  h.q0 = gr.q0;
+  h.mt = gr.mt;
+  h.n = gr.n;
+  h.row0 = gr.row0;
+  h.c0 = gr.c0;
+  h.c1 = pl.groups[gh + 1].c0;
+  h.row = gr.row0 + int32_t(c - gr.c0) * pl.ch;
+#pragma unroll
+  for (int j = 0; j < kPlanMT; ++j) h.tok[j] = gr.tok[j];
+  pl.cta_head[b] = h;
+}
+
 // Work plan of the gather-attend (see PlanOut), from the finished segment table.
 __device__ void plan_pass(const uint64_t* keys, int64_t T, const int32_t* seg_start, int S,
                           const PlanOut& pl, DevStatus* st, int* warp_tot, int* total) {
@@ -208,15 +231,24 @@ __device__ void plan_pass(const uint64_t* keys, int64_t T, const int32_t* seg_st
   if (U == 0) {
     for (int b = threadIdx.x; b <= n; b += blockDim.x) {
       pl.cta_start[b] = 0;
-      if (b < n) pl.cta_group[b] = 0;
+      if (b < n) {
+        pl.cta_group[b] = 0;
+        pl.cta_head[b] = CtaHead{};
+      }
     }
     return;
   }
   // CTAs with tau_b = 0: b U < n
   const int64_t b_zero = (n + U - 1) / U;  // smallest b with b U >= n
+  // the first group with chunks (groups without rows have none)
+  int g_first = 0;
+  while (g_first < NG && pl.groups[g_first + 1].c0 == pl.groups[g_first].c0) ++g_first;
   for (int64_t b = threadIdx.x; b < b_zero && b <= n; b += blockDim.x) {
     pl.cta_start[b] = 0;
-    if (b < n) pl.cta_group[b] = 0;
+    if (b < n) {
+      pl.cta_group[b] = 0;
+      write_head(pl, b, g_first, 0, NG);
+    }
   }
   for (int g = threadIdx.x; g < NG; g += blockDim.x) {
     const int64_t c0 = pl.groups[g].c0, c1 = pl.groups[g + 1].c0;
@@ -232,7 +264,15 @@ __device__ void plan_pass(const uint64_t* keys, int64_t T, const int32_t* seg_st
       const int64_t cs = r < 0 ? c0 : c0 + r / pl.w_chunk;  // chunk covering u1
       pl.cta_start[b] = int32_t(cs + 1);
       // group holding chunk cs + 1: this one, or (at its end) the search starts at the next
-      if (b < n) pl.cta_group[b] = cs + 1 < c1 ? g : g + 1;
+      if (b < n) {
+        pl.cta_group[b] = cs + 1 < c1 ? g : g + 1;
+        int gh = g;
+        if (cs + 1 >= c1) {  // the range starts at the next group with chunks
+          gh = g + 1;
+          while (gh < NG && pl.groups[gh + 1].c0 == pl.groups[gh].c0) ++gh;
+        }
+        write_head(pl, b, gh, cs + 1, NG);
+      }
     }
   }
 }
@@ -302,6 +342,35 @@ __global__ void __launch_bounds__(1024) route_small_kernel(const int32_t* __rest
   for (int i = threadIdx.x; i < T; i += blockDim.x) keys_out[i] = s[i];
   __syncthreads();
   segment_pass(s, T, perm, seg_start, seg_id, n_seg, with_plan ? &plan : nullptr, st, warp_tot,
+               &total);
+}
+
+// T <= kRankN: one CTA; each thread ranks its key among all keys of the batch (keys are
+// unique, so the ranks are a permutation: the stable sort), then the segment and plan passes.
+// One pass over shared memory instead of the radix passes' many CTA-wide barriers.
+constexpr int kRankN = 256;
+__global__ void __launch_bounds__(kRankN) route_rank_kernel(const int32_t* __restrict__ ids,
+                                                            int64_t T, int64_t vocab,
+                                                            uint64_t* keys_out, int32_t* perm,
+                                                            int32_t* seg_start, int32_t* seg_id,
+                                                            int32_t* n_seg, DevStatus* st,
+                                                            const PlanOut plan, int with_plan) {
+  grid_dep_release();  // as in the one-CTA radix kernel
+  __shared__ uint64_t kin[kRankN], kout[kRankN];
+  __shared__ int warp_tot[32];
+  __shared__ int total;
+  const int i = threadIdx.x;
+  const uint64_t key = make_key(ids, T, vocab, i, st);  // all ones past the batch
+  kin[i] = key;
+  __syncthreads();
+  if (i < T) {
+    int r = 0;
+    for (int j = 0; j < int(T); ++j) r += kin[j] < key ? 1 : 0;
+    kout[r] = key;
+    keys_out[r] = key;
+  }
+  __syncthreads();
+  segment_pass(kout, T, perm, seg_start, seg_id, n_seg, with_plan ? &plan : nullptr, st, warp_tot,
                &total);
 }
 
@@ -521,6 +590,13 @@ cudaError_t launch_route(const int32_t* ids, int64_t T, int64_t vocab, void* scr
   uint64_t* k0 = static_cast<uint64_t*>(scratch);
   uint64_t* k1 = reinterpret_cast<uint64_t*>(static_cast<char*>(scratch) +
                                              align_up(size_t(T) * sizeof(uint64_t), kAlign));
+  if (T <= kRankN) {
+    route_rank_kernel<<<1, kRankN, 0, stream>>>(ids, T, vocab, k0, out.perm, out.seg_start,
+                                                out.seg_id, out.n_seg, st, pl, with_plan);
+    count_launch();
+    *sorted_keys = k0;
+    return cudaGetLastError();
+  }
   // bits of the largest id; the radix path packs (id, index) into 32 bits
   int idbits = 1;
   while (idbits < 31 && (int64_t(1) << idbits) < vocab) ++idbits;

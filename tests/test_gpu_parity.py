@@ -130,7 +130,10 @@ def test_single_row_tokens_return_value_row_exactly_fp32():
     assert np.array_equal(a, V)
 
 
-@pytest.mark.parametrize("cid,T", [(5, None), (1, 1), (1, 129), (5, 300), (2, 1024), (2, 333)])
+# (T <= 64 takes the transposed GEMMs: 37 tokens on d = 320 ends the last feature tile at 64
+# rows, 64 tokens on d = 64 has a single partial tile)
+@pytest.mark.parametrize("cid,T", [(5, None), (1, 1), (1, 129), (5, 300), (2, 1024), (2, 333),
+                                   (6, 37), (5, 64), (2, 50), (3, 1)])
 def test_forward_small_all_tokens(cid, T):
     c = Case(cid, T=T)
     y, _ = c.forward()
