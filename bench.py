@@ -493,6 +493,16 @@ def run_ours(args, rank, world, local_rank):
     names = l3.STAGE_NAMES
     peaks = load_peaks()
 
+    if args.profile_bwd:
+        # profiler captures of the backward: a few forward + row-gradient backward steps
+        acct = workload_bytes(p, lay.wl.ids, lay.offs_np)
+        args.bwd_steps, args.warmup = 3, 1
+        fb = fwd_bwd_rows_rate(l3, lay, args, flush, acct, world)
+        clk.stop()
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "fwd_bwd": fb, "config": config_block(p, T),
+                              "note": "forward + backward (profiling run)"}), flush=True)
+        return 0
     if args.fwd_only:
         clk.stop()
         if rank == 0:
@@ -825,6 +835,8 @@ def main(argv=None):
     ap.add_argument("--bwd-steps", type=int, default=20,
                     help="timed steps of the forward + row-gradient backward leg")
     ap.add_argument("--no-bwd", action="store_true", help="skip the forward + backward leg")
+    ap.add_argument("--profile-bwd", action="store_true",
+                    help="only a few forward + backward steps (for profiler captures)")
     ap.add_argument("--rows", type=int, default=None,
                     help="profiling: table rows v of a smaller table with the preset's shapes")
     ap.add_argument("--vocab", type=int, default=None, help="profiling: vocabulary size")

@@ -173,9 +173,10 @@ struct BwdRowsWs {
   AttendGroup* groups;
   int32_t* hdr;
   int32_t* counters;
-  __nv_bfloat16 *a_hi, *a_lo, *h16, *du_hi, *du_lo, *x_sorted, *da_sorted, *da16, *da16_lo;
+  __nv_bfloat16 *a_hi, *a_lo, *h16, *du_hi, *du_lo, *x_sorted, *da16, *da16_lo;
   float *U32, *rstd, *dh, *da, *delta, *p_buf, *ds_buf;
   int32_t *seg_row0, *seg_unit0;
+  int64_t* seg_cost0;
   void* lt_ws;
 };
 
@@ -195,7 +196,6 @@ BwdRowsWs carve_bwd_rows(Carve& c, const l3_layer* L, int64_t T) {
   w.du_hi = c.take<__nv_bfloat16>(t * d);
   w.du_lo = c.take<__nv_bfloat16>(t * d);
   w.x_sorted = c.take<__nv_bfloat16>(t * d);
-  w.da_sorted = c.take<__nv_bfloat16>(t * dv);
   w.da16 = c.take<__nv_bfloat16>(t * dv);
   w.da16_lo = c.take<__nv_bfloat16>(t * dv);
   w.U32 = c.take<float>(t * d);
@@ -207,6 +207,7 @@ BwdRowsWs carve_bwd_rows(Carve& c, const l3_layer* L, int64_t T) {
   w.ds_buf = c.take<float>(t * km);
   w.seg_row0 = c.take<int32_t>(t + 1);
   w.seg_unit0 = c.take<int32_t>(t + 1);
+  w.seg_cost0 = c.take<int64_t>(t + 1);
   w.lt_ws = c.raw(kLtWorkspace);
   return w;
 }
@@ -467,6 +468,7 @@ size_t l3_workspace_size(const l3_layer* L, int64_t T, int32_t pass) {
     c.raw(route_scratch_bytes(T));
     for (int k = 0; k < 3; ++k) c.take<int32_t>(size_t(T) + 1);
     c.take<int32_t>(1);
+    c.take<int64_t>(size_t(T) + 1);
   } else {
     return 0;
   }
@@ -759,9 +761,11 @@ l3_status l3_backward_rows(const l3_layer* L, const int32_t* ids, int64_t T, con
   Carve cs(const_cast<void*>(saved));
   const Saved sv = carve_saved(cs, L, T);
   const int ch = attend_bwd_rows_per_chunk(d, dv);
-  // batch sorting and the token groups (every segment in groups of at most 8 tokens)
+  // batch sorting and the token groups (every segment in groups of at most 8 tokens); the
+  // CTAs of Phase A split the groups by cost: 2 units a chunk, 3 more a group (its fragment
+  // loads and its dx stores)
   PlanOut plan{w.groups, w.hdr, w.counters, nullptr, L->offs, L->v, L->k_max, ch, kPlanMT,
-               INT32_MAX, nullptr, nullptr, nullptr, 0, 1, 0};
+               INT32_MAX, nullptr, nullptr, nullptr, 0, 2, 3};
   const uint64_t* keys = nullptr;
   L3_CUDA(launch_route(ids, T, L->vocab, w.route_scratch,
                        RouteOut{nullptr, w.seg_start, nullptr, w.n_seg}, w.st, s, &keys, &plan));
@@ -792,10 +796,8 @@ l3_status l3_backward_rows(const l3_layer* L, const int32_t* ids, int64_t T, con
   // dW_mix = dyᵀ [h x]
   L3_CUDA(gemm(d, d, Ti, false, true, w.h16, d, dy, d, dW_mix, 2 * d, false, false));
   L3_CUDA(gemm(d, d, Ti, false, true, x, d, dy, d, dW_mix + d, 2 * d, false, false));
-  // dh = dy W_mix[:, :d] and the direct term dx = dy W_mix[:, d:]
+  // dh = dy W_mix[:, :d]
   L3_CUDA(gemm(d, Ti, d, false, false, L->W_mix, 2 * d, dy, d, w.dh, d, false, false));
-  L3_CUDA(gemm(d, Ti, d, false, false, static_cast<const __nv_bfloat16*>(L->W_mix) + d, 2 * d, dy,
-               d, dx, d, false, false));
   // du = LayerNorm backward (bf16 hi + lo); dW_up = duᵀ a; da = du W_up from both parts
   sa.stage = 1;
   sa.dh = w.dh;
@@ -811,12 +813,11 @@ l3_status l3_backward_rows(const l3_layer* L, const int32_t* ids, int64_t T, con
   sa.x = static_cast<const __nv_bfloat16*>(x);
   sa.da = w.da;
   sa.x_sorted = w.x_sorted;
-  sa.da_sorted = w.da_sorted;
   sa.da16 = w.da16;
   sa.da16_lo = w.da16_lo;
   sa.delta = w.delta;
   L3_CUDA(launch_bwd_small(sa, s));
-  // Phase A: p, ds per token and row; dx += sum_j ds_j K_j
+  // Phase A: p, ds per token and row; dx = sum_j ds_j K_j
   AttendBwdRowsArgs ab{};
   ab.sorted_keys = keys;
   ab.T = T;
@@ -829,7 +830,7 @@ l3_status l3_backward_rows(const l3_layer* L, const int32_t* ids, int64_t T, con
   ab.d_v = dv;
   ab.ch = ch;
   ab.k_max = L->k_max;
-  ab.x = static_cast<const __nv_bfloat16*>(x);
+  ab.x_sorted = w.x_sorted;
   ab.da16 = w.da16;
   ab.da16_lo = w.da16_lo;
   ab.ml = sv.ml;
@@ -840,9 +841,12 @@ l3_status l3_backward_rows(const l3_layer* L, const int32_t* ids, int64_t T, con
   ab.n_cta = device_sm_count();
   ab.st = w.st;
   L3_CUDA(launch_attend_bwd_rows(ab, s));
+  // dx += the direct term dy W_mix[:, d:]
+  L3_CUDA(gemm(d, Ti, d, false, false, static_cast<const __nv_bfloat16*>(L->W_mix) + d, 2 * d, dy,
+               d, dx, d, false, true));
   // Phase B: the touched rows' dK and dV, in segment order
   L3_CUDA(launch_row_plan(keys, w.seg_start, w.n_seg, L->offs, d, dv, w.seg_row0, w.seg_unit0,
-                          n_rows, max_rows, w.st, s));
+                          w.seg_cost0, n_rows, max_rows, w.st, s));
   SegRowsArgs sr{};
   sr.sorted_keys = keys;
   sr.seg_start = w.seg_start;
@@ -850,8 +854,9 @@ l3_status l3_backward_rows(const l3_layer* L, const int32_t* ids, int64_t T, con
   sr.offs = L->offs;
   sr.seg_row0 = w.seg_row0;
   sr.seg_unit0 = w.seg_unit0;
+  sr.seg_cost0 = w.seg_cost0;
   sr.x_sorted = w.x_sorted;
-  sr.da_sorted = w.da_sorted;
+  sr.da_sorted = w.da16;
   sr.p_buf = w.p_buf;
   sr.ds_buf = w.ds_buf;
   sr.k_max = L->k_max;
@@ -904,12 +909,13 @@ l3_status l3_stage_rows(const l3_layer* L, const int32_t* ids, int64_t T, void* 
   int32_t* n_seg = c.take<int32_t>(1);
   int32_t* seg_row0 = c.take<int32_t>(size_t(T) + 1);
   int32_t* seg_unit0 = c.take<int32_t>(size_t(T) + 1);
+  int64_t* seg_cost0 = c.take<int64_t>(size_t(T) + 1);
   L3_CUDA(cudaMemsetAsync(st, 0, sizeof(DevStatus), s));
   const uint64_t* keys = nullptr;
   L3_CUDA(launch_route(ids, T, L->vocab, route_scratch, RouteOut{nullptr, seg_start, nullptr, n_seg},
                        st, s, &keys));
   L3_CUDA(launch_row_plan(keys, seg_start, n_seg, L->offs, int(L->d), int(L->d_v), seg_row0,
-                          seg_unit0, n_rows, max_rows, st, s));
+                          seg_unit0, seg_cost0, n_rows, max_rows, st, s));
   const size_t es = L->dtype == L3_BF16 ? 2 : 4;
   StageArgs sa{};
   sa.sorted_keys = keys;

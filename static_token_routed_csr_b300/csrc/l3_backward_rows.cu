@@ -11,13 +11,14 @@
 //   dx_i += Σ_j ds_j K_j,  dK_j = Σ_{i of t} ds_ij x_i,  dV_j = Σ_{i of t} p_ij da_i.
 //
 // Phase A (attend_bwd_kernel) takes the routing plan's groups of at most 8 tokens of one id,
-// whole groups per CTA (cut by chunk count). Per group it streams the id's rows (TMA, as
-// the forward's split-row kernel) and computes the scores and dp with warp MMAs (x and da
-// fragments from shared-memory slots the producer fills; da as bf16 hi + lo, so that dp and
-// δ = a · da agree to about 2^-17 and ds = p (dp - δ) keeps its digits), p and ds in fp32
-// (stored per sorted position and row), and dx with a warp MMA over Kᵀ with ds as bf16
-// hi + lo; dx is added to the direct term the GEMMs left there. No group is split, so no
-// merge is needed.
+// whole groups per CTA (cut by the plan's cost units: a chunk and a group start each cost
+// a fixed share). Per group it streams the id's rows (TMA, as the forward's split-row
+// kernel) and computes the scores and dp with warp MMAs (x and da fragments loaded straight
+// from the sorted rows, which the producer prefetches into L2 when it reaches the group; da
+// as bf16 hi + lo, so that dp and δ = a · da agree to about 2^-17 and ds = p (dp - δ) keeps
+// its digits), p and ds in fp32 (stored per sorted position and row), and the attention
+// term of dx with a warp MMA over Kᵀ with ds as bf16 hi + lo, stored to dx (the direct term
+// is added afterwards). No group is split, so no merge is needed.
 // Phase B (seg_rows_kernel) takes, per id segment, 64-row blocks x 256-column blocks of
 // [dK | dV]: the sums over the segment's tokens (x or da rows in sorted order, p or ds as
 // bf16 hi + lo), written in segment order to the compact row outputs with each row's table
@@ -36,8 +37,7 @@ using namespace wmma;
 constexpr int kAThreads = 256;           // consumer threads (8 warps)
 constexpr int kAWarps = kAThreads / 32;
 constexpr int kACta = kAThreads + 32;    // + the producer warp
-constexpr int kAMaxStages = 4;
-constexpr int kASlots = 2;               // groups whose x and da rows are in shared memory
+constexpr int kAMaxStages = 6;
 constexpr int kAMaxKS = 16;              // 16-wide k-steps of d per warp (d <= 2048)
 constexpr int kAMaxKSV = 4;              // of d_v (d_v <= 512)
 constexpr int kAMaxDT = 16;              // 16-column tiles of dx per warp
@@ -47,7 +47,7 @@ constexpr int kASmemLimit = 232448;
 
 // A stage's group (written by the producer before it arms the stage).
 struct BMeta {
-  int32_t q0, mt, n, c0, c1, slot, pad0, pad1;
+  int32_t q0, mt, n, c0, c1, pad0, pad1, pad2;
   int32_t tok[kPlanMT];
   float m[kPlanMT], inv_l[kPlanMT], delta[kPlanMT];
 };
@@ -57,8 +57,6 @@ struct BMisc {
   uint64_t meta_full[kAMaxStages];
   uint64_t full[kAMaxStages];
   uint64_t empty[kAMaxStages];
-  uint64_t x_full[kASlots];
-  uint64_t x_empty[kASlots];
   float red_s[kAWarps][kPlanMT][kARedLd];  // score partials per warp
   float red_p[kAWarps][kPlanMT][kARedLd];  // dp partials per warp
   float e_buf[kPlanMT][kAEld];             // the step's ds per token and row
@@ -67,7 +65,7 @@ struct BMisc {
 };
 
 struct BShape {
-  int ch, stages, k_bytes, stage_bytes, x_row, da_row, slot_bytes, smem;
+  int ch, stages, k_bytes, stage_bytes, smem;
 };
 
 BShape bwd_shape(int d, int d_v) {
@@ -75,10 +73,7 @@ BShape bwd_shape(int d, int d_v) {
   s.ch = 16 * 2 * (d + d_v) <= 49152 ? 16 : 8;
   s.k_bytes = s.ch * 2 * d;
   s.stage_bytes = int(align_up(size_t(s.ch) * 2 * size_t(d + d_v), 1024));
-  s.x_row = 2 * d + 16;
-  s.da_row = 2 * d_v + 16;
-  s.slot_bytes = int(align_up(size_t(kPlanMT) * size_t(s.x_row + 2 * s.da_row), 128));
-  const int fixed = 1024 + int(align_up(sizeof(BMisc), 128)) + kASlots * s.slot_bytes;
+  const int fixed = 1024 + int(align_up(sizeof(BMisc), 128));
   s.stages = (kASmemLimit - fixed) / s.stage_bytes;
   if (s.stages > kAMaxStages) s.stages = kAMaxStages;
   s.smem = fixed + s.stages * s.stage_bytes;
@@ -89,23 +84,24 @@ __device__ __forceinline__ void abar() {
   asm volatile("bar.sync 1, %0;" ::"n"(kAThreads) : "memory");
 }
 
-__device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(dst),
-      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(tc::smem_u32(bar))
-      : "memory");
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)),
+               "r"(bytes)
+               : "memory");
 }
 
-// First group whose first chunk is >= c, by a 32-way search of the producer warp (groups
-// are ordered by first chunk; entry NG holds the total).
+__device__ __forceinline__ uint32_t ld_u32(const __nv_bfloat16* p) {
+  return __ldg(reinterpret_cast<const unsigned int*>(p));
+}
+
+// First group whose cost offset w0 is >= c, by a 32-way search of the producer warp (w0
+// increases along the groups; entry NG holds the total).
 __device__ int first_group_at(const AttendGroup* groups, int NG, int64_t c, int lane) {
   int lo = 0, hi = NG;  // answer in [lo, hi]
   while (hi - lo > 32) {
     const int step = (hi - lo + 31) / 32;
     const int probe = lo + lane * step;
-    const bool below = probe <= hi && groups[probe < hi ? probe : hi].c0 < c;
+    const bool below = probe <= hi && groups[probe < hi ? probe : hi].w0 < c;
     const unsigned m = __ballot_sync(0xffffffffu, below && probe < hi);
     // lanes whose probe lies below c form a prefix
     const int nb = __popc(m);
@@ -115,7 +111,7 @@ __device__ int first_group_at(const AttendGroup* groups, int NG, int64_t c, int 
     hi = nhi;
   }
   const int probe = lo + lane;
-  const bool below = probe < hi && groups[probe].c0 < c;
+  const bool below = probe < hi && groups[probe].w0 < c;
   return lo + __popc(__ballot_sync(0xffffffffu, below));
 }
 
@@ -128,19 +124,18 @@ __global__ void __launch_bounds__(kACta, 1)
   unsigned char* base = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   unsigned char* ring = base;
-  unsigned char* slots = base + sh.stages * sh.stage_bytes;
-  BMisc* ms = reinterpret_cast<BMisc*>(slots + kASlots * sh.slot_bytes);
+  BMisc* ms = reinterpret_cast<BMisc*>(base + sh.stages * sh.stage_bytes);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g8 = lane >> 2, t4 = lane & 3;
   const int b = blockIdx.x;
   const int d = a.d, dv = a.d_v, S = sh.stages;
-  const uint32_t ring_s = tc::smem_u32(ring), slots_s = tc::smem_u32(slots);
+  const uint32_t ring_s = tc::smem_u32(ring);
 
   if (warp == kAWarps) {
-    // this CTA's groups: those whose first chunk lies in [C b / n, C (b + 1) / n)
+    // this CTA's groups: those whose cost offset lies in [W b / n, W (b + 1) / n)
     const int NG = a.hdr[kPlanGroups];
-    const int64_t C = a.hdr[kPlanChunks];
-    const int64_t lo = C * b / gridDim.x, hi = C * (b + 1) / gridDim.x;
+    const int64_t W = a.groups[NG].w0;
+    const int64_t lo = W * b / gridDim.x, hi = W * (b + 1) / gridDim.x;
     const int gb = first_group_at(a.groups, NG, lo, lane);
     const int ge = first_group_at(a.groups, NG, hi, lane);
     if (lane == 0) {
@@ -157,10 +152,6 @@ __global__ void __launch_bounds__(kACta, 1)
       tc::mbar_init(&ms->full[s], 1);
       tc::mbar_init(&ms->empty[s], 1);
     }
-    for (int s = 0; s < kASlots; ++s) {
-      tc::mbar_init(&ms->x_full[s], 1);
-      tc::mbar_init(&ms->x_empty[s], 1);
-    }
     ms->abort = 0;
     tc::fence_barrier_init();
   }
@@ -170,9 +161,10 @@ __global__ void __launch_bounds__(kACta, 1)
   volatile int* abort_flag = &ms->abort;
 
   if (warp == kAWarps) {
-    // Producer: per group, its x and da rows into a slot, then its chunks' K and V rows.
+    // Producer: per group, an L2 prefetch of its x and da rows (the consumers load their
+    // fragments from there when they reach the group), then its chunks' K and V rows.
     const uint32_t tx = uint32_t(CH) * 2u * uint32_t(d + dv);
-    int issued = 0, ns = 0;
+    int issued = 0;
     bool ok = true;
     for (int g = ms->gb; ok && g < ms->ge; ++g) {
       const AttendGroup G = a.groups[g];
@@ -186,32 +178,12 @@ __global__ void __launch_bounds__(kACta, 1)
         tl = a.ml[2 * int64_t(tok) + 1];
         td = a.delta[tok];
       }
-      const int xsl = ns % kASlots;
-      int okx = 1;
       if (lane == 0) {
-        okx = tc::mbar_wait_watch(&ms->x_empty[xsl], ((ns / kASlots) & 1) ^ 1, abort_flag, a.st,
-                                  0x100000)
-                  ? 1
-                  : 0;
-        if (okx)
-          tc::mbar_arrive_expect_tx(&ms->x_full[xsl],
-                                    uint32_t(G.mt) * 2u * uint32_t(d + 2 * dv));
+        const int64_t q0 = G.q0;
+        prefetch_l2(a.x_sorted + q0 * d, uint32_t(G.mt) * 2u * uint32_t(d));
+        prefetch_l2(a.da16 + q0 * dv, uint32_t(G.mt) * 2u * uint32_t(dv));
+        prefetch_l2(a.da16_lo + q0 * dv, uint32_t(G.mt) * 2u * uint32_t(dv));
       }
-      if (!__shfl_sync(0xffffffffu, okx, 0)) {
-        ok = false;
-        break;
-      }
-      __syncwarp();
-      if (lane < G.mt) {
-        const uint32_t sb = slots_s + uint32_t(xsl * sh.slot_bytes);
-        bulk_copy(sb + uint32_t(lane * sh.x_row), a.x + int64_t(tok) * d, uint32_t(2 * d),
-                  &ms->x_full[xsl]);
-        bulk_copy(sb + uint32_t(kPlanMT * sh.x_row + lane * sh.da_row), a.da16 + int64_t(tok) * dv,
-                  uint32_t(2 * dv), &ms->x_full[xsl]);
-        bulk_copy(sb + uint32_t(kPlanMT * (sh.x_row + sh.da_row) + lane * sh.da_row),
-                  a.da16_lo + int64_t(tok) * dv, uint32_t(2 * dv), &ms->x_full[xsl]);
-      }
-      ++ns;
       for (int c = 0; c < nc; ++c, ++issued) {
         const int s = issued % S;
         int oke = 1;
@@ -237,7 +209,6 @@ __global__ void __launch_bounds__(kACta, 1)
           m->n = G.n;
           m->c0 = G.c0;
           m->c1 = G.c0 + nc;
-          m->slot = xsl;
         }
         __syncwarp();
         if (lane == 0) {
@@ -255,9 +226,6 @@ __global__ void __launch_bounds__(kACta, 1)
       volatile int no_abort = 0;
       for (int j = issued - S > 0 ? issued - S : 0; j < issued; ++j)
         tc::mbar_wait(&ms->full[j % S], (j / S) & 1, &no_abort, a.st, 0x400000, 100000000ull);
-      for (int j = ns - kASlots > 0 ? ns - kASlots : 0; j < ns; ++j)
-        tc::mbar_wait(&ms->x_full[j % kASlots], (j / kASlots) & 1, &no_abort, a.st, 0x400000,
-                      100000000ull);
     }
     return;
   }
@@ -271,12 +239,12 @@ __global__ void __launch_bounds__(kACta, 1)
   const int nks = d / 16, nksv = dv / 16, ndt = d / 16;
   float acc[DT][4];
   uint32_t bx[KS][2], bda[KSV][2], bdl[KSV][2];
-  int q0 = 0, mt = 0, gn = 0, ngc = 0, x_release = -1;
+  int q0 = 0, mt = 0, gn = 0;
   int64_t gc0 = 0, c_next = -1, i0 = 0, i1 = 0;
   bool ok = true, started = false;
   const int64_t cbase = a.groups[ms->gb].c0;
 
-  auto finish = [&]() {  // dx of the group's tokens += the attention term
+  auto finish = [&]() {  // dx of the group's tokens = the attention term
     const int n0 = 2 * t4, n1 = 2 * t4 + 1;
 #pragma unroll
     for (int mi = 0; mi < DT; ++mi) {
@@ -284,12 +252,12 @@ __global__ void __launch_bounds__(kACta, 1)
       if (!DTW && mtile >= ndt) break;
       const int col0 = 16 * mtile + g8, col1 = col0 + 8;
       if (n0 < mt) {
-        a.dx[i0 * d + col0] += acc[mi][0];
-        a.dx[i0 * d + col1] += acc[mi][2];
+        a.dx[i0 * d + col0] = acc[mi][0];
+        a.dx[i0 * d + col1] = acc[mi][2];
       }
       if (n1 < mt) {
-        a.dx[i1 * d + col0] += acc[mi][1];
-        a.dx[i1 * d + col1] += acc[mi][3];
+        a.dx[i1 * d + col0] = acc[mi][1];
+        a.dx[i1 * d + col1] = acc[mi][3];
       }
     }
   };
@@ -318,41 +286,36 @@ __global__ void __launch_bounds__(kACta, 1)
       started = true;
       i0 = 2 * t4 < mt ? int64_t(m->tok[2 * t4]) : 0;
       i1 = 2 * t4 + 1 < mt ? int64_t(m->tok[2 * t4 + 1]) : 0;
-      const int slot = got ? m->slot : 0;
-      // x and da fragments from the slot (token slots past mt zeroed)
+      // x and da fragments of token g8 of the group (zero past mt): B[k][n] = row n at
+      // columns 16 s + 2 t4 (+1) and 16 s + 8 + 2 t4 (+1)
 #pragma unroll
       for (int i = 0; i < KS; ++i) bx[i][0] = bx[i][1] = 0u;
 #pragma unroll
       for (int i = 0; i < KSV; ++i) bda[i][0] = bda[i][1] = bdl[i][0] = bdl[i][1] = 0u;
-      if (got &&
-          tc::mbar_wait(&ms->x_full[slot], (ngc / kASlots) & 1, abort_flag, a.st, 0x20000)) {
-        const uint32_t sb = slots_s + uint32_t(slot * sh.slot_bytes);
-        const uint32_t xr = sb + uint32_t((lane & 7) * sh.x_row + ((lane >> 3) & 1) * 16);
-        const uint32_t dr =
-            sb + uint32_t(kPlanMT * sh.x_row + (lane & 7) * sh.da_row + ((lane >> 3) & 1) * 16);
-        const uint32_t dl = dr + uint32_t(kPlanMT * sh.da_row);
+      if (g8 < mt) {
+        const int64_t q = q0 + g8;
+        const __nv_bfloat16* xr = a.x_sorted + q * d + 2 * t4;
+        const __nv_bfloat16* dr = a.da16 + q * dv + 2 * t4;
+        const __nv_bfloat16* dl = a.da16_lo + q * dv + 2 * t4;
 #pragma unroll
         for (int i = 0; i < KS; ++i) {
           const int s16 = warp + kAWarps * i;
-          if (KSW || s16 < nks) ldsm_x2(xr + uint32_t(s16 * 32), bx[i][0], bx[i][1]);
+          if (KSW || s16 < nks) {
+            bx[i][0] = ld_u32(xr + 16 * s16);
+            bx[i][1] = ld_u32(xr + 16 * s16 + 8);
+          }
         }
 #pragma unroll
         for (int i = 0; i < KSV; ++i) {
           const int s16 = warp + kAWarps * i;
           if (KSVW || s16 < nksv) {
-            ldsm_x2(dr + uint32_t(s16 * 32), bda[i][0], bda[i][1]);
-            ldsm_x2(dl + uint32_t(s16 * 32), bdl[i][0], bdl[i][1]);
+            bda[i][0] = ld_u32(dr + 16 * s16);
+            bda[i][1] = ld_u32(dr + 16 * s16 + 8);
+            bdl[i][0] = ld_u32(dl + 16 * s16);
+            bdl[i][1] = ld_u32(dl + 16 * s16 + 8);
           }
         }
-        if (g8 >= mt) {
-#pragma unroll
-          for (int i = 0; i < KS; ++i) bx[i][0] = bx[i][1] = 0u;
-#pragma unroll
-          for (int i = 0; i < KSV; ++i) bda[i][0] = bda[i][1] = bdl[i][0] = bdl[i][1] = 0u;
-        }
-        x_release = slot;
       }
-      ++ngc;
 #pragma unroll
       for (int mi = 0; mi < DT; ++mi) acc[mi][0] = acc[mi][1] = acc[mi][2] = acc[mi][3] = 0.f;
     }
@@ -366,10 +329,6 @@ __global__ void __launch_bounds__(kACta, 1)
     if (*abort_flag) {
       ok = false;
       break;
-    }
-    if (x_release >= 0) {  // every warp holds its fragments
-      if (tid == 0) tc::mbar_arrive(&ms->x_empty[x_release]);
-      x_release = -1;
     }
     const uint32_t st0 = ring_s + uint32_t((k % S) * sh.stage_bytes);
     const uint32_t st1 = pair ? ring_s + uint32_t(((k + 1) % S) * sh.stage_bytes) : st0;
@@ -505,36 +464,84 @@ __global__ void __launch_bounds__(kACta, 1)
 
 constexpr int kBRows = 64;   // table rows per unit
 constexpr int kBCols = 256;  // output columns per unit
+constexpr int kBTok = 32;    // tokens per step
 constexpr int kBThreads = 256;
-constexpr int kYld = kBCols + 8;  // bf16 row stride of the token tile (conflict-free)
-constexpr int kWld = 24;          // bf16 row stride of the weight tiles
+constexpr int kYld = kBCols + 8;  // bf16 row stride of the token tile (ldmatrix rows 528 B apart)
+constexpr int kWld = kBTok + 8;   // bf16 row stride of the weight tiles (80 B apart)
+constexpr int kBUnitFixed = 2;    // cost of a unit's setup and stores, in steps
+
+struct SegSmem {
+  __nv_bfloat16 ys[2][kBTok][kYld];   // Y rows of the step's tokens, double-buffered
+  __nv_bfloat16 wh[2][kBRows][kWld];  // W transposed (row, token), bf16 hi
+  __nv_bfloat16 wl[2][kBRows][kWld];  // and lo
+};
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool full) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(tc::smem_u32(dst)),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(full ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
 
 // One unit: segment s, rows [r0, r0 + 64) of its id, columns [col0, col0 + 256) of dK
-// (part 0) or dV (part 1). D[col][row] = sum_q Y[q][col] W[q][row] over the segment's
-// sorted positions q, Y = x (dK) or da (dV), W = ds (dK) or p (dV).
-__global__ void __launch_bounds__(kBThreads) seg_rows_kernel(const SegRowsArgs a) {
-  __shared__ __align__(16) __nv_bfloat16 ys[16][kYld];
-  __shared__ __align__(16) __nv_bfloat16 wh[kBRows][kWld];
-  __shared__ __align__(16) __nv_bfloat16 wl[kBRows][kWld];
+// (part 0) or dV (part 1). D[row][col] = sum_q W[q][row] Y[q][col] over the segment's
+// sorted positions q, Y = x (dK) or da (dV), W = ds (dK) or p (dV). A step takes 32 tokens:
+// Y by cp.async into one of two buffers, W through registers (split into bf16 hi + lo and
+// transposed into one of two buffers), so one barrier a step suffices. Warp w owns columns
+// [32 w, 32 w + 32) of the unit and all 64 rows.
+__global__ void __launch_bounds__(kBThreads, 2) seg_rows_kernel(const SegRowsArgs a) {
+  extern __shared__ __align__(128) unsigned char seg_smem_raw[];
+  SegSmem& sm = *reinterpret_cast<SegSmem*>(seg_smem_raw);
+  __shared__ int s_first[2];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g8 = lane >> 2, t4 = lane & 3;
   const int S = *a.n_seg;
-  const int64_t units = a.seg_unit0[S];
   const int ncb_k = (a.d + kBCols - 1) / kBCols, ncb_v = (a.d_v + kBCols - 1) / kBCols;
   const int ncb = ncb_k + ncb_v;
-  for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
-    // segment of unit u: the last s with seg_unit0[s] <= u
-    int lo = 0, hi = S - 1;
+  // This CTA's units: those whose cost interval starts in [C b / G, C (b + 1) / G) of the
+  // total cost C (a unit of segment s costs ceil(tokens / 32) + kBUnitFixed). The first is
+  // found by one binary search; the rest follow in order.
+  const int64_t C = a.seg_cost0[S];
+  const int64_t clo = C * blockIdx.x / gridDim.x, chi = C * (blockIdx.x + 1) / gridDim.x;
+  if (tid == 0) {
+    int lo = 0, hi = S;  // first segment whose cost interval ends past clo
     while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (a.seg_unit0[mid] <= u)
-        lo = mid;
+      const int mid = (lo + hi) >> 1;
+      if (a.seg_cost0[mid + 1] <= clo)
+        lo = mid + 1;
       else
-        hi = mid - 1;
+        hi = mid;
     }
-    const int s = lo;
-    const int64_t local = u - a.seg_unit0[s];
+    s_first[0] = lo;
+    int k0 = 0;
+    if (lo < S) {
+      const int64_t uc = (a.seg_cost0[lo + 1] - a.seg_cost0[lo]) /
+                         (a.seg_unit0[lo + 1] - a.seg_unit0[lo]);  // cost of each unit
+      k0 = int((clo - a.seg_cost0[lo] + uc - 1) / uc);  // first unit starting at or after clo
+    }
+    s_first[1] = k0;
+  }
+  __syncthreads();
+  int s = s_first[0];
+  int64_t local = s_first[1];
+  // W loads: row wr of the unit, tokens 8 wg .. 8 wg + 7 of the step
+  const int wr = tid & 63, wg = tid >> 6;
+  while (s < S) {
+    const int64_t nu = a.seg_unit0[s + 1] - a.seg_unit0[s];
+    if (local >= nu) {
+      ++s;
+      local = 0;
+      continue;
+    }
+    const int64_t uc = (a.seg_cost0[s + 1] - a.seg_cost0[s]) / nu;
+    if (a.seg_cost0[s] + local * uc >= chi) break;
     const int rb = int(local / ncb), cb = int(local % ncb);
+    ++local;
     const int part = cb < ncb_k ? 0 : 1;
     const int width = part ? a.d_v : a.d;
     const int col0 = (part ? cb - ncb_k : cb) * kBCols;
@@ -554,81 +561,94 @@ __global__ void __launch_bounds__(kBThreads) seg_rows_kernel(const SegRowsArgs a
         else
           atomicOr(&a.st->capacity, 1);
       }
-    float acc[2][8][4];
+    const bool wcols = col0 + 32 * warp < width;  // the warp's 32 columns exist (width % 64 == 0)
+    float acc[4][4][4];
 #pragma unroll
-    for (int mi = 0; mi < 2; ++mi)
+    for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
-      for (int nt = 0; nt < 8; ++nt) acc[mi][nt][0] = acc[mi][nt][1] = acc[mi][nt][2] = acc[mi][nt][3] = 0.f;
-    // tile loads: thread tid takes token tid / 16: 16 columns (two 16-byte pieces) of Y and
-    // 4 rows of W
-    const int lt = tid >> 4, lc = (tid & 15) * 16, lr = (tid & 15) * 4;
-    uint4 yv[2];
-    float wv[4];
-    auto load = [&](int q) {  // tile of tokens q .. q + 15
-      const int qq = q + lt;
-      yv[0] = yv[1] = make_uint4(0, 0, 0, 0);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) wv[j] = 0.f;
-      if (qq < qe) {
-        const int c = col0 + lc;
-        const __nv_bfloat16* yr = Y + int64_t(qq) * width + c;
-        if (c < width) yv[0] = __ldg(reinterpret_cast<const uint4*>(yr));
-        if (c + 8 < width) yv[1] = __ldg(reinterpret_cast<const uint4*>(yr + 8));
-        const float* wr = Wsrc + int64_t(qq) * a.k_max + r0 + lr;
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (r0 + lr + j < n) wv[j] = __ldg(wr + j);
-      }
-    };
-    load(qs);
-    for (int q = qs; q < qe; q += 16) {
-      *reinterpret_cast<uint4*>(&ys[lt][lc]) = yv[0];
-      *reinterpret_cast<uint4*>(&ys[lt][lc + 8]) = yv[1];
+      for (int nt = 0; nt < 4; ++nt) acc[mt][nt][0] = acc[mt][nt][1] = acc[mt][nt][2] = acc[mt][nt][3] = 0.f;
+    auto load_y = [&](int q, int buf) {  // tokens q .. q + 31: 1024 pieces of 16 bytes
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const __nv_bfloat16 h = __float2bfloat16_rn(wv[j]);
-        wh[lr + j][lt] = h;
-        wl[lr + j][lt] = __float2bfloat16_rn(wv[j] - __bfloat162float(h));
+        const int pc = tid + kBThreads * j;
+        const int tk = pc >> 5, cp = (pc & 31) * 8;
+        const bool ok = q + tk < qe && col0 + cp < width;
+        const __nv_bfloat16* src = ok ? Y + int64_t(q + tk) * width + col0 + cp : Y;
+        cp_async16(&sm.ys[buf][tk][cp], src, ok);
       }
-      __syncthreads();
-      if (q + 16 < qe) load(q + 16);  // the next tile is in flight during the products
-      // warp w: column tiles 2w, 2w + 1 (16 columns each), all 8 row tiles
-      const int vl = (lane & 7) + (lane >> 4) * 8;
-      const int vcol = ((lane >> 3) & 1) * 8;
+      cp_async_commit();
+    };
+    float wv[8];
+    auto load_w = [&](int q) {
+      const bool rv = r0 + wr < n;
 #pragma unroll
-      for (int mi = 0; mi < 2; ++mi) {
-        const int cl = 16 * (2 * warp + mi);
-        if (col0 + cl >= width) break;
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4_t(tc::smem_u32(&ys[vl][cl + vcol]), a0, a1, a2, a3);
+      for (int j = 0; j < 8; ++j) {
+        const int qq = q + 8 * wg + j;
+        wv[j] = (rv && qq < qe) ? __ldg(Wsrc + int64_t(qq) * a.k_max + r0 + wr) : 0.f;
+      }
+    };
+    auto store_w = [&](int buf) {
+      uint32_t h[4], l[4];
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
-          const int row = 8 * nt + g8;
-          const uint32_t h0 = *reinterpret_cast<const uint32_t*>(&wh[row][2 * t4]);
-          const uint32_t h1 = *reinterpret_cast<const uint32_t*>(&wh[row][2 * t4 + 8]);
-          const uint32_t l0 = *reinterpret_cast<const uint32_t*>(&wl[row][2 * t4]);
-          const uint32_t l1 = *reinterpret_cast<const uint32_t*>(&wl[row][2 * t4 + 8]);
-          mma16(acc[mi][nt], a0, a1, a2, a3, h0, h1);
-          mma16(acc[mi][nt], a0, a1, a2, a3, l0, l1);
+      for (int j = 0; j < 4; ++j) split_pair(wv[2 * j], wv[2 * j + 1], h[j], l[j]);
+      *reinterpret_cast<uint4*>(&sm.wh[buf][wr][8 * wg]) = make_uint4(h[0], h[1], h[2], h[3]);
+      *reinterpret_cast<uint4*>(&sm.wl[buf][wr][8 * wg]) = make_uint4(l[0], l[1], l[2], l[3]);
+    };
+    load_y(qs, 0);
+    load_w(qs);
+    store_w(0);
+    int buf = 0;
+    for (int q = qs; q < qe; q += kBTok, buf ^= 1) {
+      cp_async_wait_all();
+      __syncthreads();  // step q's tiles are in place; every warp is past the previous step
+      const bool more = q + kBTok < qe;
+      if (more) {
+        load_y(q + kBTok, buf ^ 1);
+        load_w(q + kBTok);
+      }
+      if (wcols) {
+#pragma unroll
+        for (int ks = 0; ks < kBTok / 16; ++ks) {
+          uint32_t b[4][2];
+          const int yt = 16 * ks + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+          for (int pr = 0; pr < 2; ++pr) {
+            const int yc = 32 * warp + 16 * pr + ((lane >> 4) & 1) * 8;
+            ldsm_x4_t(tc::smem_u32(&sm.ys[buf][yt][yc]), b[2 * pr][0], b[2 * pr][1],
+                      b[2 * pr + 1][0], b[2 * pr + 1][1]);
+          }
+          const int ar = lane & 15, ak = 16 * ks + (lane >> 4) * 8;
+#pragma unroll
+          for (int mt = 0; mt < 4; ++mt) {
+            uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
+            ldsm_x4(tc::smem_u32(&sm.wh[buf][16 * mt + ar][ak]), h0, h1, h2, h3);
+            ldsm_x4(tc::smem_u32(&sm.wl[buf][16 * mt + ar][ak]), l0, l1, l2, l3);
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+              mma16(acc[mt][nt], h0, h1, h2, h3, b[nt][0], b[nt][1]);
+              mma16(acc[mt][nt], l0, l1, l2, l3, b[nt][0], b[nt][1]);
+            }
+          }
         }
       }
-      __syncthreads();
+      if (more) store_w(buf ^ 1);
     }
-    // D[col][row]: lane (g8, t4) holds cols cl + g8 (+ 8) and rows 8 nt + 2 t4 (+ 1)
+    __syncthreads();  // the buffers are free for the next unit
+    // D[row][col]: lane (g8, t4) holds rows 16 mt + g8 (+ 8), columns 8 nt + 2 t4 (+ 1)
+    if (wcols) {
 #pragma unroll
-    for (int mi = 0; mi < 2; ++mi) {
-      const int c0 = col0 + 16 * (2 * warp + mi) + g8;
-      if (col0 + 16 * (2 * warp + mi) >= width) break;
+      for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-        const int rr = 8 * nt + 2 * t4;
+        for (int hr = 0; hr < 2; ++hr) {
+          const int row = 16 * mt + g8 + 8 * hr;
+          if (r0 + row < n && orow0 + row < a.max_rows) {
+            float* o = out + (orow0 + row) * width + col0 + 32 * warp + 2 * t4;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int row = rr + (e & 1), col = c0 + (e >> 1) * 8;
-          if (r0 + row < n && orow0 + row < a.max_rows)
-            out[(orow0 + row) * width + col] = acc[mi][nt][e];
+            for (int nt = 0; nt < 4; ++nt)
+              *reinterpret_cast<float2*>(o + 8 * nt) =
+                  make_float2(acc[mt][nt][2 * hr], acc[mt][nt][2 * hr + 1]);
+          }
         }
-      }
     }
   }
 }
@@ -700,13 +720,12 @@ __global__ void split_hilo_kernel(const float* __restrict__ src, int64_t n,
   }
 }
 
-// Per sorted position q (one warp): x and da rows in sorted order (bf16), da in batch order
-// as bf16 hi + lo, and δ_i = a_i · da_i for the token i = perm(q).
+// Per sorted position q (one warp): the x row and da as bf16 hi + lo in sorted order, and
+// δ_i = a_i · da_i for the token i = perm(q).
 __global__ void bwd_prep_kernel(const uint64_t* __restrict__ keys, int64_t T,
                                 const __nv_bfloat16* __restrict__ x, const float* __restrict__ a,
                                 const float* __restrict__ da, int d, int d_v,
                                 __nv_bfloat16* __restrict__ x_sorted,
-                                __nv_bfloat16* __restrict__ da_sorted,
                                 __nv_bfloat16* __restrict__ da16,
                                 __nv_bfloat16* __restrict__ da16_lo, float* __restrict__ delta) {
   const int lane = threadIdx.x & 31;
@@ -721,9 +740,8 @@ __global__ void bwd_prep_kernel(const uint64_t* __restrict__ keys, int64_t T,
     const float g = da[i * d_v + c];
     dot = fmaf(a[i * d_v + c], g, dot);
     const __nv_bfloat16 gb = __float2bfloat16_rn(g);
-    da_sorted[q * d_v + c] = gb;
-    da16[i * d_v + c] = gb;
-    da16_lo[i * d_v + c] = __float2bfloat16_rn(g - __bfloat162float(gb));
+    da16[q * d_v + c] = gb;
+    da16_lo[q * d_v + c] = __float2bfloat16_rn(g - __bfloat162float(gb));
   }
   dot = warp_sum(dot);
   if (lane == 0) delta[i] = dot;
@@ -736,20 +754,31 @@ __global__ void __launch_bounds__(1024) row_plan_kernel(const uint64_t* __restri
                                                         const int32_t* __restrict__ n_seg,
                                                         const int32_t* __restrict__ offs, int ncb,
                                                         int32_t* seg_row0, int32_t* seg_unit0,
-                                                        int32_t* n_rows, int64_t max_rows,
-                                                        DevStatus* st) {
+                                                        int64_t* seg_cost0, int32_t* n_rows,
+                                                        int64_t max_rows, DevStatus* st) {
   __shared__ int2 wt[32];
   __shared__ int2 tot;
+  __shared__ long long wc[32];
+  __shared__ long long totc;
   const int S = *n_seg;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  int64_t carry_r = 0, carry_u = 0;
+  int64_t carry_r = 0, carry_u = 0, carry_c = 0;
   for (int base = 0; base < S; base += blockDim.x) {
     const int s = base + threadIdx.x;
     int nr = 0, nu = 0;
+    long long nc = 0;
     if (s < S) {
-      const int t = int(keys[seg_start[s]] >> 32);
+      const int q0 = seg_start[s];
+      const int t = int(keys[q0] >> 32);
       nr = offs[t + 1] - offs[t];
       nu = (nr + kBRows - 1) / kBRows * ncb;
+      nc = (long long)nu * ((seg_start[s + 1] - q0 + kBTok - 1) / kBTok + kBUnitFixed);
+    }
+    long long inc = nc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long u = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += u;
     }
     int2 incl = make_int2(nr, nu);
 #pragma unroll
@@ -761,9 +790,21 @@ __global__ void __launch_bounds__(1024) row_plan_kernel(const uint64_t* __restri
         incl.y += uy;
       }
     }
-    if (lane == 31) wt[wid] = incl;
+    if (lane == 31) {
+      wt[wid] = incl;
+      wc[wid] = inc;
+    }
     __syncthreads();
     if (wid == 0) {
+      const long long wcv = wc[lane];
+      long long wci = wcv;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long u = __shfl_up_sync(0xffffffffu, wci, o);
+        if (lane >= o) wci += u;
+      }
+      wc[lane] = wci - wcv;
+      if (lane == 31) totc = wci;
       const int2 w = wt[lane];
       int2 wi = w;
 #pragma unroll
@@ -782,13 +823,16 @@ __global__ void __launch_bounds__(1024) row_plan_kernel(const uint64_t* __restri
     if (s < S) {
       seg_row0[s] = int32_t(carry_r + wt[wid].x + incl.x - nr);
       seg_unit0[s] = int32_t(carry_u + wt[wid].y + incl.y - nu);
+      seg_cost0[s] = carry_c + wc[wid] + inc - nc;
     }
     carry_r += tot.x;
     carry_u += tot.y;
+    carry_c += totc;
     __syncthreads();
   }
   if (threadIdx.x == 0) {
     seg_unit0[S] = int32_t(carry_u);
+    seg_cost0[S] = carry_c;
     *n_rows = int32_t(carry_r);
     if (carry_r > max_rows) atomicOr(&st->capacity, 1);
   }
@@ -814,8 +858,8 @@ cudaError_t launch_attend_bwd_rows(const AttendBwdRowsArgs& a, cudaStream_t stre
   const BShape sh = bwd_shape(a.d, a.d_v);
   if (sh.stages < 2 || sh.smem > kASmemLimit || sh.ch != a.ch || a.d % 64 || a.d_v % 64 ||
       a.d > 16 * kAWarps * kAMaxKS || a.d_v > 16 * kAWarps * kAMaxKSV ||
-      (reinterpret_cast<uintptr_t>(a.x) & 15) || (reinterpret_cast<uintptr_t>(a.da16) & 15) ||
-      (reinterpret_cast<uintptr_t>(a.da16_lo) & 15))
+      (reinterpret_cast<uintptr_t>(a.x_sorted) & 15) ||
+      (reinterpret_cast<uintptr_t>(a.da16) & 15) || (reinterpret_cast<uintptr_t>(a.da16_lo) & 15))
     return cudaErrorInvalidValue;
   if (sh.ch == 8 && a.d == 2048 && a.d_v == 512) return launch_bwd_a<8, 16, 4, 16>(a, sh, stream);
   if (sh.ch == 16 && a.d == 1024 && a.d_v == 256) return launch_bwd_a<16, 8, 2, 8>(a, sh, stream);
@@ -824,7 +868,10 @@ cudaError_t launch_attend_bwd_rows(const AttendBwdRowsArgs& a, cudaStream_t stre
 }
 
 cudaError_t launch_seg_rows(const SegRowsArgs& a, cudaStream_t stream) {
-  seg_rows_kernel<<<unsigned(device_sm_count() * 4), kBThreads, 0, stream>>>(a);
+  if (a.d % 64 || a.d_v % 64) return cudaErrorInvalidValue;
+  const cudaError_t attr = ensure_smem_attr(seg_rows_kernel, int(sizeof(SegSmem)));
+  if (attr != cudaSuccess) return attr;
+  seg_rows_kernel<<<unsigned(device_sm_count() * 2), kBThreads, sizeof(SegSmem), stream>>>(a);
   count_launch();
   return cudaGetLastError();
 }
@@ -835,11 +882,11 @@ int seg_rows_col_blocks(int d, int d_v) {
 
 cudaError_t launch_row_plan(const uint64_t* keys, const int32_t* seg_start, const int32_t* n_seg,
                             const int32_t* offs, int d, int d_v, int32_t* seg_row0,
-                            int32_t* seg_unit0, int32_t* n_rows, int64_t max_rows,
-                            DevStatus* st, cudaStream_t stream) {
+                            int32_t* seg_unit0, int64_t* seg_cost0, int32_t* n_rows,
+                            int64_t max_rows, DevStatus* st, cudaStream_t stream) {
   row_plan_kernel<<<1, 1024, 0, stream>>>(keys, seg_start, n_seg, offs,
                                           seg_rows_col_blocks(d, d_v), seg_row0, seg_unit0,
-                                          n_rows, max_rows, st);
+                                          seg_cost0, n_rows, max_rows, st);
   count_launch();
   return cudaGetLastError();
 }
@@ -854,8 +901,7 @@ cudaError_t launch_bwd_small(const BwdSmallArgs& a, cudaStream_t stream) {
                                                        a.du, a.du_lo);
   } else if (a.stage == 2) {
     bwd_prep_kernel<<<rows_grid, 256, 0, stream>>>(a.keys, a.T, a.x, a.a, a.da, a.d, a.d_v,
-                                                   a.x_sorted, a.da_sorted, a.da16, a.da16_lo,
-                                                   a.delta);
+                                                   a.x_sorted, a.da16, a.da16_lo, a.delta);
   } else {
     const int64_t n = a.T * a.d_v;
     int64_t g = (n + 255) / 256;

@@ -268,12 +268,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t acc0 = lane_base + uint32_t(int(b) * NACC * BN);
       if (SWAP && SPLIT) {
         // split-K part, transposed problem: row m is an output feature, columns are tokens;
-        // raw accumulators to slab[(part NACC + acc) M + m][N] (columns past N not stored)
+        // raw accumulators to slab[(part NACC + acc) N + n][M], token-major, so that the
+        // lanes of a warp (consecutive features) store consecutive floats
         const int part = u / tiles;
 #pragma unroll
         for (int acc = 0; acc < NACC; ++acc) {
           const bool has = NACC == 1 || (acc == 0 ? k_lo < p.kb1 : k_hi > p.kb1);
-          float* dst = p.slab + ((int64_t(part) * NACC + acc) * p.M + m) * p.N + n0;
+          float* dst = p.slab + (int64_t(part) * NACC + acc) * p.N * p.M + m;
           for (int c = 0; c < BN / 32; ++c) {
             if (c * 32 >= ncols) break;
             float v[32];
@@ -286,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (row_ok)
 #pragma unroll
               for (int j = 0; j < 32; ++j)
-                if (c * 32 + j < ncols) dst[c * 32 + j] = v[j];
+                if (c * 32 + j < ncols) dst[int64_t(n0 + c * 32 + j) * p.M] = v[j];
           }
         }
       } else if (SWAP) {
@@ -620,10 +621,9 @@ __global__ void splitk_mix_finish_kernel(const float* __restrict__ slab, int par
 }
 
 // Split-K finish of the transposed GEMM-mix (batches of at most 64 tokens): slab holds
-// [part][acc][feature][token]; y[token][feature] = rstd (sum acc0 - mu colsum) + sum acc1
+// [part][acc][token][feature]; y[token][feature] = rstd (sum acc0 - mu colsum) + sum acc1
 // with the token's mu / rstd merged from the transposed GEMM-up's per-128-feature
-// statistics. A CTA takes 32 features of every token: threads read along the tokens, and a
-// shared tile turns the result so that y is written along its rows.
+// statistics. A CTA takes one token; each thread eight consecutive features.
 constexpr int kSwapTok = 64;
 __global__ void __launch_bounds__(256) splitk_mix_swap_finish_kernel(
     const float* __restrict__ slab, int parts, int M, int N, const float* __restrict__ stats_in,
@@ -631,62 +631,60 @@ __global__ void __launch_bounds__(256) splitk_mix_swap_finish_kernel(
     int y_dtype, float* mu_out, float* rstd_out) {
   grid_dep_wait();
   grid_dep_release();
-  __shared__ float s_mean[kSwapTok], s_rstd[kSwapTok];
-  __shared__ float sy[kSwapTok][33];
-  const int tid = threadIdx.x;
-  const int f0 = blockIdx.x * 32;
-  if (tid < N) {
+  __shared__ float s_mr[2];
+  const int n = blockIdx.x, tid = threadIdx.x;
+  if (tid < 32) {
     float tot = 0.f;
-#pragma unroll 4
-    for (int j = 0; j < stat_tiles; ++j) tot += stats_in[(int64_t(j) * N + tid) * 2];
+    for (int j = tid; j < stat_tiles; j += 32) tot += stats_in[(int64_t(j) * N + n) * 2];
+    tot = warp_sum(tot);
     const float mean = tot / float(M);
     float m2 = 0.f;
-#pragma unroll 4
-    for (int j = 0; j < stat_tiles; ++j) {
-      const float* st = stats_in + (int64_t(j) * N + tid) * 2;
+    for (int j = tid; j < stat_tiles; j += 32) {
+      const float* st = stats_in + (int64_t(j) * N + n) * 2;
       const int cnt = M - j * stat_bn < stat_bn ? M - j * stat_bn : stat_bn;
       const float dm = st[0] / float(cnt) - mean;
       m2 += st[1] + float(cnt) * dm * dm;
     }
-    const float rstd = 1.f / sqrtf(m2 / float(M) + eps);
-    s_mean[tid] = mean;
-    s_rstd[tid] = rstd;
-    if (blockIdx.x == 0 && mu_out) {
-      mu_out[tid] = mean;
-      rstd_out[tid] = rstd;
+    m2 = warp_sum(m2);
+    if (tid == 0) {
+      const float rstd = 1.f / sqrtf(m2 / float(M) + eps);
+      s_mr[0] = mean;
+      s_mr[1] = rstd;
+      if (mu_out) {
+        mu_out[n] = mean;
+        rstd_out[n] = rstd;
+      }
     }
   }
   __syncthreads();
-  const int fl = tid >> 3, nb = (tid & 7) * 8, f = f0 + fl;
-  if (f < M) {
-    float v0[8], v1[8];
+  const int f = 8 * tid;
+  if (f >= M) return;
+  const float mean = s_mr[0], rstd = s_mr[1];
+  float v0[8], v1[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) v0[j] = v1[j] = 0.f;
+  for (int j = 0; j < 8; ++j) v0[j] = v1[j] = 0.f;
 #pragma unroll 4
-    for (int s = 0; s < parts; ++s) {
-      const float* a = slab + ((int64_t(s) * 2) * M + f) * N;
-      const float* b = slab + ((int64_t(s) * 2 + 1) * M + f) * N;
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (nb + j < N) {
-          v0[j] += __ldcg(a + nb + j);
-          v1[j] += __ldcg(b + nb + j);
-        }
-    }
-    const float c = __ldg(colsum + f);
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (nb + j < N) sy[nb + j][fl] = fmaf(s_rstd[nb + j], v0[j] - s_mean[nb + j] * c, v1[j]);
+  for (int s = 0; s < parts; ++s) {
+    const float4* a = reinterpret_cast<const float4*>(slab + ((int64_t(s) * 2) * N + n) * M + f);
+    const float4* b =
+        reinterpret_cast<const float4*>(slab + ((int64_t(s) * 2 + 1) * N + n) * M + f);
+    const float4 a0 = __ldcg(a), a1 = __ldcg(a + 1), b0 = __ldcg(b), b1 = __ldcg(b + 1);
+    v0[0] += a0.x; v0[1] += a0.y; v0[2] += a0.z; v0[3] += a0.w;
+    v0[4] += a1.x; v0[5] += a1.y; v0[6] += a1.z; v0[7] += a1.w;
+    v1[0] += b0.x; v1[1] += b0.y; v1[2] += b0.z; v1[3] += b0.w;
+    v1[4] += b1.x; v1[5] += b1.y; v1[6] += b1.z; v1[7] += b1.w;
   }
-  __syncthreads();
-  for (int idx = tid; idx < N * 32; idx += 256) {
-    const int n = idx >> 5, fc = idx & 31;
-    if (f0 + fc >= M) continue;
-    const int64_t o = int64_t(n) * M + f0 + fc;
-    if (y_dtype == L3_BF16)
-      static_cast<__nv_bfloat16*>(Y)[o] = __float2bfloat16_rn(sy[n][fc]);
-    else
-      static_cast<float*>(Y)[o] = sy[n][fc];
+  float y[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) y[j] = fmaf(rstd, v0[j] - mean * __ldg(colsum + f + j), v1[j]);
+  if (y_dtype == L3_BF16) {
+    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(Y) + int64_t(n) * M + f) =
+        make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]),
+                   pack_bf16(y[6], y[7]));
+  } else {
+    float4* d = reinterpret_cast<float4*>(static_cast<float*>(Y) + int64_t(n) * M + f);
+    d[0] = make_float4(y[0], y[1], y[2], y[3]);
+    d[1] = make_float4(y[4], y[5], y[6], y[7]);
   }
 }
 
@@ -820,7 +818,7 @@ cudaError_t launch_tc_mix(const __nv_bfloat16* U, const __nv_bfloat16* x,
     p.slab = slab;
     cudaError_t e = launch_tc<kSwapBN, 2, 6, true, true>(mw, mw, mu, mx, p, stream);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(splitk_mix_swap_finish_kernel, dim3(unsigned((d + 31) / 32)), dim3(256), 0,
+    e = launch_pdl(splitk_mix_swap_finish_kernel, dim3(unsigned(T)), dim3(256), 0,
                    stream, slab, parts, d, int(T), stats, tc_up_stat_tiles(d), int(kBM), colsum,
                    eps, y, y_dtype, mu_out, rstd_out);
     count_launch();

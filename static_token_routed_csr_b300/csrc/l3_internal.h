@@ -277,12 +277,12 @@ struct AttendBwdRowsArgs {
   const void* V;
   int64_t v;
   int d, d_v, ch, k_max;
-  const __nv_bfloat16* x;     // [T, d] batch order
-  const __nv_bfloat16* da16;     // [T, d_v] batch order, bf16(da)
-  const __nv_bfloat16* da16_lo;  // [T, d_v] bf16(da - bf16(da))
+  const __nv_bfloat16* x_sorted;  // [T, d] sorted order
+  const __nv_bfloat16* da16;      // [T, d_v] sorted order, bf16(da)
+  const __nv_bfloat16* da16_lo;   // [T, d_v] sorted order, bf16(da - bf16(da))
   const float* ml;            // [T, 2] the forward's (max score, denominator)
   const float* delta;         // [T] a_i . da_i
-  float* dx;                  // [T, d]: holds the direct term; the attention term is added
+  float* dx;                  // [T, d]: receives the attention term (batch order)
   float* p_buf;               // [T, k_max] by sorted position and row within the id
   float* ds_buf;              // [T, k_max]
   int n_cta;
@@ -298,6 +298,7 @@ struct SegRowsArgs {
   const int32_t* offs;
   const int32_t* seg_row0;   // [S] first output row of each segment
   const int32_t* seg_unit0;  // [S + 1] first work unit of each segment
+  const int64_t* seg_cost0;  // [S + 1] cost (k-steps) of the units before each segment
   const __nv_bfloat16* x_sorted;   // [T, d]
   const __nv_bfloat16* da_sorted;  // [T, d_v]
   const float* p_buf;
@@ -313,8 +314,8 @@ int seg_rows_col_blocks(int d, int d_v);
 cudaError_t launch_seg_rows(const SegRowsArgs& a, cudaStream_t stream);
 cudaError_t launch_row_plan(const uint64_t* keys, const int32_t* seg_start, const int32_t* n_seg,
                             const int32_t* offs, int d, int d_v, int32_t* seg_row0,
-                            int32_t* seg_unit0, int32_t* n_rows, int64_t max_rows,
-                            DevStatus* st, cudaStream_t stream);
+                            int32_t* seg_unit0, int64_t* seg_cost0, int32_t* n_rows,
+                            int64_t max_rows, DevStatus* st, cudaStream_t stream);
 // Row kernels of the backward: stage 0: LayerNorm of the fp32 U (h over U, h16, rstd);
 // stage 1: du = LayerNorm backward of dh as bf16 hi + lo; stage 2: x and da in sorted
 // order, da as bf16 hi + lo, delta = a . da; stage 3: a as bf16 hi + lo.
@@ -334,7 +335,6 @@ struct BwdSmallArgs {
   const float* a;
   const float* da;
   __nv_bfloat16* x_sorted;
-  __nv_bfloat16* da_sorted;
   __nv_bfloat16* da16;
   __nv_bfloat16* da16_lo;
   float* delta;

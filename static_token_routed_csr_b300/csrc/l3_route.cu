@@ -184,7 +184,7 @@ __device__ void plan_pass(const uint64_t* keys, int64_t T, const int32_t* seg_st
       g.row0 = row0;
       g.n = n;
       g.c0 = ccarry + cex + k * per;
-      g.w0 = g.c0 * pl.w_chunk + (per > 0 ? wcarry + wex + k : 0) * pl.w_group;
+      g.w0 = g.c0 * pl.w_chunk + (wcarry + wex + (per > 0 ? k : 0)) * pl.w_group;
       g.pad = 0;
 #pragma unroll
       for (int j = 0; j < kPlanMT; ++j)
@@ -472,6 +472,7 @@ __device__ int block_radix_sort(RadixSmem& sm, int passes, int nw) {
 // bits set (they sort last). Ids outside [0, vocab) are reported and treated as id 0.
 __device__ void radix_load(RadixSmem& sm, const int32_t* ids, int64_t T, int64_t vocab,
                            int64_t base, DevStatus* st, int n) {
+#pragma unroll 8
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
     uint32_t key = 0xffffffffu;
     if (base + i < T) {
