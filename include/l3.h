@@ -56,7 +56,8 @@ typedef enum l3_status {
   L3_ERR_CUDA = 6,        /* a CUDA runtime call failed                                 */
   L3_ERR_LAYER = 7,       /* offsets not 0 = offs[0] < ... < offs[vocab] = v, or a range
                              longer than k_max                           (device-found) */
-  L3_ERR_TIMEOUT = 8      /* a bounded device-side wait gave up          (device-found) */
+  L3_ERR_TIMEOUT = 8      /* a bounded device-side wait gave up, or a kernel found its
+                             work plan inconsistent and stopped          (device-found) */
 } l3_status;
 
 enum { L3_F32 = 0, L3_BF16 = 1 };

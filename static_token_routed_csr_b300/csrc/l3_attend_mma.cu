@@ -101,6 +101,14 @@ MmaShape mma_shape(int d, int d_v) {
 }
 
 
+// t[j] for j < 8 held in registers (a select chain, no local memory).
+__device__ __forceinline__ int pick8(const int32_t (&t)[kMT], int j) {
+  int v = t[0];
+#pragma unroll
+  for (int i = 1; i < kMT; ++i) v = j == i ? t[i] : v;
+  return v;
+}
+
 // Barrier of the kThreads consumer threads (named barrier 1; the producer warp is not in it).
 __device__ __forceinline__ void cbar() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
 
@@ -127,8 +135,18 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
   }
   grid_dep_wait();  // the routing kernel's plan is complete
   grid_dep_release();
-  const int64_t cb = a.cta_start[b], ce = a.cta_start[b + 1];
+  // The CTA's head (one 80-byte read by every thread): its chunk range and the group that
+  // holds its first chunk, so that the copies and the first group's x loads start at once.
+  const CtaHead hd = a.cta_head[b];
+  const int total_chunks = a.hdr[kPlanChunks];
+  const int64_t cb = hd.cb, ce = hd.ce;
   if (cb >= ce) return;
+  if (hd.mt < 1 || hd.mt > kMT || hd.q0 < 0 || int64_t(hd.q0) + hd.mt > a.T || cb < hd.c0 ||
+      cb >= hd.c1 || ce > total_chunks) {
+    // an inconsistent plan (never expected): nothing is read or written
+    if (tid == 0) atomicOr(&a.st->timeout, 0x1000000);
+    return;
+  }
   const int nk = int(ce - cb);
   const int d = a.d, dv = a.d_v, S = sh.stages;
   const __nv_bfloat16* __restrict__ Xg = static_cast<const __nv_bfloat16*>(a.x);
@@ -156,16 +174,13 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
     // The plan's group list is read 32 groups at a time (lane l holds group w0 + l) and the
     // current group's fields are taken from the window by shuffles.
     const uint32_t tx = uint32_t(CH) * 2u * uint32_t(d + dv);
-    // The range's first group comes from the plan's head for this CTA (one 64-byte read):
-    // the copies of its first chunks go out at once; the group list is read meanwhile.
-    const int hv = lane < 16 ? reinterpret_cast<const int32_t*>(&a.cta_head[b])[lane] : 0;
-    int pg = __shfl_sync(0xffffffffu, hv, 0);
-    int g_q0 = __shfl_sync(0xffffffffu, hv, 1), g_mt = __shfl_sync(0xffffffffu, hv, 2);
-    int g_n = __shfl_sync(0xffffffffu, hv, 3), g_row0 = __shfl_sync(0xffffffffu, hv, 4);
-    int g_c0 = __shfl_sync(0xffffffffu, hv, 5);
-    int64_t p_next = __shfl_sync(0xffffffffu, hv, 6);
-    const int r_first = __shfl_sync(0xffffffffu, hv, 7);
-    int ptok = __shfl_sync(0xffffffffu, hv, 8 + (lane & 7));  // lane j < 8: token j
+    // The range's first group comes from the head: the copies of its first chunks go out
+    // at once; the group list is read meanwhile.
+    int pg = hd.g;
+    int g_q0 = hd.q0, g_mt = hd.mt, g_n = hd.n, g_row0 = hd.row0, g_c0 = hd.c0;
+    int64_t p_next = hd.c1;
+    const int r_first = hd.row;
+    int ptok = pick8(hd.tok, lane & 7);  // lane j < 8: token j
     int early = int(p_next - cb);
     early = early < S ? early : S;
     early = early < nk ? early : nk;
@@ -213,7 +228,10 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
     for (; issued < nk; ++issued) {
       const int s = issued % S;
       int ok = 1;
-      if (lane == 0)
+      // The first S stages start free. They are not waited for: the consumers take the first
+      // group from the head and may already have released some of the early copies' stages,
+      // which would put empty[s] one phase past the one a first-round wait expects.
+      if (lane == 0 && issued >= S)
         ok = tc::mbar_wait_watch(&ms->empty[s], ((issued / S) & 1) ^ 1, abort_flag, a.st,
                                  0x40000)
                  ? 1
@@ -221,7 +239,7 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       const int64_t c = cb + issued;
       bool fresh = false;
-      while (p_next <= c) {
+      while (p_next <= c && pg < n_groups) {
         ++pg;
         if (pg + 1 - w0 > 31) {
           w0 = pg;
@@ -229,6 +247,10 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
         }
         take();
         fresh = true;
+      }
+      if (p_next <= c) {  // no group holds chunk c: an inconsistent plan (never expected)
+        if (lane == 0) atomicOr(&a.st->timeout, 0x1000000);
+        break;
       }
       // the stage's group description (the consumers read it once meta_full is armed)
       StageMeta* m = &ms->meta[s];
@@ -336,9 +358,10 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
   // and k+1): RS = 2 CH rows, row R of the step is row R % CH of chunk R / CH.
   // Xᵀ fragments of this warp's k-steps for the group of stage meta m, straight from x
   // (tokens past mt zero): b0 = x[token g8][16 s + 2 t4 .. +1], b1 = x[token g8][16 s + 8 + ..]
-  auto load_x = [&](const StageMeta* m, int m_mt) {
+  auto load_x = [&](int tok_g8, int m_mt) {  // tok_g8: batch index of the group's token g8
     const unsigned int* xrow = nullptr;
-    if (g8 < m_mt) xrow = reinterpret_cast<const unsigned int*>(Xg + int64_t(m->tok[g8]) * d);
+    if (g8 < m_mt && tok_g8 >= 0 && tok_g8 < a.T)
+      xrow = reinterpret_cast<const unsigned int*>(Xg + int64_t(tok_g8) * d);
 #pragma unroll
     for (int i = 0; i < KS; ++i) {
       const int s16 = warp + kWarps * i;
@@ -350,6 +373,24 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
     }
   };
   uint32_t u = 0;  // steps done: (m, l) of the current group live in m_run/l_run[u & 1]
+  {  // the range's first group, from the head (the consumers never wait for its metadata)
+    cg = hd.g;
+    q0 = hd.q0;
+    mt = hd.mt;
+    gn = hd.n;
+    gc0 = hd.c0;
+    c_next = hd.c1;
+    i0 = 2 * t4 < mt ? int64_t(pick8(hd.tok, 2 * t4)) : 0;
+    i1 = 2 * t4 + 1 < mt ? int64_t(pick8(hd.tok, 2 * t4 + 1)) : 0;
+    itid = tid < mt ? int64_t(pick8(hd.tok, tid & 7)) : 0;
+    load_x(pick8(hd.tok, g8), mt);
+#pragma unroll
+    for (int mi = 0; mi < MT; ++mi) acc[mi][0] = acc[mi][1] = acc[mi][2] = acc[mi][3] = 0.f;
+    if (tid < kMT) {
+      ms->m_run[0][tid] = -INFINITY;
+      ms->l_run[0][tid] = 0.f;
+    }
+  }
   for (int k = 0; k < nk;) {
     const int64_t c = cb + k;
     if (c >= c_next) {  // the chunk opens the next group
@@ -378,7 +419,7 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
       i0 = 2 * t4 < mt ? int64_t(m->tok[2 * t4]) : 0;
       i1 = 2 * t4 + 1 < mt ? int64_t(m->tok[2 * t4 + 1]) : 0;
       itid = tid < mt ? int64_t(m->tok[tid]) : 0;
-      load_x(m, mt);
+      load_x(m->tok[g8], mt);
 #pragma unroll
       for (int mi = 0; mi < MT; ++mi) acc[mi][0] = acc[mi][1] = acc[mi][2] = acc[mi][3] = 0.f;
       if (tid < kMT) {

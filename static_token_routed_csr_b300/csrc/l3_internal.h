@@ -53,6 +53,8 @@ struct alignas(16) CtaHead {
   int32_t c1;   // the group's end chunk (the next group's c0)
   int32_t row;  // table row of the range's first chunk
   int32_t tok[kPlanMT];
+  int32_t cb, ce;  // the CTA's chunk range [cb, ce) (cta_start[b], cta_start[b + 1])
+  int32_t pad[2];
 };
 // A group cut by the end of a split-row CTA's range that starts in that range: written by the
 // CTA (g < 0: none) for the combine kernel, which merges the group's partials.

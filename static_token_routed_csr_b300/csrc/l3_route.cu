@@ -127,6 +127,7 @@ __device__ int4 block_exclusive_scan4(int4 v, int4* warp_tot, int4* total) {
 // when there is no such group (gh >= NG: the range is empty).
 __device__ void write_head(const PlanOut& pl, int64_t b, int gh, int64_t c, int NG) {
   CtaHead h{};
+  h.cb = int32_t(c);  // ce is filled in once every range start is known
   if (gh >= NG) {
     pl.cta_head[b] = h;
     return;
@@ -275,6 +276,8 @@ __device__ void plan_pass(const uint64_t* keys, int64_t T, const int32_t* seg_st
       }
     }
   }
+  __syncthreads();
+  for (int64_t b = threadIdx.x; b < n; b += blockDim.x) pl.cta_head[b].ce = pl.cta_start[b + 1];
 }
 
 // Segment pass over sorted keys: perm, seg_start, seg_id, n_seg (and the attend plan).
