@@ -61,7 +61,6 @@ struct FwdWs {
   int32_t* cta_start;  // the plan's split of the chunk list over the split-row kernel's CTAs
   int32_t* cta_group;
   CtaHead* cta_head;
-  AttendCut* cuts;
   int n_cta;
   AttendItem* items;
   float* a_f32;
@@ -77,6 +76,10 @@ struct FwdWs {
   float* colsum;
   float* slab;  // split-K parts of the GEMMs (decode-sized batches)
   size_t slab_floats;
+  // small batches (T <= 64): warp-MMA GEMMs with their own statistics and halves
+  bool small;
+  uint32_t* sync;  // arrival counters, zeroed with the status words
+  float *q_stats, *q_slab;
   // tensor-core gather-attend of the long segments
   __nv_bfloat16* x_sorted;
   int tc_th;      // segments with at least this many tokens go to tensor cores (0: none)
@@ -87,6 +90,7 @@ FwdWs carve_fwd(Carve& c, const l3_layer* L, int64_t T) {
   FwdWs w{};
   const size_t t = size_t(T), d = size_t(L->d), dv = size_t(L->d_v);
   w.st = c.take<DevStatus>(1);
+  w.sync = c.take<uint32_t>(size_t(kSyncWords));  // zeroed with the status words
   w.route_scratch = c.raw(route_scratch_bytes(T));
   w.perm = c.take<int32_t>(t);
   w.seg_start = c.take<int32_t>(t + 1);
@@ -102,7 +106,6 @@ FwdWs carve_fwd(Carve& c, const l3_layer* L, int64_t T) {
   w.cta_start = c.take<int32_t>(size_t(kPlanMaxCtas) + 1);
   w.cta_group = c.take<int32_t>(size_t(kPlanMaxCtas));
   w.cta_head = c.take<CtaHead>(size_t(kPlanMaxCtas));
-  w.cuts = c.take<AttendCut>(size_t(kPlanMaxCtas));
   w.tc_th = attend_tc_threshold(T, int(d), int(dv), L->dtype);
   if (w.tc_th > 0) {
     w.max_items = int(T / w.tc_th + 1);
@@ -112,10 +115,17 @@ FwdWs carve_fwd(Carve& c, const l3_layer* L, int64_t T) {
   if (L->dtype == L3_BF16) {
     w.a_bf16 = c.take<__nv_bfloat16>(t * dv);
     w.U16 = c.take<__nv_bfloat16>(t * d);
-    w.stats = c.take<float>(size_t(tc_up_stat_tiles(int(d))) * t * 2);
-    w.colsum = c.take<float>(d);
-    w.slab_floats = tc_splitk_floats(T, int(d), int(dv));
-    if (w.slab_floats) w.slab = c.take<float>(w.slab_floats);
+    w.small = small_gemm_fits(T, int(d), int(dv));
+    if (w.small) {
+      w.q_stats = c.take<float>(d / 32 * 64 * 2);
+      w.q_slab = c.take<float>(d * 128);
+      w.colsum = c.take<float>(d);
+    } else {
+      w.stats = c.take<float>(size_t(tc_up_stat_tiles(int(d))) * t * 2);
+      w.colsum = c.take<float>(d);
+      w.slab_floats = tc_splitk_floats(T, int(d), int(dv));
+      if (w.slab_floats) w.slab = c.take<float>(w.slab_floats);
+    }
   } else {
     w.a_f32 = c.take<float>(t * dv);
     w.U = c.take<float>(t * d);
@@ -266,7 +276,11 @@ l3_status forward_impl(const l3_layer* L, const int32_t* ids, int64_t T, const v
   float* rstd = saved ? sv.rstd : w.rstd;
   const int d = int(L->d), dv = int(L->d_v);
 
-  L3_CUDA(cudaMemsetAsync(w.st, 0, sizeof(DevStatus), s));
+  // the status words and the arrival counters (one zeroing of the workspace's head)
+  L3_CUDA(cudaMemsetAsync(w.st, 0,
+                          size_t(reinterpret_cast<char*>(w.sync + kSyncWords) -
+                                 reinterpret_cast<char*>(w.st)),
+                          s));
   if (ev) L3_CUDA(record_stage(ev[L3_STAGE_ROUTE], s));
   const uint64_t* keys = nullptr;
   const int ch = attend_rows_per_chunk(d, dv, L->dtype);
@@ -302,7 +316,6 @@ l3_status forward_impl(const l3_layer* L, const int32_t* ids, int64_t T, const v
     aa.cta_start = w.cta_start;
     aa.cta_group = w.cta_group;
     aa.cta_head = w.cta_head;
-    aa.cuts = w.cuts;
     aa.n_cta = w.n_cta;
     aa.st = w.st;
     L3_CUDA(launch_attend_fwd(aa, s));
@@ -331,6 +344,33 @@ l3_status forward_impl(const l3_layer* L, const int32_t* ids, int64_t T, const v
   }
 
   if (ev) L3_CUDA(record_stage(ev[L3_STAGE_UP], s));
+  if (L->dtype == L3_BF16 && w.small) {
+    // small batch: weight-streaming warp-MMA GEMMs
+    SmallGemmArgs g{};
+    g.T = T;
+    g.d = d;
+    g.d_v = dv;
+    g.eps = L->ln_eps;
+    g.a = w.a_bf16;
+    g.W_up = static_cast<const __nv_bfloat16*>(L->W_up);
+    g.W_mix = static_cast<const __nv_bfloat16*>(L->W_mix);
+    g.x = static_cast<const __nv_bfloat16*>(x);
+    g.U = w.U16;
+    g.tile_stats = w.q_stats;
+    g.mu_out = saved ? sv.mu : nullptr;
+    g.rstd_out = saved ? sv.rstd : nullptr;
+    g.slab = w.q_slab;
+    g.colsum = w.colsum;
+    g.counters = w.sync;
+    g.Y = y;
+    g.y_dtype = y_dtype;
+    g.st = w.st;
+    L3_CUDA(launch_small_up(g, s));
+    if (ev) L3_CUDA(record_stage(ev[L3_STAGE_MIX], s));
+    L3_CUDA(launch_small_mix(g, s));
+    if (ev) L3_CUDA(record_stage(ev[L3_FWD_STAGES], s));
+    return L3_OK;
+  }
   if (L->dtype == L3_BF16) {
     // Tensor cores: U = bf16(A W_upᵀ) with partial LayerNorm statistics, then
     // y = rstd (U W1ᵀ - mu c) + x W2ᵀ with the statistics merged in the epilogue.

@@ -34,7 +34,8 @@
 //           (hi = bf16(e), lo = bf16(e - hi)), which keeps them to about 2^-17 relative
 //           error; the accumulator stays in registers for the whole group.
 // A group that ends inside the CTA's range is finished there; otherwise its partial
-// (m, l, acc) is merged by the CTA that completes the group (see l3_attend_split.cuh).
+// (m, l, acc) is merged by the CTA that completes the group's chunk count
+// (see l3_attend_split.cuh).
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -300,7 +301,6 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
   int64_t i0 = 0, i1 = 0, itid = 0;
   bool ok = true;
 
-  bool cut_set = false;  // (thread 0) this CTA left a group to the combine kernel
   auto finish = [&](int par) {
     const int64_t c0 = gc0, c1 = c_next;
     const bool whole = c0 >= cb && c1 <= ce;
@@ -347,11 +347,8 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
       pe[0] = ms->m_run[par][tid];
       pe[1] = ms->l_run[par][tid];
     }
-    // a group that starts here and runs past the range is merged by the combine kernel
-    if (tid == 0 && c0 >= cb && c1 > ce) {
-      a.cuts[b] = AttendCut{cg, q0, mt, second ? 1 : 0, c0, c1};
-      cut_set = true;
-    }
+    // the CTA that completes the group's chunk count merges the partials
+    arrive_and_merge(a, cg, c0, c1, cb, ce, q0, mt, &ms->merge, tid, kThreads, [] { cbar(); });
   };
 
   // A consumer step takes one chunk, or two consecutive chunks of the same group (stages k
@@ -584,48 +581,6 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
   }
 
   if (ok && cg >= 0) finish(u & 1);
-  if (tid == 0 && !cut_set) a.cuts[b] = AttendCut{-1, 0, 0, 0, 0, 0};
-}
-
-// Merges the partials of the groups the split-row kernel's CTAs cut: CTA b takes the group
-// that starts in split-row CTA b's range and runs past it, if there is one. Its holders are
-// b and the CTAs after it whose (non-empty) ranges start before the group's end; the
-// partials are merged in CTA order, as the in-kernel merge does, so results are identical.
-constexpr int kCombineThreads = 256;
-__global__ void __launch_bounds__(kCombineThreads) attend_combine_kernel(const AttendArgs a) {
-  __shared__ MergeSmem sm;
-  grid_dep_wait();  // the split-row kernel's partials are complete
-  grid_dep_release();
-  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
-  const int32_t* cs = a.cta_start;
-  if (cs[b] >= cs[b + 1]) return;
-  const AttendCut cut = a.cuts[b];
-  if (cut.g < 0) return;
-  if (tid < 32) {
-    int nh = 1;
-    for (int base = b + 1;; base += 32) {
-      const int bb = base + lane;
-      const bool inside = bb < a.n_cta;
-      const bool ne = inside && cs[bb] < cs[bb + 1];
-      const bool holds = ne && cs[bb] < cut.c1;
-      const unsigned m_hold = __ballot_sync(0xffffffffu, holds);
-      const unsigned m_stop = __ballot_sync(0xffffffffu, !inside || (ne && cs[bb] >= cut.c1));
-      // holders come before the first non-empty range past the group
-      const unsigned take = m_stop ? m_hold & ((1u << (__ffs(m_stop) - 1)) - 1u) : m_hold;
-      if ((take >> lane) & 1u) {
-        const int k = nh + __popc(take & ((1u << lane) - 1u));
-        if (k < kMergeCap) sm.hold[k] = bb;
-      }
-      nh += __popc(take);
-      if (m_stop) break;
-    }
-    if (lane == 0) {
-      sm.hold[0] = b;
-      sm.nh = nh < kMergeCap ? nh : kMergeCap;
-      sm.first_second = cut.second;
-    }
-  }
-  merge_held(a, cut.q0, cut.mt, &sm, tid, kCombineThreads, [] { __syncthreads(); });
 }
 
 template <int CH, int KSW, int MTW>
@@ -636,11 +591,8 @@ cudaError_t launch_ch(const AttendArgs& a, const MmaShape& sh, cudaStream_t stre
   const cudaError_t attr = ensure_smem_attr(attend_mma_kernel<CH, KSW, MTW>, kSmemLimit);
   if (attr != cudaSuccess) return attr;
   if (a.n_cta < 1 || a.n_cta > kMaxCtas) return cudaErrorInvalidValue;
-  cudaError_t e = launch_pdl(attend_mma_kernel<CH, KSW, MTW>, dim3(a.n_cta), dim3(kCtaThreads),
-                             size_t(sh.smem), stream, mk, mv, a, sh);
-  count_launch();
-  if (e != cudaSuccess) return e;
-  e = launch_pdl(attend_combine_kernel, dim3(a.n_cta), dim3(kCombineThreads), 0, stream, a);
+  const cudaError_t e = launch_pdl(attend_mma_kernel<CH, KSW, MTW>, dim3(a.n_cta),
+                                   dim3(kCtaThreads), size_t(sh.smem), stream, mk, mv, a, sh);
   count_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -662,15 +614,16 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// bf16 table [rows, cols] viewed as [cols / 64][rows][64]; box: all column blocks of
-// `box_rows` rows, 128-byte swizzle.
+// bf16 table [rows, cols] viewed as [cols / 64][rows][64]; box: `box_cblocks` column blocks
+// (all when 0) of `box_rows` rows, 128-byte swizzle.
 bool make_row_block_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols,
-                        int box_rows) {
+                        int box_rows, int box_cblocks) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {64, cuuint64_t(rows), cuuint64_t(cols / 64)};
   cuuint64_t strides[2] = {cuuint64_t(cols) * 2, 128};
-  cuuint32_t box[3] = {64, cuuint32_t(box_rows), cuuint32_t(cols / 64)};
+  cuuint32_t box[3] = {64, cuuint32_t(box_rows),
+                       cuuint32_t(box_cblocks > 0 ? box_cblocks : cols / 64)};
   cuuint32_t estr[3] = {1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

@@ -77,39 +77,62 @@ __device__ __noinline__ void arrive_and_merge(const AttendArgs& a, int g, int64_
   bar();
   if (!sm->last) return;
   __threadfence();
-  // Holders: the CTAs whose non-empty range meets [c0, c1), contiguous around this one.
-  // Warp 0 looks at the 32 CTAs on each side at once; a longer run is walked one by one.
+  // Holders: the CTAs whose non-empty range meets [c0, c1), in CTA order around this one
+  // (CTAs with empty ranges may sit between them). Warp 0 looks at the 32 CTAs on each side
+  // at once (one pair of range bounds per lane and side) and takes the holders from the
+  // two ballots; only when the holders found do not cover [c0, c1) (more lie outside the
+  // windows) is the run walked one CTA at a time.
   if (tid < 32) {
     const int b = int(blockIdx.x), n = a.n_cta;
-    auto holds = [&](int bb) {
-      return bb >= 0 && bb < n && cs[bb] < cs[bb + 1] && cs[bb] < c1 && cs[bb + 1] > c0;
+    auto holds = [&](int bb, int32_t& s0, int32_t& s1) {
+      const bool in = bb >= 0 && bb < n;
+      s0 = in ? cs[bb] : 0;
+      s1 = in ? cs[bb + 1] : 0;
+      return in && s0 < s1 && s0 < c1 && s1 > c0;
     };
-    const unsigned lo = __ballot_sync(0xffffffffu, holds(b - 32 + tid));  // b-32 .. b-1
-    const unsigned hi = __ballot_sync(0xffffffffu, holds(b + 1 + tid));   // b+1 .. b+32
+    int32_t s_lo = 0, e_lo = 0, s_hi = 0, e_hi = 0;
+    const bool h_lo = holds(b - 32 + tid, s_lo, e_lo);  // b-32 .. b-1
+    const bool h_hi = holds(b + 1 + tid, s_hi, e_hi);   // b+1 .. b+32
+    const unsigned lo = __ballot_sync(0xffffffffu, h_lo);
+    const unsigned hi = __ballot_sync(0xffffffffu, h_hi);
+    // holder CTAs in order: the set bits of lo, then b, then the set bits of hi
+    const int nlo = __popc(lo), nhi = __popc(hi);
+    if (h_lo) {
+      const int k = __popc(lo & ((1u << tid) - 1u));
+      if (k < kMergeCap) sm->hold[k] = b - 32 + tid;
+    }
+    if (h_hi) {
+      const int k = nlo + 1 + __popc(hi & ((1u << tid) - 1u));
+      if (k < kMergeCap) sm->hold[k] = b + 1 + tid;
+    }
+    // range start of the lowest holder and range end of the highest one, from the lanes
+    // that looked at them
+    const int low_lane = lo ? __ffs(lo) - 1 : 0;
+    const int high_lane = hi ? 31 - __clz(hi) : 0;
+    const int32_t s_low = __shfl_sync(0xffffffffu, s_lo, low_lane);
+    const int32_t e_high = __shfl_sync(0xffffffffu, e_hi, high_lane);
+    (void)s_hi;
+    (void)e_lo;
     if (tid == 0) {
-      int b0 = b, b1 = b;
-      // holders are contiguous among the non-empty ranges; empty ranges may sit between
-      if (c0 < cb) {
-        b0 = -1;
-        for (int k = 31; k >= 0; --k)
-          if (lo >> k & 1u) b0 = b - 32 + k;  // lowest holder in the window
-        // until the holder of chunk c0 is found, step down past the window
-        for (int bb = (b0 < 0 ? b - 33 : b0 - 1); bb >= 0 && (b0 < 0 || cs[b0] > c0); --bb)
+      sm->hold[nlo < kMergeCap ? nlo : kMergeCap - 1] = b;
+      int nh = nlo + 1 + nhi;
+      int64_t start0 = lo ? s_low : cb;  // range start of the first holder
+      const int64_t end1 = hi ? e_high : ce;  // range end of the last holder
+      if (start0 > c0 || end1 < c1) {
+        // holders outside the windows: list them again, walking from the first
+        int b0 = lo ? b - 32 + low_lane : b;
+        for (int bb = b0 - 1; bb >= 0 && cs[b0] > c0; --bb)
           if (cs[bb] < cs[bb + 1]) b0 = bb;
-      }
-      if (c1 > ce) {
-        b1 = -1;
-        for (int k = 0; k < 32; ++k)
-          if (hi >> k & 1u) b1 = b + 1 + k;  // highest holder in the window
-        // until the holder of chunk c1 - 1 is found, step up past the window
-        for (int bb = (b1 < 0 ? b + 33 : b1 + 1); bb < n && (b1 < 0 || cs[b1 + 1] < c1); ++bb)
+        int b1 = b;
+        for (int bb = b + 1; bb < n && cs[bb] < c1; ++bb)
           if (cs[bb] < cs[bb + 1]) b1 = bb;
+        nh = 0;
+        for (int bb = b0; bb <= b1; ++bb)
+          if (cs[bb] < cs[bb + 1] && nh < kMergeCap) sm->hold[nh++] = bb;
+        start0 = cs[b0];
       }
-      int nh = 0;
-      for (int bb = b0; bb <= b1; ++bb)
-        if (cs[bb] < cs[bb + 1] && nh < kMergeCap) sm->hold[nh++] = bb;
-      sm->nh = nh;
-      sm->first_second = c0 > cs[b0] ? 1 : 0;  // the group is CTA b0's second slot
+      sm->nh = nh < kMergeCap ? nh : kMergeCap;
+      sm->first_second = c0 > start0 ? 1 : 0;  // the group is the first holder's second slot
     }
   }
   merge_held(a, q0, mt, sm, tid, nthr, bar);
@@ -118,6 +141,10 @@ __device__ __noinline__ void arrive_and_merge(const AttendArgs& a, int g, int64_
 // Merge the partials of a group (tokens q0 .. q0 + mt - 1 in sorted order) held by the CTAs
 // sm->hold[0 .. sm->nh) in CTA order (holder 0 keeps it in its second slot if
 // sm->first_second), and write the group's outputs. Same caller rules as arrive_and_merge.
+// Thread tid takes the column pair cp = tid % half (half = d_v / 2) of the tokens tid / half,
+// + nthr / half, ... Every load that does not depend on another goes out in one phase: the
+// holders' (m, l), the tokens' batch indices and the thread's share of the first kMergeW
+// holders' partial sums for its first two tokens; the weights follow, then the sums.
 template <typename Bar>
 __device__ __noinline__ void merge_held(const AttendArgs& a, int q0, int mt, MergeSmem* sm,
                                         int tid, int nthr, Bar bar) {
@@ -125,14 +152,31 @@ __device__ __noinline__ void merge_held(const AttendArgs& a, int q0, int mt, Mer
   const int nh = sm->nh;
   const bool fs = sm->first_second != 0;
   auto entry = [&](int h, int j) { return part_entry(a, sm->hold[h], h == 0 && fs, j); };
-  // every holder's (m, l) for every token, loaded at once (the first kMergeW holders)
   const int nw = nh < kMergeW ? nh : kMergeW;
+  const int half = a.d_v / 2;
+  const int jstep = nthr / half;
+  const int cp = tid % half, j0 = tid / half;
   for (int e = tid; e < mt * nw; e += nthr) {
     const int j = e / nw, h = e - j * nw;
     const float* pp = entry(h, j);
     sm->w[j][h] = __ldcg(pp);
     sm->l[j][h] = __ldcg(pp + 1);
   }
+  if (tid < mt) sm->tok[tid] = int64_t(uint32_t(a.sorted_keys[q0 + tid]));
+  // this thread's share of the first two of its tokens' holder sums (j0, j0 + jstep)
+  float2 pre[2][kMergeW];
+  auto load2 = [&](int ja) {
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int j = ja + u * jstep;
+#pragma unroll
+      for (int h = 0; h < kMergeW; ++h)
+        pre[u][h] = j < mt && h < nw
+                        ? __ldcg(reinterpret_cast<const float2*>(entry(h, j) + 2 + 2 * cp))
+                        : make_float2(0.f, 0.f);
+    }
+  };
+  load2(j0);
   bar();
   // token j: max and denominator over the holders, then the holders' weights
   if (tid < mt) {
@@ -149,48 +193,40 @@ __device__ __noinline__ void merge_held(const AttendArgs& a, int q0, int mt, Mer
     for (int h = 0; h < nw; ++h) sm->w[j][h] = expf(sm->w[j][h] - M) * inv;
     sm->M[j] = M;
     sm->inv_l[j] = inv;
-    const int64_t i = int64_t(uint32_t(a.sorted_keys[q0 + j]));
-    sm->tok[j] = i;
     if (a.ml) {
+      const int64_t i = sm->tok[j];
       a.ml[2 * i] = M;
       a.ml[2 * i + 1] = L;
     }
   }
   bar();
-  // a = sum_h w_h acc_h. Thread tid takes the column pair cp = tid % half of the tokens
-  // tid / half, + nthr / half, ... (d_v <= 512, so half <= nthr). The code is kept compact:
-  // a merge runs at most once per group, often with the instruction cache cold, and four
-  // holders' loads are in flight per step.
-  const int half = a.d_v / 2;
-  const int jstep = nthr / half;
-  const int cp = tid % half;
+  // a = sum_h w_h acc_h, two tokens at a time: the first two from the registers loaded
+  // above, each further pair with one batch of loads; holders past kMergeW one by one
 #pragma unroll 1
-  for (int j = tid / half; j < mt; j += jstep) {
-    float s0 = 0.f, s1 = 0.f;
-    int h = 0;
-#pragma unroll 1
-    for (; h + 4 <= nw; h += 4) {
-      float2 v[4];
+  for (int ja = j0; ja < mt; ja += 2 * jstep) {
+    if (ja != j0) load2(ja);  // two tokens' shares of every holder's sums, all loads at once
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        v[e] = __ldcg(reinterpret_cast<const float2*>(entry(h + e, j) + 2 + 2 * cp));
+    for (int u = 0; u < 2; ++u) {
+      const int j = ja + u * jstep;
+      if (j >= mt) break;
+      float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float wt = sm->w[j][h + e];
-        s0 = fmaf(v[e].x, wt, s0);
-        s1 = fmaf(v[e].y, wt, s1);
+      for (int h = 0; h < kMergeW; ++h) {
+        const float wt = h < nw ? sm->w[j][h] : 0.f;
+        s0 = fmaf(pre[u][h].x, wt, s0);
+        s1 = fmaf(pre[u][h].y, wt, s1);
       }
-    }
 #pragma unroll 1
-    for (; h < nh; ++h) {
-      const float* pp = entry(h, j);
-      const float wt = h < kMergeW ? sm->w[j][h] : expf(__ldcg(pp) - sm->M[j]) * sm->inv_l[j];
-      const float2 v = __ldcg(reinterpret_cast<const float2*>(pp + 2 + 2 * cp));
-      s0 = fmaf(v.x, wt, s0);
-      s1 = fmaf(v.y, wt, s1);
+      for (int h = kMergeW; h < nh; ++h) {
+        const float* pp = entry(h, j);
+        const float wt = expf(__ldcg(pp) - sm->M[j]) * sm->inv_l[j];
+        const float2 v = __ldcg(reinterpret_cast<const float2*>(pp + 2 + 2 * cp));
+        s0 = fmaf(v.x, wt, s0);
+        s1 = fmaf(v.y, wt, s1);
+      }
+      write_a(a, sm->tok[j], 2 * cp, s0);
+      write_a(a, sm->tok[j], 2 * cp + 1, s1);
     }
-    write_a(a, sm->tok[j], 2 * cp, s0);
-    write_a(a, sm->tok[j], 2 * cp + 1, s1);
   }
 }
 

@@ -56,12 +56,6 @@ struct alignas(16) CtaHead {
   int32_t cb, ce;  // the CTA's chunk range [cb, ce) (cta_start[b], cta_start[b + 1])
   int32_t pad[2];
 };
-// A group cut by the end of a split-row CTA's range that starts in that range: written by the
-// CTA (g < 0: none) for the combine kernel, which merges the group's partials.
-struct alignas(16) AttendCut {
-  int32_t g, q0, mt, second;  // second: the group is the CTA's second partial slot
-  int64_t c0, c1;             // the group's chunks
-};
 struct AttendItem {
   int32_t q0;  // first sorted position
   int32_t nt;  // tokens (1..kTcNT)
@@ -116,7 +110,6 @@ struct AttendArgs {
   const int32_t* cta_start;  // the plan's split of the chunk list (PlanOut)
   const int32_t* cta_group;
   const CtaHead* cta_head;
-  AttendCut* cuts;           // [n_cta] (bf16 kernel): groups left to the combine kernel
   int n_cta;                 // grid of the split-row kernel
   DevStatus* st;
 };
@@ -344,6 +337,35 @@ struct BwdSmallArgs {
   __nv_bfloat16* a_lo;
 };
 cudaError_t launch_bwd_small(const BwdSmallArgs& a, cudaStream_t stream);
+
+// ---- small-batch GEMMs (l3_gemm_small.cu) --------------------------------------------------
+// Batches of at most 64 tokens: u = W_up a with the LayerNorm statistics (GEMM-up), then
+// y = W_mix [LayerNorm(u); x] (GEMM-mix), weight rows streamed by 32-feature CTAs.
+constexpr int kSmallMaxTiles = 128;                 // d / 32 <= 128 (d <= 4096)
+constexpr int kSyncWords = kSmallMaxTiles;          // arrival counters (zeroed per forward)
+struct SmallGemmArgs {
+  int64_t T;
+  int d, d_v;
+  float eps;
+  const __nv_bfloat16* a;      // [T, d_v]
+  const __nv_bfloat16* W_up;   // [d, d_v]
+  const __nv_bfloat16* W_mix;  // [d, 2d]
+  const __nv_bfloat16* x;      // [T, d]
+  __nv_bfloat16* U;            // [T, d] bf16(u)
+  float* tile_stats;           // [d / 32][64][2] (sum, M2) per 32-feature tile and token
+  float* mu_out;               // optional (saved state)
+  float* rstd_out;
+  float* slab;                 // [d / 32][2][32][64] the mix halves' accumulators
+  float* colsum;               // [d] row sums of W_mix[:, :d]
+  uint32_t* counters;          // [d / 32], zero on entry; left at zero
+  void* Y;                     // [T, d] y_dtype
+  int y_dtype;
+  DevStatus* st;
+};
+bool small_gemm_fits(int64_t T, int d, int d_v);
+size_t small_gemm_floats(int d);
+cudaError_t launch_small_up(const SmallGemmArgs& g, cudaStream_t stream);
+cudaError_t launch_small_mix(const SmallGemmArgs& g, cudaStream_t stream);
 
 // ---- staging of a batch's rows from host-resident tables (l3_stage.cu) ---------------------
 struct StageArgs {

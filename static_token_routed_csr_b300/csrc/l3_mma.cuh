@@ -81,10 +81,10 @@ __device__ __forceinline__ void tma_load_3d(const CUtensorMap* map, uint64_t* ba
 }
 
 
-// bf16 table [rows, cols] viewed as [cols / 64][rows][64]; box: all column blocks of
-// `box_rows` rows, 128-byte swizzle (defined in l3_attend_mma.cu).
+// bf16 table [rows, cols] viewed as [cols / 64][rows][64]; box: `box_cblocks` column blocks
+// (all of them when 0) of `box_rows` rows, 128-byte swizzle (defined in l3_attend_mma.cu).
 bool make_row_block_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols,
-                        int box_rows);
+                        int box_rows, int box_cblocks = 0);
 
 }  // namespace wmma
 }  // namespace l3
