@@ -144,7 +144,7 @@ __device__ __noinline__ void arrive_and_merge(const AttendArgs& a, int g, int64_
 // Thread tid takes the column pair cp = tid % half (half = d_v / 2) of the tokens tid / half,
 // + nthr / half, ... Every load that does not depend on another goes out in one phase: the
 // holders' (m, l), the tokens' batch indices and the thread's share of the first kMergeW
-// holders' partial sums for its first two tokens; the weights follow, then the sums.
+// holders' partial sums for its first token; the weights follow, then the sums.
 template <typename Bar>
 __device__ __noinline__ void merge_held(const AttendArgs& a, int q0, int mt, MergeSmem* sm,
                                         int tid, int nthr, Bar bar) {
@@ -163,20 +163,11 @@ __device__ __noinline__ void merge_held(const AttendArgs& a, int q0, int mt, Mer
     sm->l[j][h] = __ldcg(pp + 1);
   }
   if (tid < mt) sm->tok[tid] = int64_t(uint32_t(a.sorted_keys[q0 + tid]));
-  // this thread's share of the first two of its tokens' holder sums (j0, j0 + jstep)
-  float2 pre[2][kMergeW];
-  auto load2 = [&](int ja) {
+  float2 pre[kMergeW];
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int j = ja + u * jstep;
-#pragma unroll
-      for (int h = 0; h < kMergeW; ++h)
-        pre[u][h] = j < mt && h < nw
-                        ? __ldcg(reinterpret_cast<const float2*>(entry(h, j) + 2 + 2 * cp))
-                        : make_float2(0.f, 0.f);
-    }
-  };
-  load2(j0);
+  for (int h = 0; h < kMergeW; ++h)
+    pre[h] = j0 < mt && h < nw ? __ldcg(reinterpret_cast<const float2*>(entry(h, j0) + 2 + 2 * cp))
+                               : make_float2(0.f, 0.f);
   bar();
   // token j: max and denominator over the holders, then the holders' weights
   if (tid < mt) {
@@ -200,33 +191,33 @@ __device__ __noinline__ void merge_held(const AttendArgs& a, int q0, int mt, Mer
     }
   }
   bar();
-  // a = sum_h w_h acc_h, two tokens at a time: the first two from the registers loaded
-  // above, each further pair with one batch of loads; holders past kMergeW one by one
+  // a = sum_h w_h acc_h: the first token from the registers loaded above, each further token
+  // with one batch of loads; holders past kMergeW one by one
 #pragma unroll 1
-  for (int ja = j0; ja < mt; ja += 2 * jstep) {
-    if (ja != j0) load2(ja);  // two tokens' shares of every holder's sums, all loads at once
+  for (int j = j0; j < mt; j += jstep) {
+    if (j != j0) {
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int j = ja + u * jstep;
-      if (j >= mt) break;
-      float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-      for (int h = 0; h < kMergeW; ++h) {
-        const float wt = h < nw ? sm->w[j][h] : 0.f;
-        s0 = fmaf(pre[u][h].x, wt, s0);
-        s1 = fmaf(pre[u][h].y, wt, s1);
-      }
-#pragma unroll 1
-      for (int h = kMergeW; h < nh; ++h) {
-        const float* pp = entry(h, j);
-        const float wt = expf(__ldcg(pp) - sm->M[j]) * sm->inv_l[j];
-        const float2 v = __ldcg(reinterpret_cast<const float2*>(pp + 2 + 2 * cp));
-        s0 = fmaf(v.x, wt, s0);
-        s1 = fmaf(v.y, wt, s1);
-      }
-      write_a(a, sm->tok[j], 2 * cp, s0);
-      write_a(a, sm->tok[j], 2 * cp + 1, s1);
+      for (int h = 0; h < kMergeW; ++h)
+        pre[h] = h < nw ? __ldcg(reinterpret_cast<const float2*>(entry(h, j) + 2 + 2 * cp))
+                        : make_float2(0.f, 0.f);
     }
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+    for (int h = 0; h < kMergeW; ++h) {
+      const float wt = h < nw ? sm->w[j][h] : 0.f;
+      s0 = fmaf(pre[h].x, wt, s0);
+      s1 = fmaf(pre[h].y, wt, s1);
+    }
+#pragma unroll 1
+    for (int h = kMergeW; h < nh; ++h) {
+      const float* pp = entry(h, j);
+      const float wt = expf(__ldcg(pp) - sm->M[j]) * sm->inv_l[j];
+      const float2 v = __ldcg(reinterpret_cast<const float2*>(pp + 2 + 2 * cp));
+      s0 = fmaf(v.x, wt, s0);
+      s1 = fmaf(v.y, wt, s1);
+    }
+    write_a(a, sm->tok[j], 2 * cp, s0);
+    write_a(a, sm->tok[j], 2 * cp + 1, s1);
   }
 }
 

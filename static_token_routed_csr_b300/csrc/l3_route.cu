@@ -11,6 +11,7 @@
 // A last pass marks segment starts and numbers the segments, and (for the forward) lays out
 // the work plan of the split-row gather-attend.
 #include "l3_internal.h"
+#include "l3_tc.cuh"
 
 namespace l3 {
 
@@ -288,6 +289,7 @@ constexpr int kItems = 4;
 __device__ void segment_pass(const uint64_t* keys, int64_t T, int32_t* perm,
                              int32_t* seg_start, int32_t* seg_id, int32_t* n_seg,
                              const PlanOut* plan, DevStatus* st, int* warp_tot, int* total) {
+  if (!perm && !seg_start && !seg_id && !n_seg) return;  // (the many-CTA pass follows)
   int carry = 0;
   const int64_t tile = int64_t(blockDim.x) * kItems;
   for (int64_t base = 0; base < T; base += tile) {
@@ -579,28 +581,404 @@ __global__ void __launch_bounds__(1024) route_segment_kernel(const uint64_t* __r
                warp_tot, &total);
 }
 
+// ---- many-CTA segment and plan pass (batches above kRankN tokens with a work plan) ---------
+//
+// One cooperative launch of G CTAs (all co-resident) does what segment_pass and plan_pass
+// do in one CTA, each step split over the CTAs and separated by grid barriers:
+//   1. CTA b counts the segment starts in its contiguous share of the sorted keys;
+//   2. it scans the CTAs' counts (each CTA itself), numbers its segments and writes
+//      perm, seg_start, seg_id (CTA G-1 also seg_start[S] and n_seg);
+//   3. it counts (groups, chunks, items, groups with chunks) of its share of the segments;
+//   4. it scans those per CTA and writes its segments' groups and items, the whole CTA
+//      sharing out each tile's groups (a segment of m tokens has m / 8 of them);
+//   5. the cost-balanced split of the chunk list over the attend CTAs and their heads,
+//      groups shared out over the CTAs as in the one-CTA pass;
+//   6. the heads' range ends.
+// The barriers are bounded: a CTA that waits too long records it (status word code
+// 0x2000000) and stops.
+constexpr int kCoopThreads = 1024;
+constexpr int kCoopMaxCtas = 256;
+
+struct CoopScratch {
+  int32_t cnt[kCoopMaxCtas];
+  int4 tot4[kCoopMaxCtas];
+  unsigned bar;  // arrivals: zeroed before the launch, k G after the k-th barrier
+};
+
+size_t coop_scratch_bytes() { return align_up(sizeof(CoopScratch), kAlign); }
+
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ bool coop_barrier(CoopScratch* cs, unsigned target, DevStatus* st, int* s_ok) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(&cs->bar, 1u);
+    const uint64_t t0 = tc::global_ns();
+    int ok = 1;
+    for (uint32_t i = 0;; ++i) {
+      if (ld_acquire(&cs->bar) >= target) break;
+      if ((i & 255) == 255 && tc::global_ns() - t0 > 1000000000ull) {
+        atomicOr(&st->timeout, 0x2000000);
+        ok = 0;
+        break;
+      }
+    }
+    __threadfence();
+    *s_ok = ok;
+  }
+  __syncthreads();
+  return *s_ok != 0;
+}
+
+// Sum of v[0 .. n) (n <= kCoopMaxCtas) below index `below`, and the total, by warp 0;
+// returned to every thread through shared memory.
+__device__ int2 coop_prefix(const int32_t* v, int n, int below, int2* sh) {
+  if (threadIdx.x < 32) {
+    int a = 0, t = 0;
+    for (int i = threadIdx.x; i < n; i += 32) {
+      const int x = __ldcg(v + i);
+      t += x;
+      if (i < below) a += x;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      a += __shfl_xor_sync(0xffffffffu, a, o);
+      t += __shfl_xor_sync(0xffffffffu, t, o);
+    }
+    if (threadIdx.x == 0) *sh = make_int2(a, t);
+  }
+  __syncthreads();
+  const int2 r = *sh;
+  __syncthreads();
+  return r;
+}
+
+__device__ void coop_prefix4(const int4* v, int n, int below, int4* sh_before, int4* sh_total) {
+  if (threadIdx.x < 32) {
+    int4 a = make_int4(0, 0, 0, 0), t = make_int4(0, 0, 0, 0);
+    for (int i = threadIdx.x; i < n; i += 32) {
+      const int4 x = __ldcg(v + i);
+      t.x += x.x, t.y += x.y, t.z += x.z, t.w += x.w;
+      if (i < below) a.x += x.x, a.y += x.y, a.z += x.z, a.w += x.w;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      a.x += __shfl_xor_sync(0xffffffffu, a.x, o);
+      a.y += __shfl_xor_sync(0xffffffffu, a.y, o);
+      a.z += __shfl_xor_sync(0xffffffffu, a.z, o);
+      a.w += __shfl_xor_sync(0xffffffffu, a.w, o);
+      t.x += __shfl_xor_sync(0xffffffffu, t.x, o);
+      t.y += __shfl_xor_sync(0xffffffffu, t.y, o);
+      t.z += __shfl_xor_sync(0xffffffffu, t.z, o);
+      t.w += __shfl_xor_sync(0xffffffffu, t.w, o);
+    }
+    if (threadIdx.x == 0) {
+      *sh_before = a;
+      *sh_total = t;
+    }
+  }
+  __syncthreads();
+}
+
+// A segment's share of the plan (as in plan_pass).
+struct SegPlan {
+  int q0, m, t, row0, n, per, ng, nc, ni, nw;
+};
+__device__ SegPlan seg_plan(const uint64_t* keys, const int32_t* seg_start, int s,
+                            const PlanOut& pl, DevStatus* st) {
+  SegPlan r{};
+  r.q0 = seg_start[s];
+  r.m = seg_start[s + 1] - r.q0;
+  r.t = int(keys[r.q0] >> 32);
+  r.row0 = pl.offs[r.t];
+  r.n = pl.offs[r.t + 1] - r.row0;
+  if (r.n < 1 || r.n > pl.k_max || r.row0 < 0 || int64_t(r.row0) + r.n > pl.v) {
+    atomicOr(&st->layer_bad, 1);
+    r.n = 0;
+  }
+  if (r.m >= pl.th) {
+    r.ni = r.n > 0 ? (r.m + kTcNT - 1) / kTcNT : 0;
+  } else {
+    r.ng = (r.m + pl.mt_max - 1) / pl.mt_max;
+    r.per = r.n > 0 ? (r.n + pl.ch - 1) / pl.ch : 0;
+    r.nc = r.ng * r.per;
+    r.nw = r.per > 0 ? r.ng : 0;
+  }
+  return r;
+}
+
+// Index i with off[i] <= x < off[i + 1] in the ascending off[0 .. n] (shared memory).
+__device__ __forceinline__ int find_seg(const int* off, int n, int x) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (off[mid] <= x)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo;
+}
+
+struct CoopSmem {
+  int warp_tot[32];
+  int total;
+  int4 wt4[32];
+  int4 tot4;
+  int4 before4, all4;
+  int2 pre;
+  int ok;
+  // one tile of segments: exclusive offsets of its groups and items, and their fields
+  int goff[kCoopThreads + 1], ioff[kCoopThreads + 1];
+  int q0[kCoopThreads], m[kCoopThreads], t[kCoopThreads], row0[kCoopThreads], n[kCoopThreads];
+  int per[kCoopThreads], cex[kCoopThreads], wex[kCoopThreads];
+};
+
+__global__ void __launch_bounds__(kCoopThreads, 1)
+    route_plan_coop_kernel(const uint64_t* __restrict__ keys, int64_t T, int32_t* perm,
+                           int32_t* seg_start, int32_t* seg_id, int32_t* n_seg, DevStatus* st,
+                           const PlanOut pl, CoopScratch* cs) {
+  grid_dep_release();
+  __shared__ CoopSmem sm;
+  const int G = gridDim.x, b = blockIdx.x, tid = threadIdx.x;
+  // 1. segment starts in keys [k0, k1)
+  const int64_t k0 = T * b / G, k1 = T * (b + 1) / G;
+  constexpr int kPer = 4;
+  int cnt = 0;
+  for (int64_t q = k0 + tid; q < k1; q += kCoopThreads)
+    cnt += (q == 0 || (keys[q - 1] >> 32) != (keys[q] >> 32)) ? 1 : 0;
+  {
+    const int ex = block_exclusive_scan(cnt, sm.warp_tot, &sm.total);
+    (void)ex;
+    if (tid == 0) cs->cnt[b] = sm.total;
+  }
+  if (!coop_barrier(cs, 1u * G, st, &sm.ok)) return;
+  // 2. numbering: this CTA's first segment is the number of starts before k0
+  const int2 pre = coop_prefix(cs->cnt, G, b, &sm.pre);
+  const int S = pre.y;
+  int carry = pre.x;
+  for (int64_t base = k0; base < k1; base += int64_t(kCoopThreads) * kPer) {
+    int flags[kPer], c = 0;
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int64_t q = base + int64_t(tid) * kPer + u;
+      flags[u] = 0;
+      if (q < k1) {
+        const uint64_t k = keys[q];
+        flags[u] = (q == 0 || (keys[q - 1] >> 32) != (k >> 32)) ? 1 : 0;
+        if (perm) perm[q] = int32_t(uint32_t(k));
+      }
+      c += flags[u];
+    }
+    int s = carry + block_exclusive_scan(c, sm.warp_tot, &sm.total);
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int64_t q = base + int64_t(tid) * kPer + u;
+      if (flags[u]) {
+        seg_start[s] = int32_t(q);
+        if (seg_id) seg_id[s] = int32_t(keys[q] >> 32);
+        ++s;
+      }
+    }
+    carry += sm.total;
+    __syncthreads();
+  }
+  if (b == G - 1 && tid == 0) {
+    seg_start[S] = int32_t(T);
+    if (n_seg) *n_seg = S;
+  }
+  if (!coop_barrier(cs, 2u * G, st, &sm.ok)) return;
+  // 3. plan counts of segments [s0, s1); when the CTA has at most kCoopThreads of them,
+  // thread tid keeps its segment's plan for step 4
+  const int s0 = int(int64_t(S) * b / G), s1 = int(int64_t(S) * (b + 1) / G);
+  const bool one_tile = s1 - s0 <= kCoopThreads;
+  SegPlan kept{};
+  int4 mine = make_int4(0, 0, 0, 0);
+  for (int s = s0 + tid; s < s1; s += kCoopThreads) {
+    const SegPlan r = seg_plan(keys, seg_start, s, pl, st);
+    mine.x += r.ng, mine.y += r.nc, mine.z += r.ni, mine.w += r.nw;
+    kept = r;
+  }
+  {
+    const int4 ex = block_exclusive_scan4(mine, sm.wt4, &sm.tot4);
+    (void)ex;
+    if (tid == 0) cs->tot4[b] = sm.tot4;
+  }
+  if (!coop_barrier(cs, 3u * G, st, &sm.ok)) return;
+  // 4. groups and items of segments [s0, s1), one tile of kCoopThreads segments at a time
+  coop_prefix4(cs->tot4, G, b, &sm.before4, &sm.all4);
+  const int4 all = sm.all4;
+  int4 run = sm.before4;  // (groups, chunks, items, groups with chunks) before the tile
+  for (int base = s0; base < s1; base += kCoopThreads) {
+    const int s = base + tid;
+    SegPlan r{};
+    if (s < s1) r = one_tile ? kept : seg_plan(keys, seg_start, s, pl, st);
+    const int4 ex = block_exclusive_scan4(make_int4(r.ng, r.nc, r.ni, r.nw), sm.wt4, &sm.tot4);
+    const int4 tt = sm.tot4;
+    sm.goff[tid] = ex.x;
+    sm.ioff[tid] = ex.z;
+    sm.q0[tid] = r.q0;
+    sm.m[tid] = r.m;
+    sm.t[tid] = r.t;
+    sm.row0[tid] = r.row0;
+    sm.n[tid] = r.n;
+    sm.per[tid] = r.per;
+    sm.cex[tid] = ex.y;
+    sm.wex[tid] = ex.w;
+    if (tid == 0) {
+      sm.goff[kCoopThreads] = tt.x;
+      sm.ioff[kCoopThreads] = tt.z;
+    }
+    __syncthreads();
+    const int nseg = s1 - base < kCoopThreads ? s1 - base : kCoopThreads;
+    for (int gi = tid; gi < tt.x; gi += kCoopThreads) {
+      const int i = find_seg(sm.goff, nseg, gi);
+      const int k = gi - sm.goff[i];
+      AttendGroup g;
+      g.q0 = sm.q0[i] + k * pl.mt_max;
+      g.mt = sm.m[i] - k * pl.mt_max < pl.mt_max ? sm.m[i] - k * pl.mt_max : pl.mt_max;
+      g.t = sm.t[i];
+      g.row0 = sm.row0[i];
+      g.n = sm.n[i];
+      g.c0 = run.y + sm.cex[i] + k * sm.per[i];
+      g.w0 = g.c0 * pl.w_chunk + (run.w + sm.wex[i] + (sm.per[i] > 0 ? k : 0)) * pl.w_group;
+      g.pad = 0;
+#pragma unroll
+      for (int j = 0; j < kPlanMT; ++j)
+        g.tok[j] = j < g.mt ? int32_t(uint32_t(keys[g.q0 + j])) : 0;
+      pl.groups[run.x + gi] = g;
+      pl.counters[run.x + gi] = 0;
+    }
+    for (int ii = tid; ii < tt.z; ii += kCoopThreads) {
+      int i = 0;
+      {  // the segment of item ii
+        int lo = 0, hi = nseg - 1;
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (sm.ioff[mid] <= ii)
+            lo = mid;
+          else
+            hi = mid - 1;
+        }
+        i = lo;
+      }
+      const int k = ii - sm.ioff[i];
+      AttendItem it;
+      it.q0 = sm.q0[i] + k * kTcNT;
+      it.nt = sm.m[i] - k * kTcNT < kTcNT ? sm.m[i] - k * kTcNT : kTcNT;
+      it.t = sm.t[i];
+      it.pad = 0;
+      pl.items[run.z + ii] = it;
+    }
+    run.x += tt.x, run.y += tt.y, run.z += tt.z, run.w += tt.w;
+    __syncthreads();
+  }
+  if (b == G - 1 && tid == 0) {
+    AttendGroup end{};
+    end.q0 = int32_t(T);
+    end.c0 = all.y;
+    end.w0 = all.y * pl.w_chunk + all.w * pl.w_group;
+    pl.groups[all.x] = end;
+    pl.hdr[kPlanGroups] = all.x;
+    pl.hdr[kPlanChunks] = all.y;
+    pl.hdr[kPlanItems] = all.z;
+    pl.hdr[3] = 0;
+  }
+  if (!pl.cta_start) return;
+  if (!coop_barrier(cs, 4u * G, st, &sm.ok)) return;
+  // 5. the split (as in plan_pass), groups [NG b / G, NG (b + 1) / G) here
+  const int NG = all.x;
+  const int64_t C = all.y;
+  const int64_t n = pl.n_cta;
+  const int64_t U = C * pl.w_chunk + int64_t(all.w) * pl.w_group;
+  if (U == 0) {
+    for (int64_t bb = int64_t(b) * kCoopThreads + tid; bb <= n; bb += int64_t(G) * kCoopThreads) {
+      pl.cta_start[bb] = 0;
+      if (bb < n) {
+        pl.cta_group[bb] = 0;
+        pl.cta_head[bb] = CtaHead{};
+      }
+    }
+    return;
+  }
+  if (b == 0) {
+    const int64_t b_zero = (n + U - 1) / U;
+    int g_first = 0;
+    while (g_first < NG && pl.groups[g_first + 1].c0 == pl.groups[g_first].c0) ++g_first;
+    for (int64_t bb = tid; bb < b_zero && bb <= n; bb += kCoopThreads) {
+      pl.cta_start[bb] = 0;
+      if (bb < n) {
+        pl.cta_group[bb] = 0;
+        write_head(pl, bb, g_first, 0, NG);
+      }
+    }
+  }
+  const int g0 = int(int64_t(NG) * b / G), g1 = int(int64_t(NG) * (b + 1) / G);
+  for (int g = g0 + tid; g < g1; g += kCoopThreads) {
+    const int64_t c0 = pl.groups[g].c0, c1 = pl.groups[g + 1].c0;
+    if (c1 <= c0) continue;
+    const int64_t W0 = pl.groups[g].w0;
+    const int64_t W1 = W0 + pl.w_group + (c1 - c0) * pl.w_chunk;
+    const int64_t b_lo = ((W0 + 1) * n + U - 1) / U;
+    const int64_t b_hi = ((W1 + 1) * n + U - 1) / U - 1;
+    for (int64_t bb = b_lo; bb <= b_hi && bb <= n; ++bb) {
+      const int64_t u1 = bb * U / n - 1;
+      const int64_t r = u1 - W0 - pl.w_group;
+      const int64_t cs0 = r < 0 ? c0 : c0 + r / pl.w_chunk;
+      pl.cta_start[bb] = int32_t(cs0 + 1);
+      if (bb < n) {
+        pl.cta_group[bb] = cs0 + 1 < c1 ? g : g + 1;
+        int gh = g;
+        if (cs0 + 1 >= c1) {
+          gh = g + 1;
+          while (gh < NG && pl.groups[gh + 1].c0 == pl.groups[gh].c0) ++gh;
+        }
+        write_head(pl, bb, gh, cs0 + 1, NG);
+      }
+    }
+  }
+  if (!coop_barrier(cs, 5u * G, st, &sm.ok)) return;
+  // 6. the heads' range ends
+  for (int64_t bb = int64_t(b) * kCoopThreads + tid; bb < n; bb += int64_t(G) * kCoopThreads)
+    pl.cta_head[bb].ce = pl.cta_start[bb + 1];
+}
+
 }  // namespace
 
 size_t route_scratch_bytes(int64_t T) {
-  return 2 * align_up(size_t(T) * sizeof(uint64_t), kAlign);
+  return 2 * align_up(size_t(T) * sizeof(uint64_t), kAlign) + coop_scratch_bytes();
 }
 
-// Sorted keys end up in the returned buffer (one of the two scratch halves).
+// Sorted keys end up in the returned buffer (one of the two scratch halves). With a work plan
+// and more than kRadixN tokens, the sort kernels only sort and the many-CTA pass
+// (route_plan_coop_kernel) finds the segments and lays out the plan; smaller batches keep
+// the sort, the segments and the plan in one CTA (a dependent global round trip costs a
+// microsecond or two, which is about what a step of the one-CTA pass costs at that size).
 cudaError_t launch_route(const int32_t* ids, int64_t T, int64_t vocab, void* scratch,
                          RouteOut out, DevStatus* st, cudaStream_t stream,
                          const uint64_t** sorted_keys, const PlanOut* plan) {
   const PlanOut pl = plan ? *plan : PlanOut{};
-  const int with_plan = plan && out.seg_start ? 1 : 0;
+  const bool with_plan = plan && out.seg_start;
+  const bool coop = with_plan && T > kRadixN;
   uint64_t* k0 = static_cast<uint64_t*>(scratch);
   uint64_t* k1 = reinterpret_cast<uint64_t*>(static_cast<char*>(scratch) +
                                              align_up(size_t(T) * sizeof(uint64_t), kAlign));
   if (T <= kRankN) {
     route_rank_kernel<<<1, kRankN, 0, stream>>>(ids, T, vocab, k0, out.perm, out.seg_start,
-                                                out.seg_id, out.n_seg, st, pl, with_plan);
+                                                out.seg_id, out.n_seg, st, pl, with_plan ? 1 : 0);
     count_launch();
     *sorted_keys = k0;
     return cudaGetLastError();
   }
+  // the sort; the segments and the plan in the same kernels unless the many-CTA pass follows
+  const RouteOut sort_out = coop ? RouteOut{nullptr, nullptr, nullptr, nullptr} : out;
+  const int sort_plan = with_plan && !coop ? 1 : 0;
+  const uint64_t* sorted = nullptr;
   // bits of the largest id; the radix path packs (id, index) into 32 bits
   int idbits = 1;
   while (idbits < 31 && (int64_t(1) << idbits) < vocab) ++idbits;
@@ -612,53 +990,83 @@ cudaError_t launch_route(const int32_t* ids, int64_t T, int64_t vocab, void* scr
     const int passes = (idbits + 7) / 8;
     if (T <= kRadixN) {
       route_radix_small_kernel<<<1, 1024, kRadixSmallSmem, stream>>>(
-          ids, T, vocab, passes, k0, out.perm, out.seg_start, out.seg_id, out.n_seg, st, pl,
-          with_plan);
+          ids, T, vocab, passes, k0, sort_out.perm, sort_out.seg_start, sort_out.seg_id,
+          sort_out.n_seg, st, pl, sort_plan);
       count_launch();
-      *sorted_keys = k0;
-      return cudaGetLastError();
+      sorted = k0;
+    } else {
+      const int64_t nblk = (T + kRadixN - 1) / kRadixN;
+      route_radix_chunk_kernel<<<unsigned(nblk), 1024, sizeof(RadixSmem), stream>>>(
+          ids, T, vocab, passes, k0, st);
+      count_launch();
+      uint64_t *src = k0, *dst = k1;
+      for (int64_t w = kRadixN; w < T; w *= 2) {
+        route_merge_kernel<<<unsigned((T + 255) / 256), 256, 0, stream>>>(src, dst, T, w);
+        count_launch();
+        uint64_t* t = src;
+        src = dst;
+        dst = t;
+      }
+      sorted = src;
+      if (!coop) {
+        route_segment_kernel<<<1, 1024, 0, stream>>>(src, T, out.perm, out.seg_start,
+                                                     out.seg_id, out.n_seg, st, pl, sort_plan);
+        count_launch();
+      }
     }
-    const int64_t nblk = (T + kRadixN - 1) / kRadixN;
-    route_radix_chunk_kernel<<<unsigned(nblk), 1024, sizeof(RadixSmem), stream>>>(
-        ids, T, vocab, passes, k0, st);
+  } else if (T <= kChunk) {
+    route_small_kernel<<<1, 1024, 0, stream>>>(ids, T, vocab, k0, sort_out.perm,
+                                               sort_out.seg_start, sort_out.seg_id,
+                                               sort_out.n_seg, st, pl, sort_plan);
+    count_launch();
+    sorted = k0;
+  } else {
+    const int64_t nchunks = (T + kChunk - 1) / kChunk;
+    route_chunk_kernel<<<unsigned(nchunks), 1024, 0, stream>>>(ids, T, vocab, k0, st);
     count_launch();
     uint64_t *src = k0, *dst = k1;
-    for (int64_t w = kRadixN; w < T; w *= 2) {
+    for (int64_t w = kChunk; w < T; w *= 2) {
       route_merge_kernel<<<unsigned((T + 255) / 256), 256, 0, stream>>>(src, dst, T, w);
       count_launch();
       uint64_t* t = src;
       src = dst;
       dst = t;
     }
-    route_segment_kernel<<<1, 1024, 0, stream>>>(src, T, out.perm, out.seg_start, out.seg_id,
-                                                 out.n_seg, st, pl, with_plan);
-    count_launch();
-    *sorted_keys = src;
-    return cudaGetLastError();
+    sorted = src;
+    if (!coop) {
+      route_segment_kernel<<<1, 1024, 0, stream>>>(src, T, out.perm, out.seg_start, out.seg_id,
+                                                   out.n_seg, st, pl, sort_plan);
+      count_launch();
+    }
   }
-  if (T <= kChunk) {
-    route_small_kernel<<<1, 1024, 0, stream>>>(ids, T, vocab, k0, out.perm, out.seg_start,
-                                               out.seg_id, out.n_seg, st, pl, with_plan);
-    count_launch();
-    *sorted_keys = k0;
-    return cudaGetLastError();
-  }
-  const int64_t nchunks = (T + kChunk - 1) / kChunk;
-  route_chunk_kernel<<<unsigned(nchunks), 1024, 0, stream>>>(ids, T, vocab, k0, st);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  *sorted_keys = sorted;
+  if (!coop) return cudaSuccess;
+  // the many-CTA segment and plan pass: one cooperative launch, its barrier counter zeroed
+  CoopScratch* cs = reinterpret_cast<CoopScratch*>(
+      static_cast<char*>(scratch) + 2 * align_up(size_t(T) * sizeof(uint64_t), kAlign));
+  e = cudaMemsetAsync(&cs->bar, 0, sizeof(unsigned), stream);
+  if (e != cudaSuccess) return e;
+  int G = int((T + 511) / 512);
+  const int sms = device_sm_count();
+  if (G > sms) G = sms;
+  if (G > kCoopMaxCtas) G = kCoopMaxCtas;
+  if (G < 1) G = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(unsigned(G));
+  cfg.blockDim = dim3(kCoopThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeCooperative;
+  at[0].val.cooperative = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, route_plan_coop_kernel, sorted, T, out.perm, out.seg_start,
+                         out.seg_id, out.n_seg, st, pl, cs);
   count_launch();
-  uint64_t *src = k0, *dst = k1;
-  for (int64_t w = kChunk; w < T; w *= 2) {
-    route_merge_kernel<<<unsigned((T + 255) / 256), 256, 0, stream>>>(src, dst, T, w);
-    count_launch();
-    uint64_t* t = src;
-    src = dst;
-    dst = t;
-  }
-  route_segment_kernel<<<1, 1024, 0, stream>>>(src, T, out.perm, out.seg_start, out.seg_id,
-                                               out.n_seg, st, pl, with_plan);
-  count_launch();
-  *sorted_keys = src;
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace l3
