@@ -92,10 +92,19 @@ FP32_FMA_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
 # kernel, from one ncu capture of the current kernel code on that workload (cold cache);
 # an entry is removed when its kernel changes, and the roofline then reports null.
 NCU_TRAFFIC = {
-    ("prefill-bf16", "attend"): 206.086656e6 + 4.008448e6,       # attend_mma_kernel<16,8,2>
-    ("prefill-bf16", "attend_long"): 99.067136e6 + 3.023104e6,   # attend_tc_kernel
-    ("prefill-bf16", "mix"): 38.060800e6 + 0.069888e6,           # tc_gemm_kernel<256,2,4,0>
-    ("prefill-bf16", "up"): 6.864128e6 + 0.003584e6,             # tc_gemm_kernel<256,1,4,0>
+    ("prefill-bf16", "attend"): 206.21e6 + 0.98e6,     # attend_mma_kernel<16,8,2>
+    ("prefill-bf16", "attend_long"): 99.07e6 + 0.30e6,  # attend_tc_kernel
+    ("prefill-bf16", "mix"): 38.06e6,                  # tc_gemm_kernel<256,2,4,0,0>
+    ("prefill-bf16", "up"): 6.86e6,                    # tc_gemm_kernel<256,1,4,0,0>
+    ("decode-bf16", "attend"): 85.22e6 + 0.13e6,       # attend_mma_kernel<8,16,4>
+}
+# Captures too large for ncu's replay at full size, taken on a reduced batch of the same
+# shapes: (DRAM bytes of the launch, algorithmic bytes of the launch on that batch, the
+# batch). The full-size traffic is the captured bytes scaled by the ratio of algorithmic
+# bytes (the rows read grow with the distinct ids the batch touches).
+NCU_TRAFFIC_SCALED = {
+    ("large-prefill-bf16", "attend"): (1167.85e6 + 6.10e6, 1109.75488e6,
+                                       "table rows 1048576, T 16384"),
 }
 
 
@@ -574,7 +583,7 @@ def run_ours(args, rank, world, local_rank):
                 "attend_long": "gather-attend (tensor-core)"}[names[dom]]
         roof = {"kernel": kern, "bound": "hbm", "achieved": achieved,
                 "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                "traffic": None}
+                "traffic": None, "bytes_per_launch": hbm_bytes[names[dom]]}
     else:
         flops = acct["up_flops"] if names[dom] == "up" else acct["mix_flops"]
         achieved = flops / dom_s / 1e12
@@ -586,8 +595,13 @@ def run_ours(args, rank, world, local_rank):
             roof = {"kernel": "gemm-" + names[dom] + " (fp32 CUDA cores)", "bound": "alu",
                     "achieved": achieved, "peak": FP32_FMA_TFLOPS, "unit": "TFLOP/s",
                     "frac": achieved / FP32_FMA_TFLOPS, "traffic": None}
-    roof["traffic"] = NCU_TRAFFIC.get((p.name, names[dom])) if args.rows is None and \
-        args.tokens is None and args.vocab is None else None
+    full_size = args.rows is None and args.tokens is None and args.vocab is None
+    roof["traffic"] = NCU_TRAFFIC.get((p.name, names[dom])) if full_size else None
+    sc = NCU_TRAFFIC_SCALED.get((p.name, names[dom]))
+    if full_size and sc is not None and roof.get("bytes_per_launch"):
+        roof["traffic"] = sc[0] * roof["bytes_per_launch"] / sc[1]
+        roof["traffic_note"] = ("scaled from an ncu capture on a reduced batch (" + sc[2] +
+                                ") by the ratio of algorithmic bytes")
     roof["peak_source"] = peaks["source"] if roof["bound"] != "alu" else (
         "derived: 148 SMs x 128 fp32 lanes x 2 FLOP x 2.032 GHz")
     line = {

@@ -153,6 +153,19 @@ def test_forward_ragged_tile_shapes_all_tokens():
     assert l3.l3_get_error(c.ws) == 0
 
 
+def test_forward_many_cta_plan_all_tokens():
+    # 9000 tokens (above the 8192 that one CTA sorts and plans): the many-CTA segment and
+    # plan pass, on the ragged shape (short segments split, long ones on tensor cores); all
+    # tokens against the oracle, the saved (max, denominator) too
+    c = Case(6, T=9000)
+    y, sv = c.forward(saved=True)
+    fw = c.oracle_forward()
+    assert_close(c.p, to_np(y), fw.y, "y")
+    a, ml, _, _ = c.saved_views(sv)
+    assert_fp32_close(to_np(ml[:, 0]), fw.m, "max score", rtol=1e-5)
+    assert l3.l3_get_error(c.ws) == 0
+
+
 def test_forward_bf16_fp32_output():
     c = Case(2, T=512)
     y, _ = c.forward(y_dtype=torch.float32)
