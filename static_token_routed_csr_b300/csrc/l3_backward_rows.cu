@@ -531,26 +531,36 @@ __global__ void __launch_bounds__(kBThreads, 2) seg_rows_kernel(const SegRowsArg
   int64_t local = s_first[1];
   // W loads: row wr of the unit, tokens 8 wg .. 8 wg + 7 of the step
   const int wr = tid & 63, wg = tid >> 6;
+  // the current segment's description, loaded once per segment (its loads form a chain of
+  // dependent global round trips: seg_start -> sorted key -> offsets)
+  int cur = -1, qs = 0, qe = 0, rbase = 0, n = 0;
+  int64_t nu = 0, uc = 0, cost_s = 0, srow0 = 0;
   while (s < S) {
-    const int64_t nu = a.seg_unit0[s + 1] - a.seg_unit0[s];
+    if (s != cur) {
+      nu = a.seg_unit0[s + 1] - a.seg_unit0[s];
+      cost_s = a.seg_cost0[s];
+      uc = nu > 0 ? (a.seg_cost0[s + 1] - cost_s) / nu : 0;
+      qs = a.seg_start[s];
+      qe = a.seg_start[s + 1];
+      srow0 = a.seg_row0[s];
+      const int t = int(a.sorted_keys[qs] >> 32);
+      rbase = a.offs[t];
+      n = a.offs[t + 1] - rbase;
+      cur = s;
+    }
     if (local >= nu) {
       ++s;
       local = 0;
       continue;
     }
-    const int64_t uc = (a.seg_cost0[s + 1] - a.seg_cost0[s]) / nu;
-    if (a.seg_cost0[s] + local * uc >= chi) break;
+    if (cost_s + local * uc >= chi) break;
     const int rb = int(local / ncb), cb = int(local % ncb);
     ++local;
     const int part = cb < ncb_k ? 0 : 1;
     const int width = part ? a.d_v : a.d;
     const int col0 = (part ? cb - ncb_k : cb) * kBCols;
-    const int qs = a.seg_start[s], qe = a.seg_start[s + 1];
-    const int t = int(a.sorted_keys[qs] >> 32);
-    const int rbase = a.offs[t];
-    const int n = a.offs[t + 1] - rbase;
     const int r0 = rb * kBRows;
-    const int64_t orow0 = int64_t(a.seg_row0[s]) + r0;  // output row of row r0
+    const int64_t orow0 = srow0 + r0;  // output row of row r0
     const __nv_bfloat16* Y = part ? a.da_sorted : a.x_sorted;
     const float* Wsrc = part ? a.p_buf : a.ds_buf;
     float* out = part ? a.dV_rows : a.dK_rows;
