@@ -92,6 +92,19 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 constexpr int kSwapLd = 65;
 constexpr int kSwapStageBytes = kBM * kSwapLd * 4;
 
+// Output box of the plain forms' TMA stores: 32 rows x 128 bytes.
+constexpr int kBoxRows = 32;
+constexpr int kBoxBytes = kBoxRows * 128;
+
+// Dynamic shared memory: the stage ring, 1024 bytes of alignment slack, then either the
+// barriers (256 bytes) and the transposed epilogue's staging, or the barriers padded to
+// 1024 bytes and four warps' pairs of output boxes.
+template <int BN, int STAGES, bool SPLIT, bool SWAP>
+constexpr int tc_smem_bytes() {
+  return STAGES * (kBM + BN) * kBK * 2 + 1024 +
+         (SPLIT || SWAP ? 256 + (SWAP && !SPLIT ? kSwapStageBytes : 0) : 1024 + 8 * kBoxBytes);
+}
+
 // NACC * BN TMEM columns per accumulator set; two sets (the epilogue of one tile overlaps
 // the next tile's MMAs) when they fit in the 512 columns, else one.
 // SWAP (batches of at most 64 tokens): the weight matrix is the 128-row operand A (rows =
@@ -103,7 +116,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA1,
                    const __grid_constant__ CUtensorMap mapA2,
                    const __grid_constant__ CUtensorMap mapB,
-                   const __grid_constant__ CUtensorMap mapB2, const TcParams p) {
+                   const __grid_constant__ CUtensorMap mapB2,
+                   const __grid_constant__ CUtensorMap mapY, const TcParams p) {
   static_assert(NACC * BN <= int(kTmemCols), "TMEM budget");
   constexpr uint32_t NBUF = 2 * NACC * BN <= int(kTmemCols) ? 2 : 1;
   constexpr int A_BYTES = kBM * kBK * 2;
@@ -254,6 +268,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) p.cs_out[r] = sum;
       }
     }
+    // Output staging of the plain forms: two boxes of 32 rows x 128 bytes per warp, written
+    // in the 128-byte swizzle pattern (conflict-free: the 8 lanes of a store phase hit 8
+    // distinct 16-byte columns) and stored by TMA from lane 0 as whole lines.
+    unsigned char* stage = smem + STAGES * STAGE_BYTES + 1024 + (warp - 2) * 2 * kBoxBytes;
+    uint32_t nbox = 0;
+    bool prev_stored = false;
+    auto stage_box = [&](uint32_t i) {
+      // the store that used this buffer two boxes ago must have read it
+      if (lane == 0 && i >= 2) {
+        if (prev_stored)
+          tc::bulk_wait_read<1>();
+        else
+          tc::bulk_wait_read<0>();
+      }
+      __syncwarp();
+      return stage + (i & 1) * kBoxBytes;
+    };
+    auto store_box = [&](unsigned char* box, int x, int y) {
+      tc::fence_proxy_async();  // this thread's shared-memory writes, to the async proxy
+      __syncwarp();
+      prev_stored = y < p.M;  // a warp whose 32 rows all lie past the end stores nothing
+      if (lane == 0 && prev_stored) {
+        tc::tma_store_2d(&mapY, box, x, y);
+        tc::bulk_commit();
+      }
+    };
     uint32_t lt = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++lt) {
       int m_blk, n_blk, k_lo, k_hi;
@@ -373,14 +413,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           mean = fmaf(delta, wb, mean);
           m2 += bm2 + delta * delta * float(cnt) * wb;
           cnt += 64;
-          if (row_ok) {
-            uint4* dst = reinterpret_cast<uint4*>(p.U + int64_t(m) * p.N + n0 + c * 64);
+          // the warp's 32 rows x 64 columns as one 128-byte swizzled box, stored by TMA
+          unsigned char* box = stage_box(nbox);
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              dst[j] = make_uint4(pack_bf16(v[8 * j], v[8 * j + 1]), pack_bf16(v[8 * j + 2], v[8 * j + 3]),
-                                  pack_bf16(v[8 * j + 4], v[8 * j + 5]),
-                                  pack_bf16(v[8 * j + 6], v[8 * j + 7]));
-          }
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<uint4*>(box + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                make_uint4(pack_bf16(v[8 * j], v[8 * j + 1]), pack_bf16(v[8 * j + 2], v[8 * j + 3]),
+                           pack_bf16(v[8 * j + 4], v[8 * j + 5]),
+                           pack_bf16(v[8 * j + 6], v[8 * j + 7]));
+          store_box(box, n0 + c * 64, m - lane);
+          ++nbox;
         }
         if (row_ok) {
           float* st = p.stats + (int64_t(n_blk) * p.M + m) * 2;
@@ -408,6 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           p.mu_out[m] = mean;
           p.rstd_out[m] = rstd;
         }
+        unsigned char* ybox = nullptr;
         for (int c = 0; c < BN / 32; ++c) {
           if (c * 32 >= ncols) break;
           float v0[32], v1[32];
@@ -416,23 +459,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float* cs = p.colsum + n0 + c * 32;
 #pragma unroll
           for (int j = 0; j < 32; ++j) v0[j] = fmaf(rstd, v0[j] - mean * __ldg(cs + j), v1[j]);
-          if (row_ok) {
-            if (p.y_dtype == L3_BF16) {
-              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.Y) +
-                                                    int64_t(m) * p.N + n0 + c * 32);
+          if (p.y_dtype == L3_BF16) {
+            // two 32-column steps fill one 64-column box (N is a multiple of 64)
+            if ((c & 1) == 0) ybox = stage_box(nbox);
 #pragma unroll
-              for (int j = 0; j < 4; ++j)
-                dst[j] = make_uint4(pack_bf16(v0[8 * j], v0[8 * j + 1]),
-                                    pack_bf16(v0[8 * j + 2], v0[8 * j + 3]),
-                                    pack_bf16(v0[8 * j + 4], v0[8 * j + 5]),
-                                    pack_bf16(v0[8 * j + 6], v0[8 * j + 7]));
-            } else {
-              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.Y) +
-                                                      int64_t(m) * p.N + n0 + c * 32);
-#pragma unroll
-              for (int j = 0; j < 8; ++j)
-                dst[j] = make_float4(v0[4 * j], v0[4 * j + 1], v0[4 * j + 2], v0[4 * j + 3]);
+            for (int j = 0; j < 4; ++j)
+              *reinterpret_cast<uint4*>(ybox + lane * 128 +
+                                        ((((c & 1) * 4 + j) ^ (lane & 7)) << 4)) =
+                  make_uint4(pack_bf16(v0[8 * j], v0[8 * j + 1]),
+                             pack_bf16(v0[8 * j + 2], v0[8 * j + 3]),
+                             pack_bf16(v0[8 * j + 4], v0[8 * j + 5]),
+                             pack_bf16(v0[8 * j + 6], v0[8 * j + 7]));
+            if ((c & 1) == 1) {
+              store_box(ybox, n0 + (c - 1) * 32, m - lane);
+              ++nbox;
             }
+          } else {
+            ybox = stage_box(nbox);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              *reinterpret_cast<float4*>(ybox + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                  make_float4(v0[4 * j], v0[4 * j + 1], v0[4 * j + 2], v0[4 * j + 3]);
+            store_box(ybox, n0 + c * 32, m - lane);
+            ++nbox;
           }
         }
       }
@@ -440,6 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&tempty[b]);
     }
+    if (lane == 0) tc::bulk_wait_all();  // the outputs are written before the CTA exits
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -481,11 +531,30 @@ bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, in
 
 int num_sms() { return device_sm_count(); }
 
+// Row-major output matrix [rows, cols] of 2- or 4-byte elements for the epilogue's TMA
+// stores: box of 32 rows x 128 bytes, 128-byte swizzle.
+bool make_out_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, bool f32) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const int esz = f32 ? 4 : 2;
+  cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
+  cuuint64_t strides[1] = {cuuint64_t(cols) * esz};
+  cuuint32_t box[2] = {cuuint32_t(128 / esz), cuuint32_t(kBoxRows)};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// `y` is the output map of the plain forms (U for GEMM-up, Y for GEMM-mix); the split and
+// transposed forms store with ordinary instructions and ignore it.
 template <int BN, int NACC, int STAGES, bool SPLIT, bool SWAP = false>
 cudaError_t launch_tc(const CUtensorMap& a1, const CUtensorMap& a2, const CUtensorMap& b,
-                      const CUtensorMap& b2, const TcParams& p, cudaStream_t stream) {
-  constexpr int kSmem =
-      STAGES * (kBM + BN) * kBK * 2 + 1024 + 256 + (SWAP && !SPLIT ? kSwapStageBytes : 0);
+                      const CUtensorMap& b2, const CUtensorMap& y, const TcParams& p,
+                      cudaStream_t stream) {
+  constexpr int kSmem = tc_smem_bytes<BN, STAGES, SPLIT, SWAP>();
+  static_assert(kSmem <= 232448, "dynamic shared memory per block");
   auto kern = tc_gemm_kernel<BN, NACC, STAGES, SPLIT, SWAP>;
   const cudaError_t attr = ensure_smem_attr(kern, kSmem);
   if (attr != cudaSuccess) return attr;
@@ -493,7 +562,7 @@ cudaError_t launch_tc(const CUtensorMap& a1, const CUtensorMap& a2, const CUtens
   // a side job (row sums) is spread over every SM even when there are fewer tiles
   const int grid = units < num_sms() && !p.cs_W ? units : num_sms();
   const cudaError_t e = launch_pdl(kern, dim3(grid), dim3(kThreads), size_t(kSmem), stream, a1,
-                                   a2, b, b2, p);
+                                   a2, b, b2, y, p);
   count_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -755,7 +824,7 @@ cudaError_t launch_tc_up(const __nv_bfloat16* A, const __nv_bfloat16* W_up, int6
       p.cs_cols = d;
       p.cs_out = colsum;
     }
-    return launch_tc<kSwapBN, 1, 6, false, true>(mw, mw, ma, ma, p, stream);
+    return launch_tc<kSwapBN, 1, 6, false, true>(mw, mw, ma, ma, ma, p, stream);
   }
   CUtensorMap ma, mb;
   if (!make_map(&ma, A, T, d_v, kBM) || !make_map(&mb, W_up, d, d_v, kUpBN))
@@ -781,9 +850,13 @@ cudaError_t launch_tc_up(const __nv_bfloat16* A, const __nv_bfloat16* W_up, int6
   p.splits = splitk_parts(T, d, kUpBN, p.kb1);
   if (p.splits > 1 && (!slab || size_t(p.splits) * size_t(T) * size_t(d) > slab_floats))
     p.splits = 1;  // no room for the parts: one K range per tile
-  if (p.splits == 1) return launch_tc<kUpBN, 1, 4, false>(ma, ma, mb, mb, p, stream);
+  if (p.splits == 1) {
+    CUtensorMap mu;
+    if (!make_out_map(&mu, U, T, d, false)) return cudaErrorInvalidValue;
+    return launch_tc<kUpBN, 1, 4, false>(ma, ma, mb, mb, mu, p, stream);
+  }
   p.slab = slab;
-  const cudaError_t e = launch_tc<kUpBN, 1, 4, true>(ma, ma, mb, mb, p, stream);
+  const cudaError_t e = launch_tc<kUpBN, 1, 4, true>(ma, ma, mb, mb, mb, p, stream);
   if (e != cudaSuccess) return e;
   const int64_t warps = T * ((d + kUpBN - 1) / kUpBN);
   const cudaError_t e2 = launch_pdl(splitk_up_finish_kernel, dim3(unsigned((warps + 7) / 8)),
@@ -816,7 +889,7 @@ cudaError_t launch_tc_mix(const __nv_bfloat16* U, const __nv_bfloat16* x,
     p.st = st;
     p.splits = parts;
     p.slab = slab;
-    cudaError_t e = launch_tc<kSwapBN, 2, 6, true, true>(mw, mw, mu, mx, p, stream);
+    cudaError_t e = launch_tc<kSwapBN, 2, 6, true, true>(mw, mw, mu, mx, mx, p, stream);
     if (e != cudaSuccess) return e;
     e = launch_pdl(splitk_mix_swap_finish_kernel, dim3(unsigned(T)), dim3(256), 0,
                    stream, slab, parts, d, int(T), stats, tc_up_stat_tiles(d), int(kBM), colsum,
@@ -848,9 +921,13 @@ cudaError_t launch_tc_mix(const __nv_bfloat16* U, const __nv_bfloat16* x,
   p.splits = parts;
   if (p.splits > 1 && (!slab || 2 * size_t(p.splits) * size_t(T) * size_t(d) > slab_floats))
     return cudaErrorInvalidValue;  // the workspace is sized for the parts
-  if (p.splits == 1) return launch_tc<kMixBN, 2, 4, false>(mu, mx, mw, mw, p, stream);
+  if (p.splits == 1) {
+    CUtensorMap my;
+    if (!make_out_map(&my, y, T, d, y_dtype != L3_BF16)) return cudaErrorInvalidValue;
+    return launch_tc<kMixBN, 2, 4, false>(mu, mx, mw, mw, my, p, stream);
+  }
   p.slab = slab;
-  const cudaError_t e = launch_tc<kMixSplitBN, 2, 6, true>(mu, mx, mw, mw, p, stream);
+  const cudaError_t e = launch_tc<kMixSplitBN, 2, 6, true>(mu, mx, mw, mw, mw, p, stream);
   if (e != cudaSuccess) return e;
   const int64_t warps = T * ((d + 255) / 256);
   const cudaError_t e2 = launch_pdl(
