@@ -94,8 +94,6 @@ FP32_FMA_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
 NCU_TRAFFIC = {
     ("prefill-bf16", "attend"): 206.21e6 + 0.98e6,     # attend_mma_kernel<16,8,2>
     ("prefill-bf16", "attend_long"): 99.07e6 + 0.30e6,  # attend_tc_kernel
-    ("prefill-bf16", "mix"): 38.06e6,                  # tc_gemm_kernel<256,2,4,0,0>
-    ("prefill-bf16", "up"): 6.86e6,                    # tc_gemm_kernel<256,1,4,0,0>
     ("decode-bf16", "attend"): 85.22e6 + 0.13e6,       # attend_mma_kernel<8,16,4>
 }
 # Captures too large for ncu's replay at full size, taken on a reduced batch of the same

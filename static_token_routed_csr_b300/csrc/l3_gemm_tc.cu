@@ -3,8 +3,8 @@
 // Summary, "Core Architecture": u = W_up a, then W_mix [LayerNorm(u); x]).
 //
 //   up:  U = A W_upᵀ          (M = T, N = d, K = d_v). The epilogue rounds U to bf16,
-//        stores it, and writes per-row partial LayerNorm statistics of its N tile:
-//        (sum, sum of squared deviations from the tile mean) of the rounded values.
+//        stores it, and writes per-row partial LayerNorm statistics of each 128 columns:
+//        (sum, sum of squared deviations from their mean) of the rounded values.
 //   mix: Y = [h; x] W_mixᵀ with h = (U - mu) rstd, never materialised. Two TMEM
 //        accumulators take the two halves of the K loop: acc0 = U W_mix[:, :d]ᵀ and
 //        acc1 = x W_mix[:, d:]ᵀ. LayerNorm is affine per row, so
@@ -12,11 +12,12 @@
 //        The epilogue merges the up GEMM's partial statistics (Chan's pairwise rule) into
 //        mu and rstd for its rows.
 //
-// One persistent CTA per SM, 6 warps: warp 0 issues TMA loads (128-byte swizzled K-major
+// One persistent CTA per SM, 10 warps: warp 0 issues TMA loads (128-byte swizzled K-major
 // tiles, BK = 64) into a ring of shared-memory stages; one thread of warp 1 issues
-// tcgen05.mma (M = 128, N = BN, K = 16 per instruction) into a double-buffered TMEM
-// accumulator; warps 2..5 drain TMEM (tcgen05.ld) and run the epilogue while the next
-// tile accumulates. Every mbarrier wait is bounded: a wait that runs out sets a status
+// tcgen05.mma (M = 128, N = BN, K = 16 per instruction) into a TMEM accumulator (double-
+// buffered where two fit in the 512 columns); warps 2..9 drain TMEM (tcgen05.ld) and run the
+// epilogue while the next tile accumulates, two warps per 32-lane quarter, one per half of
+// the columns (the split and transposed forms use warps 2..5 only). Every mbarrier wait is bounded: a wait that runs out sets a status
 // word, the CTA drains its copies and MMAs in flight, frees TMEM and returns.
 #include <cudaTypedefs.h>
 
@@ -31,7 +32,7 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 512;
 
 struct TcParams {
@@ -92,13 +93,20 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 constexpr int kSwapLd = 65;
 constexpr int kSwapStageBytes = kBM * kSwapLd * 4;
 
+// Longest K loop (in 64-wide blocks) whose next tile's A rows are prefetched into L2.
+constexpr int kPrefetchKb = 16;
+
 // Output box of the plain forms' TMA stores: 32 rows x 128 bytes.
 constexpr int kBoxRows = 32;
 constexpr int kBoxBytes = kBoxRows * 128;
 
+// Columns of one partial LayerNorm statistic of GEMM-up: each plain-form epilogue warp
+// covers one such half of a 256-column tile.
+constexpr int kStatBN = 128;
+
 // Dynamic shared memory: the stage ring, 1024 bytes of alignment slack, then either the
 // barriers (256 bytes) and the transposed epilogue's staging, or the barriers padded to
-// 1024 bytes and four warps' pairs of output boxes.
+// 1024 bytes and the eight epilogue warps' output boxes.
 template <int BN, int STAGES, bool SPLIT, bool SWAP>
 constexpr int tc_smem_bytes() {
   return STAGES * (kBM + BN) * kBK * 2 + 1024 +
@@ -119,7 +127,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap mapB2,
                    const __grid_constant__ CUtensorMap mapY, const TcParams p) {
   static_assert(NACC * BN <= int(kTmemCols), "TMEM budget");
+  // epilogue warps: eight in the plain forms (two per TMEM lane quarter, each taking half of
+  // the tile's columns), four in the split and transposed forms
+  constexpr int kEpiWarps = SPLIT || SWAP ? 4 : 8;
+  static_assert(SPLIT || SWAP || BN % 128 == 0, "plain forms split BN into two halves");
   constexpr uint32_t NBUF = 2 * NACC * BN <= int(kTmemCols) ? 2 : 1;
+  // One set of two accumulators (GEMM-mix, BN = 256): the epilogue frees acc0 (tempty[0])
+  // as soon as it holds its columns in registers, and acc1 (tempty[1]) at the end; the next
+  // tile's MMAs wait for each only when they first write it, so acc0's K half overlaps the
+  // rest of the epilogue.
+  constexpr bool kSplitFree = NACC == 2 && NBUF == 1;
   constexpr int A_BYTES = kBM * kBK * 2;
   constexpr int B_BYTES = BN * kBK * 2;
   constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -157,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&tfull[b], 1);
-      tc::mbar_init(&tempty[b], 4);
+      tc::mbar_init(&tempty[b], kEpiWarps);
     }
     tc::mbar_init(drain, 1);
     *abort_flag = 0;
@@ -183,6 +200,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
         int m_blk, n_blk, k_lo, k_hi;
         unit_of(u, m_blk, n_blk, k_lo, k_hi);
+        if (!SWAP && !SPLIT && kbt <= kPrefetchKb && u + int(gridDim.x) < units) {
+          // short K loops (GEMM-up): the next tile's rows of A, which the ring reaches only
+          // a few stages before its MMAs, go to L2 now
+          int m2, n2, k2lo, k2hi;
+          unit_of(u + int(gridDim.x), m2, n2, k2lo, k2hi);
+          if (m2 != m_blk)
+            for (int kb = k2lo; kb < k2hi; ++kb)
+              tc::tma_prefetch_l2_2d(kb < p.kb1 ? &mapA1 : &mapA2,
+                                     (kb < p.kb1 ? kb : kb - p.kb1) * kBK, m2 * kBM);
+        }
         for (int kb = k_lo; kb < k_hi; ++kb) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
           if (!tc::mbar_wait(&empty[s], ph ^ 1, abort_flag, p.st, 0x1)) {
@@ -225,12 +252,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         int m_blk, n_blk, k_lo, k_hi;
         unit_of(u, m_blk, n_blk, k_lo, k_hi);
         const uint32_t b = lt % NBUF, tph = (lt / NBUF) & 1;
-        if (!tc::mbar_wait(&tempty[b], tph ^ 1, abort_flag, p.st, 0x2)) {
-          ok = false;
-          break;
+        if (!kSplitFree) {
+          if (!tc::mbar_wait(&tempty[b], tph ^ 1, abort_flag, p.st, 0x2)) {
+            ok = false;
+            break;
+          }
+          tc::tc_fence_after();
         }
-        tc::tc_fence_after();
         for (int kb = k_lo; kb < k_hi; ++kb) {
+          if (kSplitFree && (kb == k_lo || kb == p.kb1)) {
+            // first MMA into this accumulator of the tile: the previous tile's epilogue
+            // has read it
+            if (!tc::mbar_wait(&tempty[kb < p.kb1 ? 0 : 1], tph ^ 1, abort_flag, p.st, 0x2)) {
+              ok = false;
+              break;
+            }
+            tc::tc_fence_after();
+          }
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
           if (!tc::mbar_wait(&full[s], ph, abort_flag, p.st, 0x4)) {
             ok = false;
@@ -258,38 +296,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       volatile int no_abort = 0;
       tc::mbar_wait(drain, 0, &no_abort, p.st, 0x20, 100000000ull);
     }
-  } else {
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
+  } else if (warp < 2 + kEpiWarps) {
+    const int q = warp & 3;         // TMEM lane quarter this warp may access
+    const int h = (warp - 2) >> 2;  // plain forms: the half of the tile's columns it takes
     const uint32_t lane_base = tmem + (uint32_t(q * 32) << 16);
     if (p.cs_W) {  // while the first accumulator fills
-      for (int64_t r = int64_t(blockIdx.x) * 4 + (warp - 2); r < p.cs_rows;
-           r += int64_t(gridDim.x) * 4) {
+      for (int64_t r = int64_t(blockIdx.x) * kEpiWarps + (warp - 2); r < p.cs_rows;
+           r += int64_t(gridDim.x) * kEpiWarps) {
         const float sum = warp_row_sum(p.cs_W + r * p.cs_ld, p.cs_cols, lane);
         if (lane == 0) p.cs_out[r] = sum;
       }
     }
-    // Output staging of the plain forms: two boxes of 32 rows x 128 bytes per warp, written
+    // Output staging of the plain forms: one box of 32 rows x 128 bytes per warp, written
     // in the 128-byte swizzle pattern (conflict-free: the 8 lanes of a store phase hit 8
     // distinct 16-byte columns) and stored by TMA from lane 0 as whole lines.
-    unsigned char* stage = smem + STAGES * STAGE_BYTES + 1024 + (warp - 2) * 2 * kBoxBytes;
-    uint32_t nbox = 0;
-    bool prev_stored = false;
-    auto stage_box = [&](uint32_t i) {
-      // the store that used this buffer two boxes ago must have read it
-      if (lane == 0 && i >= 2) {
-        if (prev_stored)
-          tc::bulk_wait_read<1>();
-        else
-          tc::bulk_wait_read<0>();
-      }
+    unsigned char* box = smem + STAGES * STAGE_BYTES + 1024 + (warp - 2) * kBoxBytes;
+    auto stage_box = [&]() {
+      if (lane == 0) tc::bulk_wait_read<0>();  // the box's previous store has read it
       __syncwarp();
-      return stage + (i & 1) * kBoxBytes;
     };
-    auto store_box = [&](unsigned char* box, int x, int y) {
+    auto store_box = [&](int x, int y) {
       tc::fence_proxy_async();  // this thread's shared-memory writes, to the async proxy
       __syncwarp();
-      prev_stored = y < p.M;  // a warp whose 32 rows all lie past the end stores nothing
-      if (lane == 0 && prev_stored) {
+      if (lane == 0 && y < p.M) {  // a warp whose 32 rows all lie past the end stores nothing
         tc::tma_store_2d(&mapY, box, x, y);
         tc::bulk_commit();
       }
@@ -389,43 +418,45 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else if (p.mode == 0) {
-        // One pass over the tile row, 64 columns per TMEM load: round to bf16, store, and
-        // fold each 64-column block's (mean, squared deviations) into the row's running
-        // pair by the pairwise rule.
+        // This warp's half of the tile row (kStatBN columns), 64 columns per TMEM load:
+        // round to bf16, store, and fold each 64-column block's (mean, squared deviations)
+        // into the half's running pair by the pairwise rule; the half's (sum, squared
+        // deviations) are the row's statistics of that kStatBN-column tile.
         float mean = 0.f, m2 = 0.f;
         int cnt = 0;
-        for (int c = 0; c < BN / 64; ++c) {
+        for (int cc = 0; cc < BN / 128; ++cc) {
+          const int c = h * (BN / 128) + cc;
           if (c * 64 >= ncols) break;
           float v[64];
           tc::tmem_ld64(acc0 + c * 64, v);
-          float bs = 0.f;
+          float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int j = 0; j < 64; ++j) {
             v[j] = round_bf16(v[j]);
-            bs += v[j];
+            ps[j & 3] += v[j];
           }
-          const float bmean = bs * (1.f / 64.f);
-          float bm2 = 0.f;
+          const float bmean = ((ps[0] + ps[1]) + (ps[2] + ps[3])) * (1.f / 64.f);
+          float pm[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int j = 0; j < 64; ++j) bm2 = fmaf(v[j] - bmean, v[j] - bmean, bm2);
+          for (int j = 0; j < 64; ++j) pm[j & 3] = fmaf(v[j] - bmean, v[j] - bmean, pm[j & 3]);
+          const float bm2 = (pm[0] + pm[1]) + (pm[2] + pm[3]);
           const float delta = bmean - mean;
           const float wb = 64.f / float(cnt + 64);
           mean = fmaf(delta, wb, mean);
           m2 += bm2 + delta * delta * float(cnt) * wb;
           cnt += 64;
           // the warp's 32 rows x 64 columns as one 128-byte swizzled box, stored by TMA
-          unsigned char* box = stage_box(nbox);
+          stage_box();
 #pragma unroll
           for (int j = 0; j < 8; ++j)
             *reinterpret_cast<uint4*>(box + lane * 128 + ((j ^ (lane & 7)) << 4)) =
                 make_uint4(pack_bf16(v[8 * j], v[8 * j + 1]), pack_bf16(v[8 * j + 2], v[8 * j + 3]),
                            pack_bf16(v[8 * j + 4], v[8 * j + 5]),
                            pack_bf16(v[8 * j + 6], v[8 * j + 7]));
-          store_box(box, n0 + c * 64, m - lane);
-          ++nbox;
+          store_box(n0 + c * 64, m - lane);
         }
-        if (row_ok) {
-          float* st = p.stats + (int64_t(n_blk) * p.M + m) * 2;
+        if (row_ok && cnt > 0) {
+          float* st = p.stats + (int64_t(n_blk * (BN / kStatBN) + h) * p.M + m) * 2;
           st[0] = mean * float(cnt);
           st[1] = m2;
         }
@@ -446,48 +477,66 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           rstd = 1.f / sqrtf(m2 / float(p.N) + p.eps);
         }
-        if (row_ok && n_blk == 0 && p.mu_out) {
+        if (row_ok && n_blk == 0 && h == 0 && p.mu_out) {
           p.mu_out[m] = mean;
           p.rstd_out[m] = rstd;
         }
-        unsigned char* ybox = nullptr;
-        for (int c = 0; c < BN / 32; ++c) {
+        // kSplitFree: this warp's half of acc0 into registers as acc0 - mu c, then acc0 is
+        // released
+        float a0[kSplitFree ? BN / 2 : 1];
+        if constexpr (kSplitFree) {
+#pragma unroll
+          for (int i = 0; i < BN / 64; ++i) {
+            float t[32];
+            tc::tmem_ld32(acc0 + uint32_t(h * (BN / 2) + i * 32), t);
+            const float* cs = p.colsum + n0 + h * (BN / 2) + i * 32;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) a0[i * 32 + j] = t[j] - mean * __ldg(cs + j);
+          }
+          tc::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&tempty[0]);
+        }
+#pragma unroll
+        for (int cc = 0; cc < BN / 64; ++cc) {
+          const int c = h * (BN / 64) + cc;  // this warp's half of the columns
           if (c * 32 >= ncols) break;
           float v0[32], v1[32];
-          tc::tmem_ld32(acc0 + c * 32, v0);
           tc::tmem_ld32(acc0 + BN + c * 32, v1);
-          const float* cs = p.colsum + n0 + c * 32;
+          if constexpr (kSplitFree) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v0[j] = fmaf(rstd, v0[j] - mean * __ldg(cs + j), v1[j]);
+            for (int j = 0; j < 32; ++j) v0[j] = fmaf(rstd, a0[cc * 32 + j], v1[j]);
+          } else {
+            tc::tmem_ld32(acc0 + c * 32, v0);
+            const float* cs = p.colsum + n0 + c * 32;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v0[j] = fmaf(rstd, v0[j] - mean * __ldg(cs + j), v1[j]);
+          }
           if (p.y_dtype == L3_BF16) {
             // two 32-column steps fill one 64-column box (N is a multiple of 64)
-            if ((c & 1) == 0) ybox = stage_box(nbox);
+            if ((c & 1) == 0) stage_box();
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-              *reinterpret_cast<uint4*>(ybox + lane * 128 +
+              *reinterpret_cast<uint4*>(box + lane * 128 +
                                         ((((c & 1) * 4 + j) ^ (lane & 7)) << 4)) =
                   make_uint4(pack_bf16(v0[8 * j], v0[8 * j + 1]),
                              pack_bf16(v0[8 * j + 2], v0[8 * j + 3]),
                              pack_bf16(v0[8 * j + 4], v0[8 * j + 5]),
                              pack_bf16(v0[8 * j + 6], v0[8 * j + 7]));
-            if ((c & 1) == 1) {
-              store_box(ybox, n0 + (c - 1) * 32, m - lane);
-              ++nbox;
-            }
+            if ((c & 1) == 1) store_box(n0 + (c - 1) * 32, m - lane);
           } else {
-            ybox = stage_box(nbox);
+            stage_box();
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-              *reinterpret_cast<float4*>(ybox + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+              *reinterpret_cast<float4*>(box + lane * 128 + ((j ^ (lane & 7)) << 4)) =
                   make_float4(v0[4 * j], v0[4 * j + 1], v0[4 * j + 2], v0[4 * j + 3]);
-            store_box(ybox, n0 + c * 32, m - lane);
-            ++nbox;
+            store_box(n0 + c * 32, m - lane);
           }
         }
       }
       tc::tc_fence_before();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&tempty[b]);
+      if (lane == 0) tc::mbar_arrive(&tempty[kSplitFree ? 1 : b]);
     }
     if (lane == 0) tc::bulk_wait_all();  // the outputs are written before the CTA exits
   }
@@ -581,9 +630,9 @@ int splitk_parts(int64_t M, int N, int BN, int kbt) {
   return s < 1 ? 1 : s;
 }
 
-// Split-K finish of GEMM-up: U = bf16(sum of the parts), and per 256-column tile the
-// row's (sum, squared deviations from the tile mean) of the rounded values, as the fused
-// epilogue writes them. One warp per (row, tile), 8 columns per lane.
+// Split-K finish of GEMM-up: U = bf16(sum of the parts), and per 128 columns the row's
+// (sum, squared deviations from their mean) of the rounded values, as the fused epilogue
+// writes them. One warp per (row, 256-column tile), 8 columns per lane.
 __global__ void splitk_up_finish_kernel(const float* __restrict__ slab, int parts, int M, int N,
                                         __nv_bfloat16* __restrict__ U, float* __restrict__ stats) {
   grid_dep_wait();
@@ -607,25 +656,29 @@ __global__ void splitk_up_finish_kernel(const float* __restrict__ slab, int part
       v[0] += a.x; v[1] += a.y; v[2] += a.z; v[3] += a.w;
       v[4] += b.x; v[5] += b.y; v[6] += b.z; v[7] += b.w;
     }
+  // statistics per kStatBN = 128 columns: lanes 0..15 and 16..31 reduce separately
+  const int half = lane >> 4;
+  const int hcols = ncols - half * kStatBN < kStatBN ? ncols - half * kStatBN : kStatBN;
   float sum = 0.f;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     v[j] = round_bf16(v[j]);
     sum += on ? v[j] : 0.f;
   }
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-  const float mean = sum / float(ncols);
+  for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  const float mean = hcols > 0 ? sum / float(hcols) : 0.f;
   float m2 = 0.f;
 #pragma unroll
   for (int j = 0; j < 8; ++j) m2 += on ? (v[j] - mean) * (v[j] - mean) : 0.f;
-  for (int o = 16; o > 0; o >>= 1) m2 += __shfl_xor_sync(0xffffffffu, m2, o);
+  for (int o = 8; o > 0; o >>= 1) m2 += __shfl_xor_sync(0xffffffffu, m2, o);
   if (on)
     *reinterpret_cast<uint4*>(U + int64_t(m) * N + c0) =
         make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]),
                    pack_bf16(v[6], v[7]));
-  if (lane == 0) {
-    stats[(int64_t(tile) * M + m) * 2] = sum;
-    stats[(int64_t(tile) * M + m) * 2 + 1] = m2;
+  if ((lane & 15) == 0 && hcols > 0) {
+    const int64_t j = int64_t(tile) * (kUpBN / kStatBN) + half;
+    stats[(j * M + m) * 2] = sum;
+    stats[(j * M + m) * 2 + 1] = m2;
   }
 }
 
@@ -909,8 +962,8 @@ cudaError_t launch_tc_mix(const __nv_bfloat16* U, const __nv_bfloat16* x,
   p.kb2 = d / kBK;
   p.mode = 1;
   p.stats_in = stats;
-  p.stat_tiles = (d + kUpBN - 1) / kUpBN;
-  p.stat_bn = kUpBN;
+  p.stat_tiles = (d + kStatBN - 1) / kStatBN;
+  p.stat_bn = kStatBN;
   p.colsum = colsum;
   p.eps = eps;
   p.Y = y;

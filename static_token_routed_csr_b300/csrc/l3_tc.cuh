@@ -126,6 +126,14 @@ __device__ __forceinline__ void tma_load_2d(const CUtensorMap* map, uint64_t* ba
       : "memory");
 }
 
+// Prefetch of a 2-D box of the tensor into L2 (no shared memory, no completion).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 // 2-D tiled store of a shared-memory box (laid out in the map's swizzle pattern) to the
 // tensor at (x, y), in the calling thread's current bulk async-group. Elements of the box
 // that fall outside the tensor are not written. x * element size must be a multiple of 16
