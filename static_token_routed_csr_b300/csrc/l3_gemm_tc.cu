@@ -21,6 +21,7 @@
 // word, the CTA drains its copies and MMAs in flight, frees TMEM and returns.
 #include <cudaTypedefs.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "l3_internal.h"
@@ -82,11 +83,18 @@ __device__ __forceinline__ float round_bf16(float v) {
   return __bfloat162float(__float2bfloat16_rn(v));
 }
 
+// Two floats rounded (to nearest even) to a bf16 pair, `a` in the low half, by one paired
+// conversion (the scalar conversions run at a fraction of the paired one's rate).
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-  const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(a));
-  const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(b));
-  return lo | (hi << 16);
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  uint32_t r;
+  memcpy(&r, &h, sizeof(r));
+  return r;
 }
+
+// The two values of a bf16 pair, as floats.
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
 // Shared staging of the swapped GEMM-up epilogue: 128 rows (features) x up to 64 columns
 // (tokens), row stride 65 floats (conflict-free both ways).
@@ -107,9 +115,9 @@ constexpr int kStatBN = 128;
 // Dynamic shared memory: the stage ring, 1024 bytes of alignment slack, then either the
 // barriers (256 bytes) and the transposed epilogue's staging, or the barriers padded to
 // 1024 bytes and the eight epilogue warps' output boxes.
-template <int BN, int STAGES, bool SPLIT, bool SWAP>
+template <int BN, int STAGES, bool SPLIT, bool SWAP, bool PAIR>
 constexpr int tc_smem_bytes() {
-  return STAGES * (kBM + BN) * kBK * 2 + 1024 +
+  return STAGES * (kBM + (PAIR ? BN / 2 : BN)) * kBK * 2 + 1024 +
          (SPLIT || SWAP ? 256 + (SWAP && !SPLIT ? kSwapStageBytes : 0) : 1024 + 8 * kBoxBytes);
 }
 
@@ -119,7 +127,14 @@ constexpr int tc_smem_bytes() {
 // output features, K contiguous, from mapA1 at every k-block) and the tokens are the N = 64
 // columns, from mapB for k-blocks below kb1 and mapB2 above; the epilogue writes the
 // transposed outputs.
-template <int BN, int NACC, int STAGES, bool SPLIT, bool SWAP = false>
+//
+// PAIR (plain forms): clusters of two CTAs share each tcgen05 MMA (M = 256: each CTA holds
+// its own 128 rows of A and half of the tile's BN rows of B; each receives its 128 rows of
+// the accumulator in its own TMEM). A CTA then reads a third less from L2 per output and
+// its shared memory carries a third less per MMA. The even CTA issues the MMAs; both CTAs'
+// TMA loads complete on its full barriers, its commits arrive on both CTAs' barriers, and
+// both CTAs' epilogue warps release the accumulator on its tempty barriers.
+template <int BN, int NACC, int STAGES, bool SPLIT, bool SWAP = false, bool PAIR = false>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA1,
                    const __grid_constant__ CUtensorMap mapA2,
@@ -137,8 +152,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // tile's MMAs wait for each only when they first write it, so acc0's K half overlaps the
   // rest of the epilogue.
   constexpr bool kSplitFree = NACC == 2 && NBUF == 1;
+  static_assert(!PAIR || (!SPLIT && !SWAP), "CTA pairs take the plain forms");
   constexpr int A_BYTES = kBM * kBK * 2;
-  constexpr int B_BYTES = BN * kBK * 2;
+  constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * kBK * 2;
   constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -152,16 +168,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = PAIR ? tc::cluster_rank() : 0u;  // CTA of the pair
+  const int cta0 = PAIR ? int(blockIdx.x >> 1) : int(blockIdx.x);  // first unit
+  const int ncta = PAIR ? int(gridDim.x >> 1) : int(gridDim.x);    // unit stride
   const int m_tiles = (p.M + kBM - 1) / kBM;
   const int n_tiles = (p.N + BN - 1) / BN;
-  const int tiles = m_tiles * n_tiles;
+  const int tiles = (PAIR ? (m_tiles + 1) / 2 : m_tiles) * n_tiles;
   const int splits = SPLIT ? p.splits : 1;
   const int units = tiles * splits;
   const int kbt = p.kb1 + p.kb2;
   // unit -> output tile and K range [k_lo, k_hi)
   auto unit_of = [&](int u, int& m_blk, int& n_blk, int& k_lo, int& k_hi) {
     const int tile = u % tiles, part = u / tiles;
-    m_blk = tile / n_tiles;
+    m_blk = PAIR ? (tile / n_tiles) * 2 + int(rank) : tile / n_tiles;
     n_blk = tile % n_tiles;
     k_lo = SPLIT ? int(int64_t(part) * kbt / splits) : 0;
     k_hi = SPLIT ? int(int64_t(part + 1) * kbt / splits) : kbt;
@@ -174,16 +193,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&tfull[b], 1);
-      tc::mbar_init(&tempty[b], kEpiWarps);
+      tc::mbar_init(&tempty[b], kEpiWarps * (PAIR ? 2 : 1));
     }
     tc::mbar_init(drain, 1);
     *abort_flag = 0;
     tc::fence_barrier_init();
     tc::fence_proxy_async();
   }
-  if (warp == 1) tc::tmem_alloc(tmem_slot, kTmemCols);
+  if (warp == 1) {
+    if (PAIR)
+      tc::tmem_alloc_pair(tmem_slot, kTmemCols);
+    else
+      tc::tmem_alloc(tmem_slot, kTmemCols);
+  }
   tc::tc_fence_before();
   __syncthreads();
+  if (PAIR) tc::cluster_sync();  // both CTAs' barriers exist before either signals the other
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   grid_dep_wait();  // the previous kernels' outputs (A or U, the statistics) are complete
@@ -197,14 +222,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (SWAP) tc::tma_prefetch_desc(&mapB2);
       uint32_t it = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+      for (int u = cta0; ok && u < units; u += ncta) {
         int m_blk, n_blk, k_lo, k_hi;
         unit_of(u, m_blk, n_blk, k_lo, k_hi);
-        if (!SWAP && !SPLIT && kbt <= kPrefetchKb && u + int(gridDim.x) < units) {
+        if (!SWAP && !SPLIT && kbt <= kPrefetchKb && u + ncta < units) {
           // short K loops (GEMM-up): the next tile's rows of A, which the ring reaches only
           // a few stages before its MMAs, go to L2 now
           int m2, n2, k2lo, k2hi;
-          unit_of(u + int(gridDim.x), m2, n2, k2lo, k2hi);
+          unit_of(u + ncta, m2, n2, k2lo, k2hi);
           if (m2 != m_blk)
             for (int kb = k2lo; kb < k2hi; ++kb)
               tc::tma_prefetch_l2_2d(kb < p.kb1 ? &mapA1 : &mapA2,
@@ -216,8 +241,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          tc::mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
           unsigned char* a_dst = smem + s * STAGE_BYTES;
+          if constexpr (PAIR) {
+            // both CTAs' halves complete on the even CTA's barrier
+            if (rank == 0) tc::mbar_arrive_expect_tx(&full[s], 2 * STAGE_BYTES);
+            const uint32_t fb = tc::map_to_rank(&full[s], 0);
+            if (kb < p.kb1)
+              tc::tma_load_2d_pair(&mapA1, fb, a_dst, kb * kBK, m_blk * kBM);
+            else
+              tc::tma_load_2d_pair(&mapA2, fb, a_dst, (kb - p.kb1) * kBK, m_blk * kBM);
+            tc::tma_load_2d_pair(&mapB, fb, a_dst + A_BYTES, kb * kBK,
+                                 n_blk * BN + int(rank) * (BN / 2));
+            ++it;
+            continue;
+          }
+          tc::mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
           if (SWAP) {
             tc::tma_load_2d(&mapA1, &full[s], a_dst, kb * kBK, m_blk * kBM);
             if (kb < p.kb1)
@@ -235,20 +273,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) {
-        // Let the copies already issued land before the CTA's shared memory goes away.
+        // Let the copies already issued land before the CTA's shared memory goes away (the
+        // odd CTA of a pair cannot watch the even CTA's barriers: it waits 200 us).
         const uint32_t first = it > uint32_t(STAGES) ? it - STAGES : 0;
         volatile int no_abort = 0;
-        for (uint32_t j = first; j < it; ++j)
-          tc::mbar_wait(&full[j % STAGES], (j / STAGES) & 1, &no_abort, p.st, 0x10,
-                        100000000ull);
+        if (PAIR && rank != 0) {
+          for (int i = 0; i < 200; ++i) __nanosleep(1000);
+        } else {
+          for (uint32_t j = first; j < it; ++j)
+            tc::mbar_wait(&full[j % STAGES], (j / STAGES) & 1, &no_abort, p.st, 0x10,
+                          100000000ull);
+        }
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      constexpr uint32_t idesc = tc::idesc_bf16_f32(kBM, BN);
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(PAIR ? 2 * kBM : kBM, BN);
       uint32_t it = 0, lt = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < units; u += gridDim.x, ++lt) {
+      for (int u = cta0; ok && u < units; u += ncta, ++lt) {
         int m_blk, n_blk, k_lo, k_hi;
         unit_of(u, m_blk, n_blk, k_lo, k_hi);
         const uint32_t b = lt % NBUF, tph = (lt / NBUF) & 1;
@@ -281,18 +324,37 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t a_addr = tc::smem_u32(smem + s * STAGE_BYTES);
           const uint32_t b_addr = a_addr + A_BYTES;
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k)
-            tc::mma_bf16(d_tmem, tc::desc_kmajor_sw128(a_addr + 32 * k),
-                         tc::desc_kmajor_sw128(b_addr + 32 * k), idesc,
-                         (first && k == 0) ? 0u : 1u);
-          tc::mma_commit(&empty[s]);
+          for (int k = 0; k < kBK / 16; ++k) {
+            if (PAIR)
+              tc::mma_bf16_pair(d_tmem, tc::desc_kmajor_sw128(a_addr + 32 * k),
+                                tc::desc_kmajor_sw128(b_addr + 32 * k), idesc,
+                                (first && k == 0) ? 0u : 1u);
+            else
+              tc::mma_bf16(d_tmem, tc::desc_kmajor_sw128(a_addr + 32 * k),
+                           tc::desc_kmajor_sw128(b_addr + 32 * k), idesc,
+                           (first && k == 0) ? 0u : 1u);
+          }
+          if (PAIR)
+            tc::mma_commit_pair(&empty[s], 0x3);
+          else
+            tc::mma_commit(&empty[s]);
           ++it;
         }
         if (!ok) break;
-        tc::mma_commit(&tfull[b]);
+        if (PAIR)
+          tc::mma_commit_pair(&tfull[b], 0x3);
+        else
+          tc::mma_commit(&tfull[b]);
       }
       // All MMAs issued by this thread must finish before TMEM is released.
-      tc::mma_commit(drain);
+      if (PAIR)
+        tc::mma_commit_pair(drain, 0x3);
+      else
+        tc::mma_commit(drain);
+      volatile int no_abort = 0;
+      tc::mbar_wait(drain, 0, &no_abort, p.st, 0x20, 100000000ull);
+    } else if (PAIR && lane == 0) {
+      // the odd CTA: the even CTA's MMAs into this CTA's TMEM are done before it is freed
       volatile int no_abort = 0;
       tc::mbar_wait(drain, 0, &no_abort, p.st, 0x20, 100000000ull);
     }
@@ -323,15 +385,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::bulk_commit();
       }
     };
+    // release of an accumulator: on this CTA's tempty barrier, or on the even CTA's
+    auto release = [&](int i) {
+      if (lane == 0) {
+        if (PAIR)
+          tc::mbar_arrive_cluster(tc::map_to_rank(&tempty[i], 0));
+        else
+          tc::mbar_arrive(&tempty[i]);
+      }
+    };
     uint32_t lt = 0;
-    for (int u = blockIdx.x; u < units; u += gridDim.x, ++lt) {
+    for (int u = cta0; u < units; u += ncta, ++lt) {
       int m_blk, n_blk, k_lo, k_hi;
       unit_of(u, m_blk, n_blk, k_lo, k_hi);
       const uint32_t b = lt % NBUF, tph = (lt / NBUF) & 1;
-      if (!tc::mbar_wait(&tfull[b], tph, abort_flag, p.st, 0x8)) break;
-      tc::tc_fence_after();
       const int m = m_blk * kBM + q * 32 + lane;
       const bool row_ok = m < p.M;
+      // GEMM-mix: merge the row's partial statistics from GEMM-up (fixed order:
+      // deterministic) while the tile's MMAs still run
+      float row_mean = 0.f, row_rstd = 0.f;
+      if (!SPLIT && !SWAP && p.mode == 1) {
+        const int mm = row_ok ? m : 0;
+        float tot = 0.f;
+        for (int j = 0; j < p.stat_tiles; ++j) tot += p.stats_in[(int64_t(j) * p.M + mm) * 2];
+        row_mean = tot / float(p.N);
+        float m2 = 0.f;
+        for (int j = 0; j < p.stat_tiles; ++j) {
+          const float* st = p.stats_in + (int64_t(j) * p.M + mm) * 2;
+          const int cnt = p.N - j * p.stat_bn < p.stat_bn ? p.N - j * p.stat_bn : p.stat_bn;
+          const float dm = st[0] / float(cnt) - row_mean;
+          m2 += st[1] + float(cnt) * dm * dm;
+        }
+        row_rstd = 1.f / sqrtf(m2 / float(p.N) + p.eps);
+      }
+      if (!tc::mbar_wait(&tfull[b], tph, abort_flag, p.st, 0x8)) break;
+      tc::tc_fence_after();
       const int n0 = n_blk * BN;
       const int ncols = p.N - n0 < BN ? p.N - n0 : BN;
       const uint32_t acc0 = lane_base + uint32_t(int(b) * NACC * BN);
@@ -429,12 +517,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (c * 64 >= ncols) break;
           float v[64];
           tc::tmem_ld64(acc0 + c * 64, v);
+          uint32_t w[32];  // the rounded values as stored; v takes them back as floats
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            w[j] = pack_bf16(v[2 * j], v[2 * j + 1]);
+            v[2 * j] = bf16_lo(w[j]);
+            v[2 * j + 1] = bf16_hi(w[j]);
+          }
           float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int j = 0; j < 64; ++j) {
-            v[j] = round_bf16(v[j]);
-            ps[j & 3] += v[j];
-          }
+          for (int j = 0; j < 64; ++j) ps[j & 3] += v[j];
           const float bmean = ((ps[0] + ps[1]) + (ps[2] + ps[3])) * (1.f / 64.f);
           float pm[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -450,9 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 8; ++j)
             *reinterpret_cast<uint4*>(box + lane * 128 + ((j ^ (lane & 7)) << 4)) =
-                make_uint4(pack_bf16(v[8 * j], v[8 * j + 1]), pack_bf16(v[8 * j + 2], v[8 * j + 3]),
-                           pack_bf16(v[8 * j + 4], v[8 * j + 5]),
-                           pack_bf16(v[8 * j + 6], v[8 * j + 7]));
+                make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
           store_box(n0 + c * 64, m - lane);
         }
         if (row_ok && cnt > 0) {
@@ -461,25 +551,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           st[1] = m2;
         }
       } else {
-        // Merge the partial statistics of the row (fixed order: deterministic).
-        float mean = 0.f, rstd = 0.f;
-        {
-          const int mm = row_ok ? m : 0;
-          float tot = 0.f;
-          for (int j = 0; j < p.stat_tiles; ++j) tot += p.stats_in[(int64_t(j) * p.M + mm) * 2];
-          mean = tot / float(p.N);
-          float m2 = 0.f;
-          for (int j = 0; j < p.stat_tiles; ++j) {
-            const float* st = p.stats_in + (int64_t(j) * p.M + mm) * 2;
-            const int cnt = p.N - j * p.stat_bn < p.stat_bn ? p.N - j * p.stat_bn : p.stat_bn;
-            const float dm = st[0] / float(cnt) - mean;
-            m2 += st[1] + float(cnt) * dm * dm;
-          }
-          rstd = 1.f / sqrtf(m2 / float(p.N) + p.eps);
-        }
+        // row_mean and row_rstd: merged above, before the wait
         if (row_ok && n_blk == 0 && h == 0 && p.mu_out) {
-          p.mu_out[m] = mean;
-          p.rstd_out[m] = rstd;
+          p.mu_out[m] = row_mean;
+          p.rstd_out[m] = row_rstd;
         }
         // kSplitFree: this warp's half of acc0 into registers as acc0 - mu c, then acc0 is
         // released
@@ -491,11 +566,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::tmem_ld32(acc0 + uint32_t(h * (BN / 2) + i * 32), t);
             const float* cs = p.colsum + n0 + h * (BN / 2) + i * 32;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) a0[i * 32 + j] = t[j] - mean * __ldg(cs + j);
+            for (int j = 0; j < 32; ++j) a0[i * 32 + j] = t[j] - row_mean * __ldg(cs + j);
           }
           tc::tc_fence_before();
           __syncwarp();
-          if (lane == 0) tc::mbar_arrive(&tempty[0]);
+          release(0);
         }
 #pragma unroll
         for (int cc = 0; cc < BN / 64; ++cc) {
@@ -505,12 +580,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::tmem_ld32(acc0 + BN + c * 32, v1);
           if constexpr (kSplitFree) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v0[j] = fmaf(rstd, a0[cc * 32 + j], v1[j]);
+            for (int j = 0; j < 32; ++j) v0[j] = fmaf(row_rstd, a0[cc * 32 + j], v1[j]);
           } else {
             tc::tmem_ld32(acc0 + c * 32, v0);
             const float* cs = p.colsum + n0 + c * 32;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v0[j] = fmaf(rstd, v0[j] - mean * __ldg(cs + j), v1[j]);
+            for (int j = 0; j < 32; ++j) v0[j] = fmaf(row_rstd, v0[j] - row_mean * __ldg(cs + j), v1[j]);
           }
           if (p.y_dtype == L3_BF16) {
             // two 32-column steps fill one 64-column box (N is a multiple of 64)
@@ -536,16 +611,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc::tc_fence_before();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&tempty[kSplitFree ? 1 : b]);
+      release(kSplitFree ? 1 : int(b));
     }
     if (lane == 0) tc::bulk_wait_all();  // the outputs are written before the CTA exits
   }
   tc::tc_fence_before();
   __syncthreads();
+  if (PAIR) tc::cluster_sync();  // neither CTA frees TMEM or exits while the other works
   tc::tc_fence_after();
   if (warp == 1) {
     __syncwarp();
-    tc::tmem_dealloc(tmem, kTmemCols);
+    if (PAIR)
+      tc::tmem_dealloc_pair(tmem, kTmemCols);
+    else
+      tc::tmem_dealloc(tmem, kTmemCols);
   }
 }
 
@@ -598,15 +677,53 @@ bool make_out_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols
 
 // `y` is the output map of the plain forms (U for GEMM-up, Y for GEMM-mix); the split and
 // transposed forms store with ordinary instructions and ignore it.
-template <int BN, int NACC, int STAGES, bool SPLIT, bool SWAP = false>
+// Persistent launch of a CTA-pair kernel: one pair per two SMs that can hold a cluster of
+// two (looked up once), at most one per unit; programmatic dependent launch as launch_pdl.
+template <typename K, typename... Args>
+cudaError_t launch_pairs(K* kern, int units, int smem, cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = size_t(smem);
+  cfg.stream = stream;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  static int max_pairs = 0;  // per kernel instantiation
+  if (max_pairs == 0) {
+    cfg.gridDim = dim3(2 * (num_sms() / 2));
+    cfg.numAttrs = 1;
+    int n = 0;
+    const cudaError_t q = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (q != cudaSuccess) return q;
+    if (n < 1) return cudaErrorInvalidConfiguration;
+    max_pairs = n;
+  }
+  const int pairs = units < max_pairs ? units : max_pairs;
+  cfg.gridDim = dim3(2 * pairs);
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+template <int BN, int NACC, int STAGES, bool SPLIT, bool SWAP = false, bool PAIR = false>
 cudaError_t launch_tc(const CUtensorMap& a1, const CUtensorMap& a2, const CUtensorMap& b,
                       const CUtensorMap& b2, const CUtensorMap& y, const TcParams& p,
                       cudaStream_t stream) {
-  constexpr int kSmem = tc_smem_bytes<BN, STAGES, SPLIT, SWAP>();
+  constexpr int kSmem = tc_smem_bytes<BN, STAGES, SPLIT, SWAP, PAIR>();
   static_assert(kSmem <= 232448, "dynamic shared memory per block");
-  auto kern = tc_gemm_kernel<BN, NACC, STAGES, SPLIT, SWAP>;
+  auto kern = tc_gemm_kernel<BN, NACC, STAGES, SPLIT, SWAP, PAIR>;
   const cudaError_t attr = ensure_smem_attr(kern, kSmem);
   if (attr != cudaSuccess) return attr;
+  if constexpr (PAIR) {
+    const int pair_units = ((p.M + 2 * kBM - 1) / (2 * kBM)) * ((p.N + BN - 1) / BN);
+    const cudaError_t e = launch_pairs(kern, pair_units, kSmem, stream, a1, a2, b, b2, y, p);
+    count_launch();
+    return e != cudaSuccess ? e : cudaGetLastError();
+  }
   const int units = ((p.M + kBM - 1) / kBM) * ((p.N + BN - 1) / BN) * (SPLIT ? p.splits : 1);
   // a side job (row sums) is spread over every SM even when there are fewer tiles
   const int grid = units < num_sms() && !p.cs_W ? units : num_sms();
@@ -848,6 +965,14 @@ size_t tc_splitk_floats(int64_t T, int d, int d_v) {
 // (the buffer is sized for the larger count).
 int tc_up_stat_tiles(int d) { return (d + kBM - 1) / kBM; }
 
+// The plain forms run as CTA pairs when the GEMM has at least four waves of 128 x 256
+// tiles (the pairs' higher MMA rate then outweighs their coarser last wave and the pair
+// coupling; measured: 65536 tokens faster as pairs, 8192 tokens faster as single CTAs).
+bool use_pairs(int64_t M, int N) {
+  const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + 255) / 256);
+  return tiles >= 4 * int64_t(num_sms());
+}
+
 cudaError_t launch_tc_up(const __nv_bfloat16* A, const __nv_bfloat16* W_up, int64_t T, int d,
                          int d_v, __nv_bfloat16* U, float* stats, float* slab,
                          size_t slab_floats, const __nv_bfloat16* W_mix, float* colsum,
@@ -879,8 +1004,12 @@ cudaError_t launch_tc_up(const __nv_bfloat16* A, const __nv_bfloat16* W_up, int6
     }
     return launch_tc<kSwapBN, 1, 6, false, true>(mw, mw, ma, ma, ma, p, stream);
   }
+  const int splits = splitk_parts(T, d, kUpBN, d_v / kBK);
+  const bool split = splits > 1 && slab && size_t(splits) * size_t(T) * size_t(d) <= slab_floats;
+  const bool pairs = !split && use_pairs(T, d);
   CUtensorMap ma, mb;
-  if (!make_map(&ma, A, T, d_v, kBM) || !make_map(&mb, W_up, d, d_v, kUpBN))
+  // the CTA-pair form loads half of a tile's W_up rows per CTA
+  if (!make_map(&ma, A, T, d_v, kBM) || !make_map(&mb, W_up, d, d_v, pairs ? kUpBN / 2 : kUpBN))
     return cudaErrorInvalidValue;
   TcParams p{};
   p.M = int(T);
@@ -900,12 +1029,11 @@ cudaError_t launch_tc_up(const __nv_bfloat16* A, const __nv_bfloat16* W_up, int6
     p.cs_cols = d;
     p.cs_out = colsum;
   }
-  p.splits = splitk_parts(T, d, kUpBN, p.kb1);
-  if (p.splits > 1 && (!slab || size_t(p.splits) * size_t(T) * size_t(d) > slab_floats))
-    p.splits = 1;  // no room for the parts: one K range per tile
+  p.splits = split ? splits : 1;  // no room for the parts: one K range per tile
   if (p.splits == 1) {
     CUtensorMap mu;
     if (!make_out_map(&mu, U, T, d, false)) return cudaErrorInvalidValue;
+    if (pairs) return launch_tc<kUpBN, 1, 6, false, false, true>(ma, ma, mb, mb, mu, p, stream);
     return launch_tc<kUpBN, 1, 4, false>(ma, ma, mb, mb, mu, p, stream);
   }
   p.slab = slab;
@@ -952,8 +1080,11 @@ cudaError_t launch_tc_mix(const __nv_bfloat16* U, const __nv_bfloat16* x,
   }
   const int parts = mix_parts(T, d);
   CUtensorMap mu, mx, mw;
+  const bool pairs = parts == 1 && use_pairs(T, d);
+  // the CTA-pair form loads half of a tile's W_mix rows per CTA
   if (!make_map(&mu, U, T, d, kBM) || !make_map(&mx, x, T, d, kBM) ||
-      !make_map(&mw, W_mix, d, 2 * int64_t(d), parts > 1 ? kMixSplitBN : kMixBN))
+      !make_map(&mw, W_mix, d, 2 * int64_t(d),
+                parts > 1 ? kMixSplitBN : (pairs ? kMixBN / 2 : kMixBN)))
     return cudaErrorInvalidValue;
   TcParams p{};
   p.M = int(T);
@@ -977,6 +1108,7 @@ cudaError_t launch_tc_mix(const __nv_bfloat16* U, const __nv_bfloat16* x,
   if (p.splits == 1) {
     CUtensorMap my;
     if (!make_out_map(&my, y, T, d, y_dtype != L3_BF16)) return cudaErrorInvalidValue;
+    if (pairs) return launch_tc<kMixBN, 2, 6, false, false, true>(mu, mx, mw, mw, my, p, stream);
     return launch_tc<kMixBN, 2, 4, false>(mu, mx, mw, mw, my, p, stream);
   }
   p.slab = slab;

@@ -4,6 +4,7 @@
 // tensor maps.
 #pragma once
 
+#include <cstring>
 #include <cudaTypedefs.h>
 
 #include "l3_internal.h"
@@ -53,15 +54,18 @@ __device__ __forceinline__ void mma8(float (&c)[4], uint32_t a0, uint32_t a1, ui
       : "r"(a0), "r"(a1), "r"(b0));
 }
 
+// Two floats rounded (to nearest even) to a bf16 pair, `lo` in the low half, by one paired
+// conversion (the scalar conversions run at a fraction of its rate).
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  return uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
-         (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  uint32_t r;
+  memcpy(&r, &h, sizeof(r));
+  return r;
 }
 // hi = bf16(v), lo = bf16(v - hi), packed in pairs (lower k in the low half).
 __device__ __forceinline__ void split_pair(float v0, float v1, uint32_t& hi, uint32_t& lo) {
-  const float h0 = __bfloat162float(__float2bfloat16_rn(v0));
-  const float h1 = __bfloat162float(__float2bfloat16_rn(v1));
-  hi = pack_bf16(h0, h1);
+  hi = pack_bf16(v0, v1);
+  const float h0 = __uint_as_float(hi << 16), h1 = __uint_as_float(hi & 0xffff0000u);
   lo = pack_bf16(v0 - h0, v1 - h1);
 }
 
