@@ -308,6 +308,34 @@ def test_forward_bf16_saved_state_and_layernorm_statistics(T):
     assert l3.l3_get_error(c.ws) == 0
 
 
+def test_tile_gemms_as_cta_pairs_every_token_and_column():
+    # 37900 tokens of the ragged-tile shapes (d = 320): 297 row tiles x 2 column tiles of
+    # 128 x 256 make four waves on 148 SMs, so GEMM-up and GEMM-mix run as CTA pairs. The
+    # last pair's second CTA holds no rows at all, and in the second column tile the second
+    # CTA's half of the weight rows lies wholly past d. Reference: the oracle's LayerNorm and
+    # fp64 products on the GPU's own a rounded to bf16 (the GEMMs' input), with U rounded to
+    # bf16 before the LayerNorm (reading "bf16 storage"), for every token and column.
+    c = Case(6, T=37900)
+    y, sv = c.forward(saved=True)
+    y32, _ = c.forward(y_dtype=torch.float32)
+    torch.cuda.synchronize()
+    a, _, mu, rstd = c.saved_views(sv)
+    a16 = to_np(a.to(torch.bfloat16))
+    u16 = to_np(torch.as_tensor(a16 @ to_np(c.W_up).T).to(torch.bfloat16))
+    ln = [oracle.layer_norm(u16[i], 1e-5) for i in range(c.T)]
+    h = np.stack([r[0] for r in ln])
+    y_ref = np.concatenate([h, to_np(c.x)], axis=1) @ to_np(c.W_mix).T
+    np.testing.assert_allclose(to_np(rstd), [r[2] for r in ln], rtol=2 * BF16_U)
+    np.testing.assert_allclose(to_np(mu), [r[1] for r in ln], rtol=0,
+                               atol=2 * BF16_U * np.abs(u16).max())
+    g, g32 = to_np(y), to_np(y32)
+    assert_close(c.p, g, y_ref, "y")
+    # bf16 output: each element rounded once (relative u); fp32 output: fp32 sums only
+    assert np.linalg.norm(g - y_ref) <= 2 * BF16_U * np.linalg.norm(y_ref)
+    assert np.linalg.norm(g32 - y_ref) <= 1e-3 * np.linalg.norm(y_ref)
+    assert l3.l3_get_error(c.ws) == 0
+
+
 def test_tensor_core_attend_one_long_segment_and_mixed_ranges():
     # 1400 tokens: 1100 of id 0 (512 rows: 4 row chunks, 18 token chunks) and ids with
     # few rows (partial 16-row boxes, single-token items)
