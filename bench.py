@@ -93,7 +93,6 @@ FP32_FMA_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
 # an entry is removed when its kernel changes, and the roofline then reports null.
 NCU_TRAFFIC = {
     ("prefill-bf16", "attend"): 206.20e6 + 1.06e6,     # attend_mma_kernel<16,8,2>
-    ("prefill-bf16", "attend_long"): 99.06e6 + 0.30e6,  # attend_tc_kernel
     ("prefill-bf16", "mix"): 38.34e6,                  # tc_gemm_kernel<256,2,4,0,0,0>
     ("prefill-bf16", "up"): 6.87e6,                    # tc_gemm_kernel<256,1,4,0,0,0>
     ("decode-bf16", "attend"): 85.23e6 + 0.12e6,       # attend_mma_kernel<8,16,4>

@@ -48,7 +48,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSCol = 0;    // Sᵀ chunk rc at columns 64 rc
 constexpr uint32_t kACol = 256;  // Aᵀ chunk dc at columns 256 + 64 dc
 constexpr int kSmemBytes =
-    kStages * kStageBytes + kXSlots * kXTile + kPBytes + 7 * kNT * 4 + 256 + 1024;
+    kStages * kStageBytes + kXSlots * kXTile + kPBytes + 8 * kNT * 4 + 256 + 1024;
 
 static_assert(kNT == kTcNT, "item size of the plan");
 using Item = AttendItem;
@@ -122,6 +122,23 @@ __device__ __forceinline__ void reduce_scatter32(float (&v)[32], int lane) {
   }
 }
 
+// 4-row gather of a 2-D tensor (box one row high, 64 columns): rows r0..r3 at column x land
+// as consecutive 128-byte rows of dst in the map's swizzle, completing 512 bytes on bar.
+__device__ __forceinline__ void tma_gather4(const CUtensorMap* map, uint64_t* bar, void* dst,
+                                            int32_t x, int32_t r0, int32_t r1, int32_t r2,
+                                            int32_t r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(tc::smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(tc::smem_u32(bar)), "r"(x), "r"(r0), "r"(r1),
+      "r"(r2), "r"(r3)
+      : "memory");
+}
+
+// GATHER: mapX views x itself (one-row boxes) and the item's x rows are gathered by batch
+// index with 4-row TMA gathers; otherwise mapX views a copy of the items' x rows in sorted
+// order (64-row boxes).
+template <bool GATHER>
 __global__ void __launch_bounds__(kThreads, 1)
     attend_tc_kernel(const __grid_constant__ CUtensorMap mapK,
                      const __grid_constant__ CUtensorMap mapX,
@@ -136,7 +153,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* fin_m = red + 4 * kNT;                              // [64]
   float* fin_l = fin_m + kNT;                                // [64]
   int32_t* orig = reinterpret_cast<int32_t*>(fin_l + kNT);  // [64]
-  uint64_t* full = reinterpret_cast<uint64_t*>(orig + kNT);
+  int32_t* xrow = orig + kNT;                                // [64] producer: x row per token
+  uint64_t* full = reinterpret_cast<uint64_t*>(xrow + kNT);
   uint64_t* empty = full + kStages;
   uint64_t* xfull = empty + kStages;
   uint64_t* xempty = xfull + kXSlots;
@@ -190,10 +208,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::tma_prefetch_desc(&mapK);
       tc::tma_prefetch_desc(&mapX);
       tc::tma_prefetch_desc(&mapV);
-      uint32_t it = 0, xt = 0;
-      bool ok = true;
-      for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
-        const Item item = p.items[i];
+    }
+    uint32_t it = 0, xt = 0;
+    bool ok = true;
+    for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
+      const Item item = p.items[i];
+      if (GATHER) {
+        // the batch index of each of the item's tokens (slots past nt repeat the first: read,
+        // then masked like the rows past a segment in the sorted copy)
+        for (int j = lane; j < kNT; j += 32)
+          xrow[j] = int32_t(uint32_t(p.sorted_keys[item.q0 + (j < item.nt ? j : 0)]));
+        __syncwarp();
+      }
+      if (lane == 0) {
         const int r0 = p.offs[item.t];
         const int n = p.offs[item.t + 1] - r0;
         const int RC = (n + 127) / 128;
@@ -205,7 +232,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             tc::mbar_arrive_expect_tx(&xfull[xs], uint32_t(kXTile));
-            tc::tma_load_2d(&mapX, &xfull[xs], xbuf + xs * kXTile, kb * 64, item.q0);
+            if (GATHER) {
+              unsigned char* xd = xbuf + xs * kXTile;
+#pragma unroll 4
+              for (int g = 0; g < kNT / 4; ++g)
+                tma_gather4(&mapX, &xfull[xs], xd + g * 512, kb * 64, xrow[4 * g],
+                            xrow[4 * g + 1], xrow[4 * g + 2], xrow[4 * g + 3]);
+            } else {
+              tc::tma_load_2d(&mapX, &xfull[xs], xbuf + xs * kXTile, kb * 64, item.q0);
+            }
           }
           for (int rc = 0; rc < RC; ++rc) {
             const uint32_t s = it % kStages, ph = (it / kStages) & 1;
@@ -237,6 +272,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      // lane 0's verdict for the whole warp; xrow is rewritten only after its copies issued
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      __syncwarp();
+    }
+    if (lane == 0) {
       if (!ok) {
         // Let the copies already issued land before the CTA's shared memory goes away.
         const uint32_t first = it > uint32_t(kStages) ? it - kStages : 0;
@@ -544,20 +584,25 @@ int attend_tc_threshold(int64_t T, int d, int d_v, int dtype) {
 
 cudaError_t launch_attend_tc(const AttendTcArgs& a, cudaStream_t stream) {
   if (a.T <= 0 || a.max_items <= 0) return cudaSuccess;
-  // the item count is on the device: enough CTAs for every unit of a typical batch, each
-  // walking the units by a stride beyond that
-  int64_t g_units = int64_t(a.max_items) * kGatherSplit;
-  const int64_t g_cap = int64_t(sm_count()) * 8;
-  cudaError_t e = launch_pdl(gather_rows_kernel, dim3(unsigned(g_units < g_cap ? g_units : g_cap)),
-                             dim3(256), 0,
-                             stream, a.items, a.hdr, a.sorted_keys,
-                             static_cast<const __nv_bfloat16*>(a.x), a.d, a.x_sorted);
-  count_launch();
-  if (e != cudaSuccess) return e;
-  const Item* items = a.items;
+  cudaError_t e = cudaSuccess;
   CUtensorMap mk, mx, mv;
-  if (!make_map(&mk, a.K, a.v, a.d, 128) || !make_map(&mx, a.x_sorted, a.T, a.d, kNT) ||
-      !make_map(&mv, a.V, a.v, a.d_v, 64))
+  // x itself in one-row boxes for the kernel's 4-row gathers (needs a 16-byte aligned x);
+  // otherwise the items' x rows are first copied in sorted order
+  const bool gather = make_map(&mx, a.x, a.T, a.d, 1);
+  if (!gather) {
+    // the item count is on the device: enough CTAs for every unit of a typical batch, each
+    // walking the units by a stride beyond that
+    int64_t g_units = int64_t(a.max_items) * kGatherSplit;
+    const int64_t g_cap = int64_t(sm_count()) * 8;
+    e = launch_pdl(gather_rows_kernel, dim3(unsigned(g_units < g_cap ? g_units : g_cap)),
+                   dim3(256), 0, stream, a.items, a.hdr, a.sorted_keys,
+                   static_cast<const __nv_bfloat16*>(a.x), a.d, a.x_sorted);
+    count_launch();
+    if (e != cudaSuccess) return e;
+    if (!make_map(&mx, a.x_sorted, a.T, a.d, kNT)) return cudaErrorInvalidValue;
+  }
+  const Item* items = a.items;
+  if (!make_map(&mk, a.K, a.v, a.d, 128) || !make_map(&mv, a.V, a.v, a.d_v, 64))
     return cudaErrorInvalidValue;
   TcAttendParams p{};
   p.items = items;
@@ -570,10 +615,11 @@ cudaError_t launch_attend_tc(const AttendTcArgs& a, cudaStream_t stream) {
   p.a_f32 = a.a_f32;
   p.ml = a.ml;
   p.st = a.st;
-  const cudaError_t attr = ensure_smem_attr(attend_tc_kernel, kSmemBytes);
+  auto kern = gather ? attend_tc_kernel<true> : attend_tc_kernel<false>;
+  const cudaError_t attr = ensure_smem_attr(kern, kSmemBytes);
   if (attr != cudaSuccess) return attr;
-  e = launch_pdl(attend_tc_kernel, dim3(sm_count()), dim3(kThreads), size_t(kSmemBytes), stream,
-                 mk, mx, mv, p);
+  e = launch_pdl(kern, dim3(sm_count()), dim3(kThreads), size_t(kSmemBytes), stream, mk, mx, mv,
+                 p);
   count_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
 }
