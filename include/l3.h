@@ -210,10 +210,12 @@ l3_status l3_route_noalloc(const l3_layer* layer, const int32_t* ids, int64_t T,
  *   s = K_t x_i (t = ids[i]); p = softmax(s) (no temperature); a_i = V_tᵀ p;
  *   u_i = W_up a_i; h_i = LayerNorm(u_i); y_i = W_mix [h_i; x_i].
  *   ids   [T]    int32 (device)
- *   x     [T, d] layer dtype
- *   y     [T, d] y_dtype (L3_F32, or the layer dtype)
+ *   x     [T, d] layer dtype, 16-byte aligned
+ *   y     [T, d] y_dtype (L3_F32, or the layer dtype), 16-byte aligned
  *   saved nullable; if given, l3_saved_size(layer, T) bytes that l3_backward reads
  *   ws    >= l3_workspace_size(layer, T, L3_PASS_FORWARD) bytes
+ * x and y rows are moved by TMA tensor copies, whose global addresses must be 16-byte
+ * aligned; a misaligned x or y returns L3_ERR_INVALID_ARG.
  * T may be 0 (nothing is enqueued). Errors: L3_ERR_INVALID_ARG, L3_ERR_UNSUPPORTED,
  * L3_ERR_WORKSPACE, L3_ERR_CUDA; token ids out of range are reported by l3_get_error.
  */

@@ -81,7 +81,6 @@ struct FwdWs {
   uint32_t* sync;  // arrival counters, zeroed with the status words
   float *q_stats, *q_slab;
   // tensor-core gather-attend of the long segments
-  __nv_bfloat16* x_sorted;
   int tc_th;      // segments with at least this many tokens go to tensor cores (0: none)
   int max_items;  // bound on their item count
 };
@@ -110,7 +109,6 @@ FwdWs carve_fwd(Carve& c, const l3_layer* L, int64_t T) {
   if (w.tc_th > 0) {
     w.max_items = int(T / w.tc_th + 1);
     w.items = c.take<AttendItem>(size_t(w.max_items));
-    w.x_sorted = c.take<__nv_bfloat16>(t * d);
   }
   if (L->dtype == L3_BF16) {
     w.a_bf16 = c.take<__nv_bfloat16>(t * dv);
@@ -261,6 +259,9 @@ l3_status forward_impl(const l3_layer* L, const int32_t* ids, int64_t T, const v
   if (T < 0 || T >= (int64_t(1) << 31)) return L3_ERR_INVALID_ARG;
   if (!(y_dtype == L3_F32 || y_dtype == L->dtype)) return L3_ERR_INVALID_ARG;
   if (T > 0 && (!ids || !x || !y || !ws)) return L3_ERR_INVALID_ARG;
+  // x and y rows move through TMA tensor copies, whose global addresses are 16-byte aligned
+  if (((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15) != 0)
+    return L3_ERR_INVALID_ARG;
   if (ws_bytes < l3_workspace_size(L, T, L3_PASS_FORWARD)) return L3_ERR_WORKSPACE;
   if (T == 0) return L3_OK;
 
@@ -335,7 +336,6 @@ l3_status forward_impl(const l3_layer* L, const int32_t* ids, int64_t T, const v
     at.v = L->v;
     at.d = d;
     at.d_v = dv;
-    at.x_sorted = w.x_sorted;
     at.a_bf16 = w.a_bf16;
     at.a_f32 = a_copy;
     at.ml = ml;

@@ -13,9 +13,10 @@
 //   phase 2   Aᵀ = V_tᵀ Pᵀ           M = 128 value columns per chunk, N tokens, K = rows
 //                                    in 16-row steps (both operands MN-major).
 //   epilogue  a = Aᵀ / l, scattered to batch order (bf16 for the GEMM, fp32 if asked).
-// K_t rows arrive by TMA in 128-row boxes, V_t rows in 64-row boxes and x in 64-token
-// boxes (rows past an item's range are read and masked): few large copies per stage, since
-// each TMA instruction costs tens of nanoseconds to issue.
+// K_t rows arrive by TMA in 128-row boxes and V_t rows in 64-row boxes (rows past an item's
+// range are read and masked): few large copies per stage, since each TMA instruction costs
+// tens of nanoseconds to issue. The item's x rows come straight from x, 64 columns of four
+// tokens per 4-row TMA gather (the producer warp looks up the tokens' batch indices).
 // Phase 1 walks the 64-wide K blocks outermost: an x block is copied once into its own
 // small ring and serves all row chunks of the item (released after the last chunk's MMAs),
 // so the K ring holds only K boxes and more bytes are in flight.
@@ -124,6 +125,7 @@ __device__ __forceinline__ void reduce_scatter32(float (&v)[32], int lane) {
 
 // 4-row gather of a 2-D tensor (box one row high, 64 columns): rows r0..r3 at column x land
 // as consecutive 128-byte rows of dst in the map's swizzle, completing 512 bytes on bar.
+// dst must lie in a 1024-byte aligned tile (the swizzle follows the shared address).
 __device__ __forceinline__ void tma_gather4(const CUtensorMap* map, uint64_t* bar, void* dst,
                                             int32_t x, int32_t r0, int32_t r1, int32_t r2,
                                             int32_t r3) {
@@ -135,10 +137,7 @@ __device__ __forceinline__ void tma_gather4(const CUtensorMap* map, uint64_t* ba
       : "memory");
 }
 
-// GATHER: mapX views x itself (one-row boxes) and the item's x rows are gathered by batch
-// index with 4-row TMA gathers; otherwise mapX views a copy of the items' x rows in sorted
-// order (64-row boxes).
-template <bool GATHER>
+// mapX views x in one-row boxes (for the 4-row gathers).
 __global__ void __launch_bounds__(kThreads, 1)
     attend_tc_kernel(const __grid_constant__ CUtensorMap mapK,
                      const __grid_constant__ CUtensorMap mapX,
@@ -213,13 +212,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
       const Item item = p.items[i];
-      if (GATHER) {
-        // the batch index of each of the item's tokens (slots past nt repeat the first: read,
-        // then masked like the rows past a segment in the sorted copy)
-        for (int j = lane; j < kNT; j += 32)
-          xrow[j] = int32_t(uint32_t(p.sorted_keys[item.q0 + (j < item.nt ? j : 0)]));
-        __syncwarp();
-      }
+      // the batch index of each of the item's tokens (slots past nt repeat the first: read,
+      // then masked as the softmax masks token columns past nt)
+      for (int j = lane; j < kNT; j += 32)
+        xrow[j] = int32_t(uint32_t(p.sorted_keys[item.q0 + (j < item.nt ? j : 0)]));
+      __syncwarp();
       if (lane == 0) {
         const int r0 = p.offs[item.t];
         const int n = p.offs[item.t + 1] - r0;
@@ -232,15 +229,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             tc::mbar_arrive_expect_tx(&xfull[xs], uint32_t(kXTile));
-            if (GATHER) {
-              unsigned char* xd = xbuf + xs * kXTile;
+            unsigned char* xd = xbuf + xs * kXTile;
 #pragma unroll 4
-              for (int g = 0; g < kNT / 4; ++g)
-                tma_gather4(&mapX, &xfull[xs], xd + g * 512, kb * 64, xrow[4 * g],
-                            xrow[4 * g + 1], xrow[4 * g + 2], xrow[4 * g + 3]);
-            } else {
-              tc::tma_load_2d(&mapX, &xfull[xs], xbuf + xs * kXTile, kb * 64, item.q0);
-            }
+            for (int g = 0; g < kNT / 4; ++g)
+              tma_gather4(&mapX, &xfull[xs], xd + g * 512, kb * 64, xrow[4 * g],
+                          xrow[4 * g + 1], xrow[4 * g + 2], xrow[4 * g + 3]);
           }
           for (int rc = 0; rc < RC; ++rc) {
             const uint32_t s = it % kStages, ph = (it / kStages) & 1;
@@ -501,49 +494,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// x_sorted[q] = x[perm(q)] (bf16 rows of d elements) for the tokens of the items, in units
-// of a quarter item (up to 16 tokens) per CTA: the batch indices first, then all the rows'
-// 16-byte pieces spread over the threads, eight loads in flight per thread.
-constexpr int kGatherSplit = 4;
-__global__ void gather_rows_kernel(const Item* __restrict__ items, const int32_t* __restrict__ hdr,
-                                   const uint64_t* __restrict__ keys,
-                                   const __nv_bfloat16* __restrict__ x, int d,
-                                   __nv_bfloat16* __restrict__ xs) {
-  grid_dep_wait();
-  grid_dep_release();
-  constexpr int kPart = kNT / kGatherSplit;
-  __shared__ int32_t row_of[kPart];
-  const int units = hdr[kPlanItems] * kGatherSplit;
-  const int pieces = d / 8;  // 16-byte pieces per row
-  for (int unit = blockIdx.x; unit < units; unit += gridDim.x) {
-    const Item it0 = items[unit / kGatherSplit];
-    const int j0 = (unit % kGatherSplit) * kPart;  // tokens j0 .. j0 + nt - 1 of the item
-    if (j0 >= it0.nt) continue;
-    const int64_t q0 = int64_t(it0.q0) + j0;
-    const int nt = it0.nt - j0 < kPart ? it0.nt - j0 : kPart;
-    __syncthreads();  // row_of of the previous unit is no longer read
-    if (int(threadIdx.x) < nt) row_of[threadIdx.x] = int32_t(uint32_t(keys[q0 + threadIdx.x]));
-    __syncthreads();
-    const int total = nt * pieces;
-    for (int base = threadIdx.x; base < total; base += 8 * blockDim.x) {
-      uint4 v[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int idx = base + u * int(blockDim.x);
-        if (idx < total)
-          v[u] = __ldg(reinterpret_cast<const uint4*>(x + int64_t(row_of[idx / pieces]) * d) +
-                       idx % pieces);
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int idx = base + u * int(blockDim.x);
-        if (idx < total)
-          reinterpret_cast<uint4*>(xs + (q0 + idx / pieces) * d)[idx % pieces] = v[u];
-      }
-    }
-  }
-}
-
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -584,26 +534,12 @@ int attend_tc_threshold(int64_t T, int d, int d_v, int dtype) {
 
 cudaError_t launch_attend_tc(const AttendTcArgs& a, cudaStream_t stream) {
   if (a.T <= 0 || a.max_items <= 0) return cudaSuccess;
-  cudaError_t e = cudaSuccess;
   CUtensorMap mk, mx, mv;
-  // x itself in one-row boxes for the kernel's 4-row gathers (needs a 16-byte aligned x);
-  // otherwise the items' x rows are first copied in sorted order
-  const bool gather = make_map(&mx, a.x, a.T, a.d, 1);
-  if (!gather) {
-    // the item count is on the device: enough CTAs for every unit of a typical batch, each
-    // walking the units by a stride beyond that
-    int64_t g_units = int64_t(a.max_items) * kGatherSplit;
-    const int64_t g_cap = int64_t(sm_count()) * 8;
-    e = launch_pdl(gather_rows_kernel, dim3(unsigned(g_units < g_cap ? g_units : g_cap)),
-                   dim3(256), 0, stream, a.items, a.hdr, a.sorted_keys,
-                   static_cast<const __nv_bfloat16*>(a.x), a.d, a.x_sorted);
-    count_launch();
-    if (e != cudaSuccess) return e;
-    if (!make_map(&mx, a.x_sorted, a.T, a.d, kNT)) return cudaErrorInvalidValue;
-  }
-  const Item* items = a.items;
-  if (!make_map(&mk, a.K, a.v, a.d, 128) || !make_map(&mv, a.V, a.v, a.d_v, 64))
+  // x in one-row boxes for the kernel's 4-row gathers (x is 16-byte aligned)
+  if (!make_map(&mk, a.K, a.v, a.d, 128) || !make_map(&mx, a.x, a.T, a.d, 1) ||
+      !make_map(&mv, a.V, a.v, a.d_v, 64))
     return cudaErrorInvalidValue;
+  const Item* items = a.items;
   TcAttendParams p{};
   p.items = items;
   p.n_items = a.hdr + kPlanItems;
@@ -615,11 +551,10 @@ cudaError_t launch_attend_tc(const AttendTcArgs& a, cudaStream_t stream) {
   p.a_f32 = a.a_f32;
   p.ml = a.ml;
   p.st = a.st;
-  auto kern = gather ? attend_tc_kernel<true> : attend_tc_kernel<false>;
-  const cudaError_t attr = ensure_smem_attr(kern, kSmemBytes);
+  const cudaError_t attr = ensure_smem_attr(attend_tc_kernel, kSmemBytes);
   if (attr != cudaSuccess) return attr;
-  e = launch_pdl(kern, dim3(sm_count()), dim3(kThreads), size_t(kSmemBytes), stream, mk, mx, mv,
-                 p);
+  const cudaError_t e = launch_pdl(attend_tc_kernel, dim3(sm_count()), dim3(kThreads),
+                                   size_t(kSmemBytes), stream, mk, mx, mv, p);
   count_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
 }

@@ -135,11 +135,10 @@ struct AttendTcArgs {
   const int32_t* offs;
   const void* K;
   const void* V;
-  const void* x;
+  const void* x;             // [T, d] bf16, 16-byte aligned (gathered by TMA)
   int64_t v;
   int d, d_v;
-  int max_items;            // upper bound of the item count (grid of the x gather)
-  __nv_bfloat16* x_sorted;  // [T, d] scratch: rows of the items' tokens in sorted order
+  int max_items;            // upper bound of the item count (0: no items)
   __nv_bfloat16* a_bf16;    // [T, d_v]
   float* a_f32;             // nullable
   float* ml;                // nullable

@@ -114,6 +114,9 @@ def test_forward_argument_errors(lib):
     assert lib.l3_forward(ctypes.byref(L), None, 128, 0x20, 0x30, 1, None, 0x40, 1 << 30, None) == 1
     assert lib.l3_forward(ctypes.byref(L), 0x10, 128, None, 0x30, 1, None, 0x40, 1 << 30, None) == 1
     assert lib.l3_forward(ctypes.byref(L), 0x10, -1, 0x20, 0x30, 1, None, 0x40, 1 << 30, None) == 1
+    # x or y not 16-byte aligned (their rows move by TMA tensor copies)
+    assert lib.l3_forward(ctypes.byref(L), 0x10, 128, 0x28, 0x30, 1, None, 0x40, 1 << 30, None) == 1
+    assert lib.l3_forward(ctypes.byref(L), 0x10, 128, 0x20, 0x34, 1, None, 0x40, 1 << 30, None) == 1
     # T = 0 is a no-op
     assert lib.l3_forward(ctypes.byref(L), None, 0, None, None, 1, None, None, 1 << 30, None) == 0
     # backward needs saved state and outputs
