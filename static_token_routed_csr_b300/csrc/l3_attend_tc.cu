@@ -20,8 +20,9 @@
 // Phase 1 walks the 64-wide K blocks outermost: an x block is copied once into its own
 // small ring and serves all row chunks of the item (released after the last chunk's MMAs),
 // so the K ring holds only K boxes and more bytes are in flight.
-// One persistent CTA per SM, 10 warps: TMA producer, MMA issuer, 8 softmax/epilogue warps
-// (two per TMEM lane quarter, each taking 32 of the item's 64 token columns). All waits
+// One persistent CTA per SM, 11 warps: the K / V producer, the MMA issuer, 8 softmax/epilogue
+// warps (two per TMEM lane quarter, each taking 32 of the item's 64 token columns) and the
+// x producer, whose 4-row gathers (16 per x box) would otherwise delay the K stream. All waits
 // are bounded; the softmax warps synchronise on an mbarrier (bounded) rather than a named
 // barrier, so no thread can be left waiting.
 #include <cstring>
@@ -36,7 +37,7 @@ namespace l3 {
 
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kSoftWarps = 8;  // warps 2 .. 9
 constexpr int kNT = 64;            // tokens per item
 constexpr int kStages = 8;         // K / V ring (16 KB stages)
@@ -207,34 +208,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::tma_prefetch_desc(&mapK);
       tc::tma_prefetch_desc(&mapX);
       tc::tma_prefetch_desc(&mapV);
-    }
-    uint32_t it = 0, xt = 0;
-    bool ok = true;
-    for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
-      const Item item = p.items[i];
-      // the batch index of each of the item's tokens (slots past nt repeat the first: read,
-      // then masked as the softmax masks token columns past nt)
-      for (int j = lane; j < kNT; j += 32)
-        xrow[j] = int32_t(uint32_t(p.sorted_keys[item.q0 + (j < item.nt ? j : 0)]));
-      __syncwarp();
-      if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
+        const Item item = p.items[i];
         const int r0 = p.offs[item.t];
         const int n = p.offs[item.t + 1] - r0;
         const int RC = (n + 127) / 128;
-        for (int kb = 0; ok && kb < KB; ++kb, ++xt) {
-          {
-            const uint32_t xs = xt % kXSlots, xph = (xt / kXSlots) & 1;
-            if (!tc::mbar_wait(&xempty[xs], xph ^ 1, abort_flag, p.st, 0x100)) {
-              ok = false;
-              break;
-            }
-            tc::mbar_arrive_expect_tx(&xfull[xs], uint32_t(kXTile));
-            unsigned char* xd = xbuf + xs * kXTile;
-#pragma unroll 4
-            for (int g = 0; g < kNT / 4; ++g)
-              tma_gather4(&mapX, &xfull[xs], xd + g * 512, kb * 64, xrow[4 * g],
-                          xrow[4 * g + 1], xrow[4 * g + 2], xrow[4 * g + 3]);
-          }
+        for (int kb = 0; ok && kb < KB; ++kb) {
           for (int rc = 0; rc < RC; ++rc) {
             const uint32_t s = it % kStages, ph = (it / kStages) & 1;
             if (!tc::mbar_wait(&empty[s], ph ^ 1, abort_flag, p.st, 0x100)) {
@@ -265,11 +246,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      // lane 0's verdict for the whole warp; xrow is rewritten only after its copies issued
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      __syncwarp();
-    }
-    if (lane == 0) {
       if (!ok) {
         // Let the copies already issued land before the CTA's shared memory goes away.
         const uint32_t first = it > uint32_t(kStages) ? it - kStages : 0;
@@ -277,10 +253,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (uint32_t j = first; j < it; ++j)
           tc::mbar_wait(&full[j % kStages], (j / kStages) & 1, &no_abort, p.st, 0x1000,
                         100000000ull);
-        for (uint32_t j = xt > uint32_t(kXSlots) ? xt - kXSlots : 0; j < xt; ++j)
-          tc::mbar_wait(&xfull[j % kXSlots], (j / kXSlots) & 1, &no_abort, p.st, 0x1000,
-                        100000000ull);
       }
+    }
+  } else if (warp == 2 + kSoftWarps) {
+    // x producer: per item, the tokens' batch indices (slots past nt repeat the first: read,
+    // then masked as the softmax masks token columns past nt), then per 64-wide K block one x
+    // box of 16 four-row gathers
+    uint32_t xt = 0;
+    bool ok = true;
+    for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
+      const Item item = p.items[i];
+      for (int j = lane; j < kNT; j += 32)
+        xrow[j] = int32_t(uint32_t(p.sorted_keys[item.q0 + (j < item.nt ? j : 0)]));
+      __syncwarp();
+      if (lane == 0) {
+        for (int kb = 0; kb < KB; ++kb, ++xt) {
+          const uint32_t xs = xt % kXSlots, xph = (xt / kXSlots) & 1;
+          if (!tc::mbar_wait(&xempty[xs], xph ^ 1, abort_flag, p.st, 0x100)) {
+            ok = false;
+            break;
+          }
+          tc::mbar_arrive_expect_tx(&xfull[xs], uint32_t(kXTile));
+          unsigned char* xd = xbuf + xs * kXTile;
+#pragma unroll 4
+          for (int g = 0; g < kNT / 4; ++g)
+            tma_gather4(&mapX, &xfull[xs], xd + g * 512, kb * 64, xrow[4 * g],
+                        xrow[4 * g + 1], xrow[4 * g + 2], xrow[4 * g + 3]);
+        }
+      }
+      // lane 0's verdict for the whole warp; xrow is rewritten only after its copies issued
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      __syncwarp();
+    }
+    if (lane == 0 && !ok) {
+      volatile int no_abort = 0;
+      for (uint32_t j = xt > uint32_t(kXSlots) ? xt - kXSlots : 0; j < xt; ++j)
+        tc::mbar_wait(&xfull[j % kXSlots], (j / kXSlots) & 1, &no_abort, p.st, 0x1000,
+                      100000000ull);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -355,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       volatile int no_abort = 0;
       tc::mbar_wait(drain, 0, &no_abort, p.st, 0x2000, 100000000ull);
     }
-  } else {
+  } else if (warp < 2 + kSoftWarps) {
     // softmax / epilogue warp (q, h): TMEM lane quarter q (hardware rule: warp % 4), token
     // columns [32 h, 32 h + 32) of the item
     const int q = warp & 3;
