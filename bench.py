@@ -92,9 +92,9 @@ FP32_FMA_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
 # kernel, from one ncu capture of the current kernel code on that workload (cold cache);
 # an entry is removed when its kernel changes, and the roofline then reports null.
 NCU_TRAFFIC = {
-    ("prefill-bf16", "attend"): 206.20e6 + 1.03e6,     # attend_mma_kernel<16,8,2>
-    ("prefill-bf16", "attend_long"): 98.56e6 + 0.30e6,  # attend_tc_kernel
-    ("prefill-bf16", "mix"): 38.34e6,                  # tc_gemm_kernel<256,2,4,0,0,0>
+    ("prefill-bf16", "attend"): 206.20e6 + 1.13e6,     # attend_mma_kernel<16,8,2>
+    ("prefill-bf16", "attend_long"): 98.56e6 + 0.26e6,  # attend_tc_kernel
+    ("prefill-bf16", "mix"): 38.34e6 + 0.01e6,         # tc_gemm_kernel<256,2,4,0,0,0>
     ("prefill-bf16", "up"): 6.87e6,                    # tc_gemm_kernel<256,1,4,0,0,0>
     ("decode-bf16", "attend"): 85.23e6 + 0.12e6,       # attend_mma_kernel<8,16,4>
 }
@@ -103,7 +103,7 @@ NCU_TRAFFIC = {
 # batch). The full-size traffic is the captured bytes scaled by the ratio of algorithmic
 # bytes (the rows read grow with the distinct ids the batch touches).
 NCU_TRAFFIC_SCALED = {
-    ("large-prefill-bf16", "attend"): (1167.81e6 + 6.14e6, 1109.75488e6,
+    ("large-prefill-bf16", "attend"): (1167.82e6 + 6.12e6, 1109.75488e6,
                                        "table rows 1048576, T 16384"),
 }
 
