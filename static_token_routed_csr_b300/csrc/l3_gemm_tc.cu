@@ -17,8 +17,11 @@
 // tcgen05.mma (M = 128, N = BN, K = 16 per instruction) into a TMEM accumulator (double-
 // buffered where two fit in the 512 columns); warps 2..9 drain TMEM (tcgen05.ld) and run the
 // epilogue while the next tile accumulates, two warps per 32-lane quarter, one per half of
-// the columns (the split and transposed forms use warps 2..5 only). Every mbarrier wait is bounded: a wait that runs out sets a status
-// word, the CTA drains its copies and MMAs in flight, frees TMEM and returns.
+// the columns (the split and transposed forms use warps 2..5 only). The plain forms store
+// their outputs through shared memory with TMA tensor stores, and with four or more waves of
+// tiles run as CTA pairs (one cta_group::2 MMA of M = 256 per pair). Every mbarrier wait is
+// bounded: a wait that runs out sets a status word, the CTA drains its copies and MMAs in
+// flight, frees TMEM and returns.
 #include <cudaTypedefs.h>
 
 #include <cstring>
