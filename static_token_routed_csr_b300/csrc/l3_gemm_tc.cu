@@ -696,7 +696,14 @@ cudaError_t launch_pairs(K* kern, int units, int smem, cudaStream_t stream, Args
   at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
-  static int max_pairs = 0;  // per kernel instantiation
+  // co-resident pairs, per kernel instantiation and device (a race only repeats the query)
+  constexpr int kDevs = 64;
+  static int max_pairs_of[kDevs];
+  int dev = 0;
+  const cudaError_t ed = cudaGetDevice(&dev);
+  if (ed != cudaSuccess) return ed;
+  if (dev < 0 || dev >= kDevs) return cudaErrorInvalidDevice;
+  int max_pairs = __atomic_load_n(&max_pairs_of[dev], __ATOMIC_RELAXED);
   if (max_pairs == 0) {
     cfg.gridDim = dim3(2 * (num_sms() / 2));
     cfg.numAttrs = 1;
@@ -704,6 +711,7 @@ cudaError_t launch_pairs(K* kern, int units, int smem, cudaStream_t stream, Args
     const cudaError_t q = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
     if (q != cudaSuccess) return q;
     if (n < 1) return cudaErrorInvalidConfiguration;
+    __atomic_store_n(&max_pairs_of[dev], n, __ATOMIC_RELAXED);
     max_pairs = n;
   }
   const int pairs = units < max_pairs ? units : max_pairs;
